@@ -1,0 +1,274 @@
+"""fp64 oracle: exact attention written out from its definition.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring). Section names cite the
+page "FlashAttention：快速且内存高效的准确注意力机制" (cloud.tencent.com.cn).
+
+Definitions used (the page's notation where it has one):
+
+* Scores (section "使用示例"): S = Q·Kᵀ·softmax_scale, default scale
+  1/sqrt(headdim) (section "参数说明").
+* Causal mask (section "2.1：更改causal标志的行为"): aligned to the
+  bottom-right corner of the Sq x Sk score matrix, so query row i may attend
+  key j iff j <= i + Sk - Sq. We call c(i) = i + Sk - Sq the diagonal key of row i.
+* Sliding window (sections "参数说明" and "2.3：局部（即滑动窗口）注意力"):
+  window_size = (left, right), -1 meaning unbounded on that side. Reading
+  taken here: the window is centred on the same diagonal c(i), keys
+  j in [c(i) - left, c(i) + right], inclusive; causal=True sets right = 0.
+* ALiBi (sections "参数说明" and "2.4"): bias -slope * |i - j| added to the
+  score; reading taken here: the distance is measured from the diagonal,
+  |c(i) - j|, which equals |i - j| when Sq == Sk, and the bias is not
+  multiplied by softmax_scale.
+* Masked entries are -inf (exact), not the -10000 of the page's naive
+  SelfAttention. A row with no live key gives O = 0 (section "2.1", last
+  sentence) and, by the logsumexp of an empty set, L = -inf.
+* L is the natural-log row logsumexp of S, the only statistic the backward
+  uses (sections "前向传播" and "反向传播").
+* Backward: the textbook derivative of softmax with the same P
+  (dV = PᵀdO, dP = dO·Vᵀ, D_i = sum_j P_ij dP_ij, dS = P∘(dP - D),
+  dQ = scale·dS·K, dK = scale·dSᵀ·Q).
+* Split-KV decode (section "2.2：针对推理进行优化"): each split computes
+  attention over its key range; a separate step merges them. Merge used here
+  is the exact logsumexp merge: L = log sum_s exp(L_s), O = sum_s exp(L_s - L) O_s.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+NEG_INF = -np.inf
+
+
+def _window(causal: bool, window_left: int, window_right: int):
+    """Return (left, right) after folding causal in; -1 = unbounded."""
+    wl = int(window_left)
+    wr = int(window_right)
+    if causal:
+        wr = 0
+    return wl, wr
+
+
+def live_mask(Sq: int, Sk: int, causal: bool = False, window_left: int = -1,
+              window_right: int = -1) -> np.ndarray:
+    """Boolean (Sq, Sk) matrix: True where query row i may attend key j.
+
+    Bottom-right alignment (section "2.1：更改causal标志的行为"): c(i) = i + Sk - Sq.
+    """
+    wl, wr = _window(causal, window_left, window_right)
+    i = np.arange(Sq)[:, None]
+    j = np.arange(Sk)[None, :]
+    c = i + (Sk - Sq)
+    live = np.ones((Sq, Sk), dtype=bool)
+    if wr >= 0:
+        live &= j <= c + wr
+    if wl >= 0:
+        live &= j >= c - wl
+    return live
+
+
+def alibi_bias(Sq: int, Sk: int, slope: float) -> np.ndarray:
+    """(Sq, Sk) fp64 ALiBi bias -slope * |c(i) - j| (section "参数说明", alibi_slopes)."""
+    i = np.arange(Sq)[:, None]
+    j = np.arange(Sk)[None, :]
+    c = i + (Sk - Sq)
+    return -float(slope) * np.abs(c - j).astype(np.float64)
+
+
+def _scores(qh, kh, scale, causal, wl, wr, slope, rows=None, Sq=None):
+    """Materialise S for one head: scale * q k^T (+ bias), -inf where masked.
+
+    ``rows`` (optional) selects query rows; each row is independent.
+    """
+    Sq_full = qh.shape[0] if Sq is None else Sq
+    Sk = kh.shape[0]
+    live = live_mask(Sq_full, Sk, causal, wl, wr)
+    if rows is not None:
+        live = live[rows]
+        qh = qh[rows]
+    s = (qh @ kh.T) * scale
+    if slope is not None:
+        b = alibi_bias(Sq_full, Sk, slope)
+        if rows is not None:
+            b = b[rows]
+        s = s + b
+    s = np.where(live, s, NEG_INF)
+    return s, live
+
+
+def _softmax_rows(s: np.ndarray):
+    """Row softmax and natural-log logsumexp; a row that is all -inf gives P = 0, L = -inf."""
+    m = np.max(s, axis=1, keepdims=True)
+    any_live = np.isfinite(m)
+    m_safe = np.where(any_live, m, 0.0)
+    e = np.exp(s - m_safe)  # exp(-inf) = 0 on masked entries
+    z = np.sum(e, axis=1, keepdims=True)
+    p = np.where(any_live, e / np.where(any_live, z, 1.0), 0.0)
+    with np.errstate(divide="ignore"):
+        lse = np.where(any_live, m_safe + np.log(np.where(any_live, z, 1.0)), NEG_INF)
+    return p, lse[:, 0]
+
+
+def head_fwd(qh, kh, vh, scale, causal=False, window_left=-1, window_right=-1,
+             slope=None, rows=None, return_p=False):
+    """Forward for one (batch, head): q (Sq,D), k/v (Sk,D) fp64 -> O (Sq,D), L (Sq,).
+
+    O_i = sum_j P_ij V_j with P = softmax(S) row-wise (section "使用示例");
+    rows with no live key give O = 0 and L = -inf (section "2.1").
+    """
+    qh = np.asarray(qh, dtype=np.float64)
+    kh = np.asarray(kh, dtype=np.float64)
+    vh = np.asarray(vh, dtype=np.float64)
+    s, _ = _scores(qh, kh, scale, causal, window_left, window_right, slope, rows=rows)
+    p, lse = _softmax_rows(s)
+    o = p @ vh
+    if return_p:
+        return o, lse, s, p
+    return o, lse
+
+
+def head_bwd(doh, qh, kh, vh, scale, causal=False, window_left=-1, window_right=-1,
+             slope=None, row_block=None):
+    """Backward for one (batch, head) by the textbook softmax derivative.
+
+    P is recomputed from the definition (the page's backward keeps only L,
+    section "反向传播"; here P is simply rebuilt from S). ``row_block``
+    bounds memory on long heads: dK and dV are then sums over row blocks of
+    the same products.
+    """
+    doh = np.asarray(doh, dtype=np.float64)
+    qh = np.asarray(qh, dtype=np.float64)
+    kh = np.asarray(kh, dtype=np.float64)
+    vh = np.asarray(vh, dtype=np.float64)
+    Sq = qh.shape[0]
+    rb = Sq if row_block is None else int(row_block)
+    dq = np.zeros_like(qh)
+    dk = np.zeros_like(kh)
+    dv = np.zeros_like(vh)
+    for r0 in range(0, Sq, rb):
+        rows = np.arange(r0, min(Sq, r0 + rb))
+        s, _ = _scores(qh, kh, scale, causal, window_left, window_right, slope,
+                       rows=rows, Sq=Sq)
+        p, _ = _softmax_rows(s)
+        do_r = doh[rows]
+        dv += p.T @ do_r
+        dp = do_r @ vh.T
+        d = np.sum(p * dp, axis=1, keepdims=True)
+        ds = p * (dp - d)
+        dq[rows] = scale * (ds @ kh)
+        dk += scale * (ds.T @ qh[rows])
+    return dq, dk, dv
+
+
+def head_partial(qh, kh, vh, key_lo, key_hi, scale, causal=False, window_left=-1,
+                 window_right=-1, slope=None):
+    """One split of split-KV decode (section "2.2"): attention of q over keys [key_lo, key_hi).
+
+    The mask and bias use the global key index. Returns the split's own
+    normalised output O_s (Sq,D) and logsumexp L_s (Sq,); a split with no
+    live key gives O_s = 0, L_s = -inf.
+    """
+    qh = np.asarray(qh, dtype=np.float64)
+    Sq = qh.shape[0]
+    Sk = kh.shape[0]
+    s, _ = _scores(qh, np.asarray(kh, dtype=np.float64), scale, causal, window_left,
+                   window_right, slope, Sq=Sq)
+    keep = np.zeros(Sk, dtype=bool)
+    keep[key_lo:key_hi] = True
+    s = np.where(keep[None, :], s, NEG_INF)
+    p, lse = _softmax_rows(s)
+    return p @ np.asarray(vh, dtype=np.float64), lse
+
+
+def combine_partials(o_parts, l_parts):
+    """Exact merge of split results: L = log sum_s exp(L_s); O = sum_s exp(L_s - L) O_s.
+
+    o_parts: (n, Sq, D); l_parts: (n, Sq). Splits with L_s = -inf weigh 0;
+    if every split is empty the row gives O = 0, L = -inf.
+    """
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    l_parts = np.asarray(l_parts, dtype=np.float64)
+    m = np.max(l_parts, axis=0)
+    any_live = np.isfinite(m)
+    m_safe = np.where(any_live, m, 0.0)
+    w = np.exp(l_parts - m_safe[None, :])
+    z = np.sum(w, axis=0)
+    with np.errstate(divide="ignore"):
+        lse = np.where(any_live, m_safe + np.log(np.where(any_live, z, 1.0)), NEG_INF)
+    wn = np.where(any_live[None, :], w / np.where(any_live, z, 1.0)[None, :], 0.0)
+    o = np.einsum("sq,sqd->qd", wn, o_parts)
+    return o, lse
+
+
+def _slope_for(alibi_slopes, b, h):
+    if alibi_slopes is None:
+        return None
+    a = np.asarray(alibi_slopes, dtype=np.float64)
+    return float(a[h]) if a.ndim == 1 else float(a[b, h])
+
+
+def _default_scale(D, scale):
+    return 1.0 / math.sqrt(D) if (scale is None or scale <= 0) else float(scale)
+
+
+def attention_fwd(q, k, v, scale=None, causal=False, window=(-1, -1), alibi_slopes=None):
+    """Batched forward: q (B,Sq,H,D), k/v (B,Sk,H,D) -> O (B,Sq,H,D), L (B,H,Sq), all fp64."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, Sq, H, D = q.shape
+    sc = _default_scale(D, scale)
+    o = np.zeros_like(q)
+    lse = np.zeros((B, H, Sq))
+    for b in range(B):
+        for h in range(H):
+            o[b, :, h, :], lse[b, h] = head_fwd(
+                q[b, :, h, :], k[b, :, h, :], v[b, :, h, :], sc, causal, window[0],
+                window[1], _slope_for(alibi_slopes, b, h))
+    return o, lse
+
+
+def attention_bwd(dout, q, k, v, scale=None, causal=False, window=(-1, -1), alibi_slopes=None):
+    """Batched backward: returns dQ, dK, dV in the layouts of q, k, v (fp64)."""
+    dout = np.asarray(dout, dtype=np.float64)
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, Sq, H, D = q.shape
+    sc = _default_scale(D, scale)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            dq[b, :, h, :], dk[b, :, h, :], dv[b, :, h, :] = head_bwd(
+                dout[b, :, h, :], q[b, :, h, :], k[b, :, h, :], v[b, :, h, :], sc, causal,
+                window[0], window[1], _slope_for(alibi_slopes, b, h))
+    return dq, dk, dv
+
+
+def decode_splitkv(q, k, v, num_splits, scale=None, causal=False, window=(-1, -1),
+                   alibi_slopes=None):
+    """Split-KV decode as the page describes it (section "2.2"): per (b,h), the
+    key range is cut into ``num_splits`` contiguous chunks, each chunk's
+    attention is computed on its own, then the chunks are merged.
+
+    Returns O (B,Sq,H,D), L (B,H,Sq). By the exactness of the merge this equals
+    ``attention_fwd``; the tests check that.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    sc = _default_scale(D, scale)
+    bounds = [(Sk * s) // num_splits for s in range(num_splits + 1)]
+    o = np.zeros_like(q)
+    lse = np.zeros((B, H, Sq))
+    for b in range(B):
+        for h in range(H):
+            kh = np.asarray(k[b, :, h, :], dtype=np.float64)
+            vh = np.asarray(v[b, :, h, :], dtype=np.float64)
+            parts = [head_partial(q[b, :, h, :], kh, vh, bounds[s], bounds[s + 1], sc, causal,
+                                  window[0], window[1], _slope_for(alibi_slopes, b, h))
+                     for s in range(num_splits)]
+            o[b, :, h, :], lse[b, h] = combine_partials([p[0] for p in parts],
+                                                        [p[1] for p in parts])
+    return o, lse
