@@ -1,0 +1,226 @@
+"""ctypes marshalling for libfa_gb300.so (see include/fa.h for the contract)."""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libfa_gb300.so"
+
+FA_OK = 0
+FA_ERR_INVALID = -1
+FA_ERR_UNSUPPORTED = -2
+FA_ERR_CUDA = -3
+FA_ERR_TIMEOUT = -4
+FA_ERR_WORKSPACE = -5
+
+
+class FAError(RuntimeError):
+    """A libfa_gb300 call returned a non-zero status."""
+
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {msg} (status {status})")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+
+_SIGS = {
+    "fa_version": (_I, []),
+    "fa_status_string": (ctypes.c_char_p, [_I]),
+    "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _I, _P]),
+    "fa_bwd_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _I,
+                    _I, _P]),
+    "fa_decode_num_splits": (_I, [_I, _I, _I, _I, _I]),
+    "fa_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _I, _I,
+                               _P]),
+    "fa_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
+}
+
+
+def library_path() -> str:
+    return os.path.join(_PKG, _LIB_NAME)
+
+
+def library() -> ctypes.CDLL:
+    """Load libfa_gb300.so (built in-tree by ``build.py``); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise FAError("load", FA_ERR_CUDA,
+                              f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in _SIGS.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+        return _lib
+
+
+def fa_version() -> int:
+    return int(library().fa_version())
+
+
+def fa_status_string(status: int) -> str:
+    return library().fa_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != FA_OK:
+        raise FAError(fn, status, fa_status_string(status))
+
+
+def _stream_ptr(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, name, dtype, shape=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _scale(softmax_scale, D):
+    return float(softmax_scale) if softmax_scale is not None else 1.0 / math.sqrt(D)
+
+
+def _alibi(alibi_slopes, B, H, device):
+    if alibi_slopes is None:
+        return None, 0
+    _need(alibi_slopes, "alibi_slopes", torch.float32, device=device)
+    if tuple(alibi_slopes.shape) == (H,):
+        return alibi_slopes, 0
+    if tuple(alibi_slopes.shape) == (B, H):
+        return alibi_slopes, H
+    raise ValueError(f"alibi_slopes must have shape ({H},) or ({B}, {H})")
+
+
+def fa_fwd(q, k, v, *, softmax_scale=None, causal=False, window_size=(-1, -1), alibi_slopes=None,
+           out=None, lse=None, stream=None):
+    """O, L = attention(q, k, v). q (B,Sq,H,D), k/v (B,Sk,H,D) bf16 -> out (B,Sq,H,D) bf16, lse (B,H,Sq) fp32."""
+    _need(q, "q", torch.bfloat16)
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    dev = q.device
+    _need(k, "k", torch.bfloat16, (B, Sk, H, D), dev)
+    _need(v, "v", torch.bfloat16, (B, Sk, H, D), dev)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, (B, Sq, H, D), dev)
+    _need(lse, "lse", torch.float32, (B, H, Sq), dev)
+    al, al_stride = _alibi(alibi_slopes, B, H, dev)
+    st = library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Sq, Sk, H, D,
+                          _scale(softmax_scale, D), int(bool(causal)), int(window_size[0]), int(window_size[1]),
+                          _ptr(al), al_stride, _stream_ptr(stream, dev))
+    _check("fa_fwd", st)
+    return out, lse
+
+
+def fa_bwd_workspace_size(B, Sq, Sk, H, D, deterministic=False) -> int:
+    return int(library().fa_bwd_workspace_size(B, Sq, Sk, H, D, int(bool(deterministic))))
+
+
+def fa_bwd(dout, q, k, v, out, lse, *, softmax_scale=None, causal=False, window_size=(-1, -1),
+           alibi_slopes=None, deterministic=False, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dQ, dK, dV of <dout, attention(q, k, v)>; out and lse are fa_fwd's outputs for the same arguments."""
+    _need(q, "q", torch.bfloat16)
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    dev = q.device
+    for name, t, shp in (("k", k, (B, Sk, H, D)), ("v", v, (B, Sk, H, D)), ("dout", dout, (B, Sq, H, D)),
+                         ("out", out, (B, Sq, H, D))):
+        _need(t, name, torch.bfloat16, shp, dev)
+    _need(lse, "lse", torch.float32, (B, H, Sq), dev)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t, shp in (("dq", dq, (B, Sq, H, D)), ("dk", dk, (B, Sk, H, D)), ("dv", dv, (B, Sk, H, D))):
+        _need(t, name, torch.bfloat16, shp, dev)
+    need = fa_bwd_workspace_size(B, Sq, Sk, H, D, deterministic)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, device=dev)
+    al, al_stride = _alibi(alibi_slopes, B, H, dev)
+    st = library().fa_bwd(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dq), _ptr(dk),
+                          _ptr(dv), _ptr(workspace), workspace.numel(), B, Sq, Sk, H, D,
+                          _scale(softmax_scale, D), int(bool(causal)), int(window_size[0]), int(window_size[1]),
+                          _ptr(al), al_stride, int(bool(deterministic)), _stream_ptr(stream, dev))
+    _check("fa_bwd", st)
+    return dq, dk, dv
+
+
+def fa_decode_num_splits(B, Sq, Sk, H, D) -> int:
+    return int(library().fa_decode_num_splits(B, Sq, Sk, H, D))
+
+
+def fa_decode_workspace_size(B, Sq, Sk, H, D, num_splits=0) -> int:
+    return int(library().fa_decode_workspace_size(B, Sq, Sk, H, D, int(num_splits)))
+
+
+def fa_decode_splitkv(q, k_cache, v_cache, *, softmax_scale=None, causal=False, window_size=(-1, -1),
+                      alibi_slopes=None, num_splits=0, workspace=None, out=None, lse=None, stream=None):
+    """Split-KV decode: q (B,Sq<=16,H,D), caches (B,Sk,H,D) bf16 -> out (B,Sq,H,D) bf16, lse (B,H,Sq) fp32."""
+    _need(q, "q", torch.bfloat16)
+    B, Sq, H, D = q.shape
+    Sk = k_cache.shape[1]
+    dev = q.device
+    _need(k_cache, "k_cache", torch.bfloat16, (B, Sk, H, D), dev)
+    _need(v_cache, "v_cache", torch.bfloat16, (B, Sk, H, D), dev)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, (B, Sq, H, D), dev)
+    _need(lse, "lse", torch.float32, (B, H, Sq), dev)
+    need = fa_decode_workspace_size(B, Sq, Sk, H, D, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, device=dev)
+    al, al_stride = _alibi(alibi_slopes, B, H, dev)
+    st = library().fa_decode_splitkv(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse),
+                                     _ptr(workspace), workspace.numel(), B, Sq, Sk, H, D,
+                                     _scale(softmax_scale, D), int(bool(causal)), int(window_size[0]),
+                                     int(window_size[1]), _ptr(al), al_stride, int(num_splits),
+                                     _stream_ptr(stream, dev))
+    _check("fa_decode_splitkv", st)
+    return out, lse
+
+
+def fa_device_status(stream=None):
+    """Synchronise the stream and read/clear the device status word: (status, raw word)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    word = ctypes.c_uint(0)
+    st = library().fa_device_status(_stream_ptr(stream, dev), ctypes.byref(word))
+    return int(st), int(word.value)

@@ -1,0 +1,212 @@
+// C-ABI entry points of libfa_gb300.so (declared in include/fa.h).
+//
+// This layer validates arguments, folds the defaults (scale = 1/sqrt(D),
+// causal => window_right = 0), and hands a validated AttnShape to the kernel
+// launchers. It allocates nothing: all tensors and workspaces belong to the
+// caller. The one piece of library state is a device status word per GPU
+// (a __device__ variable), which bounded waits inside the kernels set.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "internal.h"
+
+namespace fa {
+
+__device__ unsigned int g_status_word;
+
+static constexpr int kMaxDevices = 64;
+
+unsigned int* device_status_word() {
+  static unsigned int* ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned int*>(p);
+  }
+  return ptrs[dev];
+}
+
+int device_sm_count() {
+  static int counts[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  if (counts[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_bshd_map(CUtensorMap* map, const void* base, int B, int S, int H, int D, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {cuuint64_t(D), cuuint64_t(H), cuuint64_t(S), cuuint64_t(B)};
+  cuuint64_t strides[3] = {cuuint64_t(D) * 2, cuuint64_t(H) * D * 2, cuuint64_t(S) * H * D * 2};
+  cuuint32_t box[4] = {64, 1, cuuint32_t(box_rows), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace fa
+
+using fa::AttnShape;
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shared validation; fills `s`. D support is checked by the caller.
+static int check_common(int B, int Sq, int Sk, int H, int D, float scale, int causal, int wl, int wr,
+                        const float* alibi, int alibi_bstride, AttnShape* s) {
+  if (B < 1 || Sq < 1 || Sk < 1 || H < 1 || D < 1) return FA_ERR_INVALID;
+  if (wl < -1 || wr < -1) return FA_ERR_INVALID;
+  if (alibi) {
+    if (reinterpret_cast<uintptr_t>(alibi) & 3u) return FA_ERR_INVALID;
+    if (alibi_bstride != 0 && alibi_bstride != H) return FA_ERR_INVALID;
+  }
+  // Index ranges: rows and tiles are addressed with 32-bit ints, elements with 64-bit offsets.
+  if (Sq > (1 << 30) || Sk > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  s->B = B;
+  s->Sq = Sq;
+  s->Sk = Sk;
+  s->H = H;
+  s->D = D;
+  s->scale = (scale > 0.0f && isfinite(scale)) ? scale : 1.0f / sqrtf(float(D));
+  s->wl = wl;
+  s->wr = causal ? 0 : wr;
+  s->alibi = alibi;
+  s->alibi_bstride = alibi ? alibi_bstride : 0;
+  return FA_OK;
+}
+
+extern "C" {
+
+int fa_version(void) { return 10000; }
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK:
+      return "ok";
+    case FA_ERR_INVALID:
+      return "invalid argument";
+    case FA_ERR_UNSUPPORTED:
+      return "unsupported configuration";
+    case FA_ERR_CUDA:
+      return "CUDA runtime or driver error";
+    case FA_ERR_TIMEOUT:
+      return "device-side bounded wait expired";
+    case FA_ERR_WORKSPACE:
+      return "workspace missing, misaligned or too small";
+    default:
+      return "unknown status";
+  }
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Sq, int Sk, int H, int D,
+           float scale, int causal, int window_left, int window_right, const float* alibi_slopes,
+           int alibi_batch_stride, fa_stream_t stream) {
+  if (!q || !k || !v || !out || !lse) return FA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse)) return FA_ERR_INVALID;
+  AttnShape s;
+  int st = check_common(B, Sq, Sk, H, D, scale, causal, window_left, window_right, alibi_slopes,
+                        alibi_batch_stride, &s);
+  if (st != FA_OK) return st;
+  if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
+  return fa::fwd_launch(s, q, k, v, out, lse, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t fa_bwd_workspace_size(int B, int Sq, int Sk, int H, int D, int deterministic) {
+  if (B < 1 || Sq < 1 || Sk < 1 || H < 1 || (D != 64 && D != 128)) return 0;
+  return fa::bwd_workspace_bytes(B, Sq, Sk, H, D, deterministic);
+}
+
+int fa_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,
+           void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Sq, int Sk, int H,
+           int D, float scale, int causal, int window_left, int window_right, const float* alibi_slopes,
+           int alibi_batch_stride, int deterministic, fa_stream_t stream) {
+  if (!dout || !q || !k || !v || !out || !lse || !dq || !dk || !dv) return FA_ERR_INVALID;
+  if (!aligned16(dout) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_INVALID;
+  AttnShape s;
+  int st = check_common(B, Sq, Sk, H, D, scale, causal, window_left, window_right, alibi_slopes,
+                        alibi_batch_stride, &s);
+  if (st != FA_OK) return st;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  const size_t need = fa::bwd_workspace_bytes(B, Sq, Sk, H, D, deterministic);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return FA_ERR_WORKSPACE;
+  return fa::bwd_launch(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, deterministic,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fa_decode_num_splits(int B, int Sq, int Sk, int H, int D) {
+  if (B < 1 || Sq < 1 || Sk < 1 || H < 1) return 1;
+  return fa::decode_auto_splits(B, Sq, Sk, H, D);
+}
+
+size_t fa_decode_workspace_size(int B, int Sq, int Sk, int H, int D, int num_splits) {
+  if (B < 1 || Sq < 1 || Sq > 16 || Sk < 1 || H < 1 || (D != 64 && D != 128 && D != 256)) return 0;
+  if (num_splits < 0 || num_splits > 256) return 0;
+  const int n = num_splits == 0 ? fa::decode_auto_splits(B, Sq, Sk, H, D) : num_splits;
+  return fa::decode_workspace_bytes(B, Sq, H, D, n);
+}
+
+int fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, void* out, float* lse,
+                      void* workspace, size_t workspace_bytes, int B, int Sq, int Sk, int H, int D, float scale,
+                      int causal, int window_left, int window_right, const float* alibi_slopes,
+                      int alibi_batch_stride, int num_splits, fa_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !out || !lse) return FA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(lse))
+    return FA_ERR_INVALID;
+  AttnShape s;
+  int st = check_common(B, Sq, Sk, H, D, scale, causal, window_left, window_right, alibi_slopes,
+                        alibi_batch_stride, &s);
+  if (st != FA_OK) return st;
+  if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
+  if (Sq > 16) return FA_ERR_UNSUPPORTED;
+  if (num_splits < 0 || num_splits > 256) return FA_ERR_INVALID;
+  const int n = num_splits == 0 ? fa::decode_auto_splits(B, Sq, Sk, H, D) : num_splits;
+  const size_t need = fa::decode_workspace_bytes(B, Sq, H, D, n);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return FA_ERR_WORKSPACE;
+  return fa::decode_launch(s, q, k_cache, v_cache, out, lse, workspace, n, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fa_device_status(fa_stream_t stream, unsigned int* detail) {
+  if (detail) *detail = 0;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned int word = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&word, fa::g_status_word, sizeof(word)) != cudaSuccess) return FA_ERR_CUDA;
+  if (word && cudaMemcpyToSymbol(fa::g_status_word, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+  if (detail) *detail = word;
+  return word ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,33 @@
+// Device-side constants shared by the attention kernels: the status word
+// layout, the watchdog limit, and the per-row live-key interval.
+#pragma once
+#include <stdint.h>
+
+namespace fa {
+
+// Device status word: FA_DEV_TIMEOUT is set when a bounded wait gives up;
+// the low bits name the wait site (kernel id << 4 | site).
+constexpr unsigned int FA_DEV_TIMEOUT = 0x80000000u;
+constexpr unsigned int FA_DEV_SITE_MASK = 0x0000FFFFu;
+// A legitimate wait inside these kernels lasts microseconds; one second
+// means a lost arrival, after which the kernel leaves instead of hanging.
+constexpr uint64_t FA_WAIT_TIMEOUT_NS = 1000000000ull;
+
+// Live key interval of query row i (page "FlashAttention：快速且内存高效的准确注意力机制",
+// sections "2.1" and "2.3"): the diagonal key is c(i) = i + Sk - Sq (bottom-right
+// alignment); the window keeps keys in [c(i) - left, c(i) + right], -1 meaning
+// unbounded, and causal means right = 0. Empty when lo > hi.
+struct RowRange {
+  int lo, hi;
+};
+
+__host__ __device__ __forceinline__ RowRange live_range(int i, int Sq, int Sk, int wl, int wr) {
+  const int c = i + Sk - Sq;
+  int lo = (wl >= 0) ? c - wl : 0;
+  int hi = (wr >= 0) ? c + wr : Sk - 1;
+  lo = lo < 0 ? 0 : lo;
+  hi = hi > Sk - 1 ? Sk - 1 : hi;
+  return RowRange{lo, hi};
+}
+
+}  // namespace fa

@@ -1,0 +1,461 @@
+// Forward attention kernel for sm_103a.
+//
+// Method (page "FlashAttention：快速且内存高效的准确注意力机制", section
+// "算法 / 前向传播"): Q is cut into 128-row tiles; for each tile the K/V
+// tiles are streamed once; an online softmax keeps an UNSCALED output O and
+// the row statistics (m, l), divides O by l only after the last tile, and
+// saves the row logsumexp L = m + log l for the backward.
+//
+// GB300 mapping (one CTA = NT query tiles of 128 rows of one (b, h)):
+//   warp 0        TMA producer: Q once, then K_j, V_j into a ring of smem slots
+//   warp 1        TMEM allocator and tcgen05.mma issuer (one thread):
+//                   S_t = Q_t K_j^T  -> TMEM (fp32, 128 columns)
+//                   O_t += P_t V_j   -> TMEM (fp32, D columns), P_t read from TMEM
+//   warps 4..     one softmax warpgroup per query tile; thread r owns row r of
+//                 the tile (TMEM lane r): it reads its S row, applies mask and
+//                 ALiBi, updates (m, l), writes P (bf16) back over its S columns,
+//                 rescales its O row in TMEM when the running max moved by more
+//                 than 2^8, and finally normalises O and writes O and L.
+// The MMA order for NT = 2 interleaves the two tiles so each softmax group has
+// two MMAs' worth of time per K/V tile.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "../../include/fa.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+
+struct FwdParams {
+  __nv_bfloat16* out;
+  float* lse;
+  const float* alibi;
+  int alibi_bstride;
+  int B, Sq, Sk, H;
+  int wl, wr;
+  float scale_log2;  // softmax scale * log2(e)
+  unsigned int* status;
+};
+
+template <int D, int NT>
+struct FwdCfg {
+  static constexpr int PANELS = D / 64;
+  static constexpr int PANEL_BYTES = 128 * 128;  // 128 rows x 128 B
+  static constexpr int TILE_BYTES = PANELS * PANEL_BYTES;
+  static constexpr int NSLOT = D == 64 ? 8 : (D == 128 ? 4 : 2);
+  static constexpr int THREADS = 128 * (1 + NT);
+  static constexpr int Q_OFF = 0;
+  static constexpr int KV_OFF = NT * TILE_BYTES;
+  static constexpr int BAR_OFF = KV_OFF + NSLOT * TILE_BYTES;
+  static constexpr int SMEM_BYTES = BAR_OFF + 512 + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t O_COL0 = 256;
+  static_assert(NT == 1 || 256 + NT * D <= 512, "TMEM budget");
+};
+
+struct FwdBars {
+  uint64_t q_full;
+  uint64_t kv_full[8];
+  uint64_t kv_empty[8];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t pv_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Wait-site codes for the status word (kernel 1).
+enum : uint32_t {
+  SITE_PROD_EMPTY = 0x11,
+  SITE_MMA_Q = 0x12,
+  SITE_MMA_K = 0x13,
+  SITE_MMA_V = 0x14,
+  SITE_MMA_P = 0x15,
+  SITE_SM_S = 0x16,
+  SITE_SM_PV = 0x17,
+  SITE_SM_EPI = 0x18,
+};
+
+// Timeout-only wait used while draining after an abort.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) return;
+  }
+}
+
+template <int D, int NT>
+__global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using C = FwdCfg<D, NT>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  FwdBars* bars = reinterpret_cast<FwdBars*>(smem + C::BAR_OFF);
+
+  const int warp = int(warp_id());
+  const int lane = int(lane_id());
+
+  const int n_groups = (p.Sq + NT * 128 - 1) / (NT * 128);
+  // Groups with more live keys first (causal / right-bounded windows).
+  const int qg = (p.wr >= 0) ? (n_groups - 1 - int(blockIdx.x)) : int(blockIdx.x);
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  const int row0 = qg * NT * 128;
+  const int last_row = min(p.Sq, row0 + NT * 128) - 1;
+
+  const RowRange first_rr = live_range(row0, p.Sq, p.Sk, p.wl, p.wr);
+  const RowRange last_rr = live_range(last_row, p.Sq, p.Sk, p.wl, p.wr);
+  const int kv_lo = first_rr.lo;
+  const int kv_hi = last_rr.hi;
+  const int jb = kv_lo / 128;
+  const int n_blocks = (kv_hi >= kv_lo) ? (kv_hi / 128 + 1 - jb) : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < C::NSLOT; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->p_full[s], 128);
+      mbar_init(&bars->pv_done[s], 1);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const Watch watch{&bars->abort, p.status};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_blocks > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(&bars->q_full, NT * C::TILE_BYTES);
+      for (int t = 0; t < NT; ++t)
+        for (int pn = 0; pn < C::PANELS; ++pn)
+          tma_load_4d(smem + C::Q_OFF + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bars->q_full, pn * 64,
+                      h, row0 + t * 128, b);
+      int issued = 0;
+      bool ok = true;
+      for (int jj = 0; jj < n_blocks && ok; ++jj) {
+        for (int kv = 0; kv < 2; ++kv) {
+          const int it = 2 * jj + kv;
+          const int s = it % C::NSLOT;
+          const uint32_t ph = uint32_t(it / C::NSLOT) & 1u;
+          if (!fa_wait(&bars->kv_empty[s], ph ^ 1u, watch, SITE_PROD_EMPTY)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->kv_full[s], C::TILE_BYTES);
+          const CUtensorMap* m = kv ? &tm_v : &tm_k;
+          for (int pn = 0; pn < C::PANELS; ++pn)
+            tma_load_4d(smem + C::KV_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, m, &bars->kv_full[s],
+                        pn * 64, h, (jb + jj) * 128, b);
+          issued = it + 1;
+        }
+      }
+      if (!ok) {  // let the copies in flight land before the CTA leaves
+        drain_wait(&bars->q_full, 0);
+        for (int it = (issued > C::NSLOT ? issued - C::NSLOT : 0); it < issued; ++it)
+          drain_wait(&bars->kv_full[it % C::NSLOT], uint32_t(it / C::NSLOT) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_blocks > 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
+      constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);    // P from TMEM, V MN-major
+      const uint32_t q_base = smem_u32(smem + C::Q_OFF);
+      const uint32_t kv_base = smem_u32(smem + C::KV_OFF);
+
+      auto slot_of = [&](int it) { return it % C::NSLOT; };
+      auto wait_full = [&](int it, uint32_t site) {
+        return fa_wait(&bars->kv_full[slot_of(it)], uint32_t(it / C::NSLOT) & 1u, watch, site);
+      };
+      auto issue_s = [&](int jj, int t, int sbuf) {
+        const uint32_t qa = q_base + t * C::TILE_BYTES;
+        const uint32_t ka = kv_base + slot_of(2 * jj) * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
+          mma_ss(tmem + sbuf * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), IDESC_S,
+                 kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int jj, int t, int sbuf) {
+        const uint32_t va = kv_base + slot_of(2 * jj + 1) * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          mma_ts(tmem + C::O_COL0 + t * D, tmem + sbuf * 128 + kk * 8,
+                 sdesc_sw128(va + kk * 2048, C::PANEL_BYTES, 1024), IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
+
+      bool ok = fa_wait(&bars->q_full, 0, watch, SITE_MMA_Q);
+      tc_fence_after();
+      if (NT == 2) {
+        for (int jj = 0; jj < n_blocks && ok; ++jj) {
+          if (!(ok = wait_full(2 * jj, SITE_MMA_K))) break;
+          tc_fence_after();
+          issue_s(jj, 0, 0);
+          mma_commit(&bars->s_full[0]);
+          if (jj > 0) {
+            if (!(ok = fa_wait(&bars->p_full[1], uint32_t(jj - 1) & 1u, watch, SITE_MMA_P))) break;
+            tc_fence_after();
+            issue_pv(jj - 1, 1, 1);
+            mma_commit(&bars->pv_done[1]);
+            mma_commit(&bars->kv_empty[slot_of(2 * (jj - 1) + 1)]);
+          }
+          issue_s(jj, 1, 1);
+          mma_commit(&bars->s_full[1]);
+          mma_commit(&bars->kv_empty[slot_of(2 * jj)]);
+          if (!(ok = wait_full(2 * jj + 1, SITE_MMA_V))) break;
+          if (!(ok = fa_wait(&bars->p_full[0], uint32_t(jj) & 1u, watch, SITE_MMA_P))) break;
+          tc_fence_after();
+          issue_pv(jj, 0, 0);
+          mma_commit(&bars->pv_done[0]);
+        }
+        if (ok) {
+          const int jj = n_blocks - 1;
+          if ((ok = fa_wait(&bars->p_full[1], uint32_t(jj) & 1u, watch, SITE_MMA_P))) {
+            tc_fence_after();
+            issue_pv(jj, 1, 1);
+            mma_commit(&bars->pv_done[1]);
+            mma_commit(&bars->kv_empty[slot_of(2 * jj + 1)]);
+          }
+        }
+      } else {
+        if (ok && (ok = wait_full(0, SITE_MMA_K))) {
+          tc_fence_after();
+          issue_s(0, 0, 0);
+          mma_commit(&bars->s_full[0]);
+          mma_commit(&bars->kv_empty[slot_of(0)]);
+        }
+        for (int jj = 0; jj < n_blocks && ok; ++jj) {
+          if (jj + 1 < n_blocks) {
+            if (!(ok = wait_full(2 * (jj + 1), SITE_MMA_K))) break;
+            tc_fence_after();
+            issue_s(jj + 1, 0, (jj + 1) & 1);
+            mma_commit(&bars->s_full[(jj + 1) & 1]);
+            mma_commit(&bars->kv_empty[slot_of(2 * (jj + 1))]);
+          }
+          if (!(ok = wait_full(2 * jj + 1, SITE_MMA_V))) break;
+          if (!(ok = fa_wait(&bars->p_full[0], uint32_t(jj) & 1u, watch, SITE_MMA_P))) break;
+          tc_fence_after();
+          issue_pv(jj, 0, jj & 1);
+          mma_commit(&bars->pv_done[0]);
+          mma_commit(&bars->kv_empty[slot_of(2 * jj + 1)]);
+        }
+      }
+      if (!ok) {  // let issued MMAs finish before TMEM is released
+        mma_commit(&bars->drain);
+        drain_wait(&bars->drain, 0);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int t = (warp - 4) / 4;
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const int i = row0 + t * 128 + r;
+    const uint32_t lane_addr = uint32_t(wq * 32) << 16;
+    const RowRange rr = live_range(i, p.Sq, p.Sk, p.wl, p.wr);
+    const int tile_first = row0 + t * 128;
+    const int tile_last = min(p.Sq - 1, tile_first + 127);
+    const int tile_lo_max = live_range(tile_last, p.Sq, p.Sk, p.wl, p.wr).lo;
+    const int tile_hi_min = live_range(tile_first, p.Sq, p.Sk, p.wl, p.wr).hi;
+    const bool has_alibi = p.alibi != nullptr;
+    const float slope_log2 =
+        has_alibi ? p.alibi[b * p.alibi_bstride + h] * 1.4426950408889634f : 0.0f;
+    const int c_i = i + p.Sk - p.Sq;
+    const float sl = p.scale_log2;
+
+    float m = -INFINITY;  // reference max (log2 units) the running O and l are relative to
+    float l = 0.0f;
+    bool ok = true;
+    for (int jj = 0; jj < n_blocks; ++jj) {
+      const int sb = (NT == 2) ? t : (jj & 1);
+      const uint32_t par = (NT == 2) ? (uint32_t(jj) & 1u) : (uint32_t(jj >> 1) & 1u);
+      if (!(ok = fa_wait_warp(&bars->s_full[sb], par, watch, SITE_SM_S))) break;
+      tc_fence_after();
+      float x[128];
+      tmem_ld_x128f(tmem + lane_addr + sb * 128, x);
+
+      const int kbase = (jb + jj) * 128;
+      const bool need_mask = !(kbase >= tile_lo_max && kbase + 127 <= tile_hi_min);
+      if (has_alibi) {
+        // x = scale*log2(e)*qk - slope*log2(e)*|c(i) - j|, in log2 units
+        const float d0 = float(c_i - kbase);
+#pragma unroll
+        for (int c = 0; c < 128; ++c) x[c] = fmaf(x[c], sl, -slope_log2 * fabsf(d0 - float(c)));
+      }
+      if (need_mask) {
+        const int lo = rr.lo - kbase, hi = rr.hi - kbase;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) x[c] = (c >= lo && c <= hi) ? x[c] : -INFINITY;
+      }
+      float mx0 = x[0], mx1 = x[1];
+#pragma unroll
+      for (int c = 2; c < 128; c += 2) {
+        mx0 = fmaxf(mx0, x[c]);
+        mx1 = fmaxf(mx1, x[c + 1]);
+      }
+      const float mx = fmaxf(mx0, mx1);
+      // block max in log2 units (without ALiBi, x still holds raw q.k)
+      const float m_blk = has_alibi ? mx : mx * sl;
+      const float m_new = fmaxf(m, m_blk);
+      float alpha = 1.0f;
+      if (m_new != -INFINITY) {
+        if (m == -INFINITY) {
+          m = m_new;  // first live key: O and l are still exactly 0
+        } else if (m_new > m + 8.0f) {
+          alpha = ex2_approx(m - m_new);
+          m = m_new;
+        }
+      }
+      l *= alpha;
+      const float m_use = (m == -INFINITY) ? 0.0f : m;
+      // without ALiBi: p = 2^(x*sl - m); with ALiBi x is already in log2 units
+      const float mul = has_alibi ? 1.0f : sl;
+      float rs0 = 0.0f, rs1 = 0.0f;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c = q4 * 32 + 2 * e;
+          const float p0 = ex2_approx(fmaf(x[c], mul, -m_use));
+          const float p1 = ex2_approx(fmaf(x[c + 1], mul, -m_use));
+          rs0 += p0;
+          rs1 += p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st_x16(tmem + lane_addr + sb * 128 + q4 * 16, pk);
+      }
+      l += rs0 + rs1;
+      const bool rescale = alpha != 1.0f;
+      if (__any_sync(0xffffffffu, rescale) && jj > 0) {
+        // O must hold P_{j-1} V_{j-1} before it is rescaled (P_j is already in TMEM).
+        if (!(ok = fa_wait_warp(&bars->pv_done[t], uint32_t(jj - 1) & 1u, watch, SITE_SM_PV))) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          const uint32_t oa = tmem + lane_addr + C::O_COL0 + t * D + cc * 32;
+          tmem_ld_x32(oa, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st_x32(oa, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[t]);
+    }
+
+    // ------------------------------------------------------------ epilogue
+    const bool row_ok = i < p.Sq;
+    const size_t orow = ((size_t(b) * p.Sq + size_t(i)) * p.H + h) * size_t(D);
+    if (n_blocks == 0) {
+      if (row_ok) {
+        uint4 z = make_uint4(0, 0, 0, 0);
+        uint4* dst = reinterpret_cast<uint4*>(p.out + orow);
+        for (int e = 0; e < D / 8; ++e) dst[e] = z;
+        p.lse[(size_t(b) * p.H + h) * p.Sq + i] = -INFINITY;
+      }
+    } else if (ok && fa_wait_warp(&bars->pv_done[t], uint32_t(n_blocks - 1) & 1u, watch, SITE_SM_EPI)) {
+      tc_fence_after();
+      const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld_x32(tmem + lane_addr + C::O_COL0 + t * D + cc * 32, o);
+        if (row_ok) {
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+          uint4* dst = reinterpret_cast<uint4*>(p.out + orow + cc * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+        }
+      }
+      if (row_ok)
+        p.lse[(size_t(b) * p.H + h) * p.Sq + i] =
+            (l > 0.0f) ? (m + lg2_approx(l)) * 0.6931471805599453f : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D, int NT>
+static int launch_fwd_t(const AttnShape& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                        void* out, float* lse, cudaStream_t stream) {
+  using C = FwdCfg<D, NT>;
+  auto kern = fa_fwd_kernel<D, NT>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+    return FA_ERR_CUDA;
+  FwdParams p;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.alibi = s.alibi;
+  p.alibi_bstride = s.alibi_bstride;
+  p.B = s.B;
+  p.Sq = s.Sq;
+  p.Sk = s.Sk;
+  p.H = s.H;
+  p.wl = s.wl;
+  p.wr = s.wr;
+  p.scale_log2 = s.scale * 1.4426950408889634f;
+  p.status = device_status_word();
+  if (!p.status) return FA_ERR_CUDA;
+  dim3 grid((s.Sq + NT * 128 - 1) / (NT * 128), s.H, s.B);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fwd_launch(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,
+               cudaStream_t stream) {
+  if (s.B > 65535 || s.H > 65535) return FA_ERR_UNSUPPORTED;
+  CUtensorMap mq, mk, mv;
+  if (!make_bshd_map(&mq, q, s.B, s.Sq, s.H, s.D, 128) || !make_bshd_map(&mk, k, s.B, s.Sk, s.H, s.D, 128) ||
+      !make_bshd_map(&mv, v, s.B, s.Sk, s.H, s.D, 128))
+    return FA_ERR_CUDA;
+  switch (s.D) {
+    case 64:
+      return launch_fwd_t<64, 2>(s, mq, mk, mv, out, lse, stream);
+    case 128:
+      return launch_fwd_t<128, 2>(s, mq, mk, mv, out, lse, stream);
+    case 256:
+      return launch_fwd_t<256, 1>(s, mq, mk, mv, out, lse, stream);
+    default:
+      return FA_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace fa

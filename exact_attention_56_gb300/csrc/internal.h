@@ -1,0 +1,42 @@
+// Host-side declarations shared by the C-ABI layer and the kernel launchers.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fa {
+
+// Arguments common to every attention entry point, after validation.
+struct AttnShape {
+  int B, Sq, Sk, H, D;
+  float scale;        // softmax scale (already defaulted)
+  int wl, wr;         // window, causal folded into wr (= 0); -1 unbounded
+  const float* alibi; // NULL or fp32 slopes
+  int alibi_bstride;  // 0 (slopes (H,)) or H (slopes (B,H))
+};
+
+// Status word of the current device (device pointer), or NULL on failure.
+unsigned int* device_status_word();
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+// Encodes a 4-D tiled TMA map over a (B, S, H, D) bf16 tensor: box of
+// 64 head-dim elements (128 B, 128-byte swizzle) x 1 head x `box_rows` rows
+// x 1 batch. Returns false if the driver rejects it.
+bool make_bshd_map(CUtensorMap* map, const void* base, int B, int S, int H, int D, int box_rows);
+
+// Kernel launchers (return an fa_status value).
+int fwd_launch(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,
+               cudaStream_t stream);
+int decode_launch(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,
+                  void* workspace, int num_splits, cudaStream_t stream);
+size_t decode_workspace_bytes(int B, int Sq, int H, int D, int num_splits);
+int decode_auto_splits(int B, int Sq, int Sk, int H, int D);
+int bwd_launch(const AttnShape& s, const void* dout, const void* q, const void* k, const void* v,
+               const void* out, const float* lse, void* dq, void* dk, void* dv, void* workspace,
+               int deterministic, cudaStream_t stream);
+size_t bwd_workspace_bytes(int B, int Sq, int Sk, int H, int D, int deterministic);
+
+}  // namespace fa

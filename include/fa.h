@@ -1,0 +1,141 @@
+/*
+ * fa.h — C ABI of the GB300 (sm_103a) exact-attention library, libfa_gb300.so.
+ *
+ * The library computes exact scaled dot-product attention,
+ *     O = softmax(scale * Q K^T + bias, masked) V,
+ * as defined on the page "FlashAttention：快速且内存高效的准确注意力机制"
+ * (cloud.tencent.com.cn/developer/article/2433927), sections "使用示例" and
+ * "参数说明" (arguments softmax_scale, causal, window_size, alibi_slopes,
+ * deterministic). Section names below refer to that page.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor pointer is DEVICE memory owned by the caller, contiguous,
+ *   16-byte aligned. The library never allocates, frees or keeps a pointer
+ *   after the call returns.
+ * - Layouts: q, out, dout, dq: (B, Sq, H, D) bf16; k, v, dk, dv, k_cache,
+ *   v_cache: (B, Sk, H, D) bf16; lse: (B, H, Sq) fp32, natural-log row
+ *   logsumexp of the masked, scaled scores.
+ * - D (head dim) is 64, 128 or 256 (backward: 64 or 128).
+ * - scale <= 0 (or NaN) selects the default 1/sqrt(D) (section "参数说明").
+ * - causal != 0 masks key j for query row i unless j <= i + Sk - Sq: the mask
+ *   is aligned to the bottom-right corner of the score matrix (section
+ *   "2.1：更改causal标志的行为").
+ * - window_left / window_right >= 0 keep only keys j with
+ *   i + Sk - Sq - window_left <= j <= i + Sk - Sq + window_right; -1 means
+ *   unbounded on that side (sections "参数说明", "2.3：局部（即滑动窗口）注意力").
+ *   causal != 0 forces window_right = 0.
+ * - alibi_slopes: NULL, or fp32 device array of shape (H,) when
+ *   alibi_batch_stride == 0, or (B, H) when alibi_batch_stride == H. The
+ *   score of (i, j) gets -slope * |i + Sk - Sq - j| added after scaling
+ *   (sections "参数说明", "2.4：ALiBi（线性偏差注意力），确定性反向传播").
+ * - A query row with no live key gets O = 0 (section "2.1", last sentence)
+ *   and lse = -inf.
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *   default stream). The return value reports argument checks and launch
+ *   errors only. A kernel whose internal bounded wait expired records it in
+ *   a device status word, read by fa_device_status().
+ * - No entry point throws, exits or traps. Nothing falls back to another
+ *   implementation.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fa_stream_t; /* same type as cudaStream_t */
+
+typedef enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID = -1,     /* NULL/misaligned pointer, size < 1, bad window or ALiBi stride */
+  FA_ERR_UNSUPPORTED = -2, /* valid request outside what is built (e.g. D = 96) */
+  FA_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed (launch, tensor-map encode) */
+  FA_ERR_TIMEOUT = -4,     /* a device-side bounded wait expired (from fa_device_status) */
+  FA_ERR_WORKSPACE = -5    /* workspace pointer NULL/misaligned or workspace_bytes too small */
+} fa_status;
+
+/* Library version, major*10000 + minor*100 + patch. */
+int fa_version(void);
+
+/* Static description of a status code. Never NULL. */
+const char* fa_status_string(int status);
+
+/*
+ * Forward. Writes out (B,Sq,H,D) bf16 and lse (B,H,Sq) fp32.
+ * Computes, per (b, h), the tiled forward with an online softmax: for each
+ * 128-row query tile the key/value tiles are streamed once, the running
+ * output is kept unscaled and divided by the row sum only at the end, and
+ * the row logsumexp L is saved for the backward (section "算法 / 前向传播").
+ * Supported: D in {64, 128, 256}; any Sq, Sk >= 1.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Sq, int Sk, int H,
+           int D, float scale, int causal, int window_left, int window_right, const float* alibi_slopes,
+           int alibi_batch_stride, fa_stream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs (fp32 dQ accumulator, the per-row
+ * D_i = rowsum(dO * O) vector and, for deterministic mode, ordering counters).
+ * Returns 0 for arguments fa_bwd would reject.
+ */
+size_t fa_bwd_workspace_size(int B, int Sq, int Sk, int H, int D, int deterministic);
+
+/*
+ * Backward (section "反向传播": recompute P from the saved logsumexp L, no
+ * stored attention matrix). Inputs: dout, q, k, v, out (bf16) and lse (fp32)
+ * from fa_fwd with the same arguments. Writes dq (B,Sq,H,D), dk, dv
+ * (B,Sk,H,D) bf16; they are overwritten, not accumulated.
+ * deterministic != 0 makes dq/dk/dv bitwise reproducible from run to run
+ * (section "2.4": slightly slower, more workspace); 0 accumulates dQ with
+ * fp32 atomic adds in arbitrary order.
+ * workspace: caller-owned device buffer of at least fa_bwd_workspace_size()
+ * bytes, 256-byte aligned; its contents on entry are ignored.
+ * Supported: D in {64, 128}.
+ */
+int fa_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,
+           void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Sq, int Sk, int H,
+           int D, float scale, int causal, int window_left, int window_right, const float* alibi_slopes,
+           int alibi_batch_stride, int deterministic, fa_stream_t stream);
+
+/*
+ * Split count fa_decode_splitkv uses when num_splits == 0: chosen from the
+ * SM count of the current device so the split kernel fills whole waves.
+ */
+int fa_decode_num_splits(int B, int Sq, int Sk, int H, int D);
+
+/* Bytes of workspace fa_decode_splitkv needs for `num_splits` (0 = auto). */
+size_t fa_decode_workspace_size(int B, int Sq, int Sk, int H, int D, int num_splits);
+
+/*
+ * Split-KV decode for short queries (section "2.2：针对推理进行优化": the
+ * key/value loading is split across thread blocks and a separate kernel
+ * merges the results). q (B,Sq,H,D) with 1 <= Sq <= 16; k_cache, v_cache
+ * (B,Sk,H,D) contiguous. Each split writes its normalised partial output and
+ * logsumexp to the workspace; the combine kernel merges them exactly,
+ * L = log sum_s exp(L_s), O = sum_s exp(L_s - L) O_s, and writes out (bf16)
+ * and lse (fp32) in the fa_fwd layouts. Masks and ALiBi as in fa_fwd.
+ * num_splits: 0 = auto (fa_decode_num_splits), else 1..256.
+ * workspace: >= fa_decode_workspace_size() bytes, 256-byte aligned.
+ */
+int fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, void* out, float* lse,
+                      void* workspace, size_t workspace_bytes, int B, int Sq, int Sk, int H, int D, float scale,
+                      int causal, int window_left, int window_right, const float* alibi_slopes,
+                      int alibi_batch_stride, int num_splits, fa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of
+ * the current device. Returns FA_OK, FA_ERR_TIMEOUT (a kernel's bounded
+ * wait expired; *detail receives the raw word: wait-site code in the low
+ * 16 bits) or FA_ERR_CUDA. `detail` may be NULL.
+ */
+int fa_device_status(fa_stream_t stream, unsigned int* detail);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

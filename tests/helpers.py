@@ -1,0 +1,38 @@
+"""Shared test helpers: device transfer of bf16 bits and the parity metrics."""
+import numpy as np
+
+# Tolerances for bf16 outputs and fp32 L against the fp64 oracle.
+ATOL_BF16 = 2e-2
+RELRMS_BF16 = 1e-2
+ATOL_LSE = 1e-3
+
+
+def to_dev(bits, device="cuda"):
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def to_f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def rel_rms(x, ref):
+    return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), 1e-30))
+
+
+def assert_bf16_close(got, ref, what=""):
+    err = np.max(np.abs(got - ref)) if got.size else 0.0
+    rr = rel_rms(got, ref) if got.size else 0.0
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    assert err <= ATOL_BF16, f"{what}: max |err| {err:.3e} > {ATOL_BF16}"
+    assert rr <= RELRMS_BF16, f"{what}: rel RMS {rr:.3e} > {RELRMS_BF16}"
+
+
+def assert_lse_close(got, ref, what=""):
+    inf_ref = np.isneginf(ref)
+    assert np.array_equal(np.isneginf(got), inf_ref), f"{what}: -inf pattern differs"
+    fin = ~inf_ref
+    if fin.any():
+        err = np.max(np.abs(got[fin] - ref[fin]))
+        assert err <= ATOL_LSE, f"{what}: L max |err| {err:.3e} > {ATOL_LSE}"

@@ -1,0 +1,72 @@
+"""The C-ABI library builds, loads and exports every symbol include/fa.h declares;
+host-side argument checks reject bad calls before any CUDA work (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_56_gb300 import build as b
+
+    b.build()
+    import exact_attention_56_gb300 as fa
+
+    return fa.library()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(fa_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for required in ("fa_fwd", "fa_bwd", "fa_decode_splitkv", "fa_bwd_workspace_size",
+                     "fa_decode_workspace_size", "fa_device_status", "fa_status_string"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_strings(lib):
+    assert lib.fa_version() >= 10000
+    assert lib.fa_status_string(0) == b"ok"
+    assert b"workspace" in lib.fa_status_string(-5)
+
+
+def _fwd(lib, **kw):
+    a = dict(q=16, k=16, v=16, out=16, lse=16, B=1, Sq=8, Sk=8, H=1, D=64, scale=0.0, causal=0, wl=-1, wr=-1,
+             alibi=None, ab=0)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.fa_fwd(P(a["q"]), P(a["k"]), P(a["v"]), P(a["out"]), P(a["lse"]), a["B"], a["Sq"], a["Sk"], a["H"],
+                      a["D"], ctypes.c_float(a["scale"]), a["causal"], a["wl"], a["wr"], P(a["alibi"]), a["ab"],
+                      P(None))
+
+
+def test_argument_checks_without_gpu(lib):
+    import exact_attention_56_gb300 as fa
+
+    assert _fwd(lib, q=0) == fa.FA_ERR_INVALID          # NULL pointer
+    assert _fwd(lib, q=8) == fa.FA_ERR_INVALID          # not 16-byte aligned
+    assert _fwd(lib, Sq=0) == fa.FA_ERR_INVALID
+    assert _fwd(lib, wl=-2) == fa.FA_ERR_INVALID
+    assert _fwd(lib, alibi=16, ab=3, H=2) == fa.FA_ERR_INVALID
+    assert _fwd(lib, D=96) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_workspace_sizes(lib):
+    lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.fa_decode_workspace_size.restype = ctypes.c_size_t
+    assert lib.fa_bwd_workspace_size(1, 128, 128, 2, 64, 0) >= 128 * 2 * 64 * 4
+    assert lib.fa_bwd_workspace_size(1, 128, 128, 2, 96, 0) == 0
+    assert lib.fa_decode_workspace_size(2, 1, 1000, 4, 128, 3) >= 2 * 4 * 3 * (128 + 1) * 4
+    assert lib.fa_decode_workspace_size(2, 17, 1000, 4, 128, 3) == 0
