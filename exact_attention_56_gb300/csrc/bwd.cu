@@ -1,20 +1,611 @@
-// Backward attention kernels (placeholder until the tcgen05 backward lands).
+// Backward attention kernels for sm_103a.
+//
+// Method (page "FlashAttention：快速且内存高效的准确注意力机制", sections
+// "反向传播" and "并行性 / 反向传播"): only the row logsumexp L is kept from
+// the forward; P is recomputed tile by tile from it; the work is parallel over
+// key/value column blocks, and dQ is accumulated across blocks by atomic adds.
+// Section "2.4" adds a deterministic variant.
+//
+// Three kernels:
+//   fa_bwd_pre      D_i = rowsum(dO_i * O_i), L2_i = L_i*log2(e) (padded to
+//                   128-row tiles), zeroes the fp32 dQ accumulator and the
+//                   deterministic-mode counters.
+//   fa_bwd_main     one CTA per (128-key tile, head, batch); loops over the
+//                   live 128-row query tiles:
+//                     S^T  = K Q^T            -> TMEM [0,128)       (tcgen05)
+//                     dP^T = V dO^T           -> TMEM [128,256)
+//                     P^T  = 2^(S^T*scale*log2e + bias - L2)  (bf16, each half over its own S^T half)
+//                     dV  += P^T dO           (A = P^T from TMEM)
+//                     dS^T = P^T o (dP^T - D) (bf16, to shared memory)
+//                     dK  += dS^T Q           (A = dS^T, K-major view)
+//                     dQ   = dS K             (A = the same buffer, MN-major view) -> TMEM [128,128+D)
+//                   and drains dQ into the fp32 accumulator with 16-byte atomic
+//                   adds (deterministic mode: in key-tile order, behind a
+//                   per-query-tile counter).
+//   fa_bwd_convert  dQ = bf16(scale * dQ_acc).
+// Warp roles in fa_bwd_main (512 threads): warp 0 TMA producer, warp 1 TMEM
+// allocator + MMA issuer, warps 4-11 two compute warpgroups (thread = key row,
+// each group one half of the 128 query columns), warps 12-15 dQ warpgroup
+// (thread = query row).
+#include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <math.h>
 
 #include "../../include/fa.h"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace fa {
 
-size_t bwd_workspace_bytes(int B, int Sq, int Sk, int H, int D, int deterministic) {
-  (void)Sk;
-  (void)deterministic;
-  return size_t(B) * Sq * H * D * 4 + size_t(B) * H * Sq * 4 + 512;
+struct BwdParams {
+  const __nv_bfloat16* dout;
+  const __nv_bfloat16* out;
+  const float* lse;
+  float* dq_acc;   // (B, Sq, H, D) fp32
+  float* l2;       // (B, H, Sq_pad): L * log2(e); +inf on rows without keys and on padding
+  float* dvec;     // (B, H, Sq_pad): rowsum(dO * O)
+  int* sem;        // (B, H, n_qt, 4) ordering counters (deterministic mode)
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  const float* alibi;
+  int alibi_bstride;
+  int B, Sq, Sk, H, Sq_pad, n_qt;
+  int wl, wr;
+  float scale;
+  float scale_log2;
+  int deterministic;
+  unsigned int* status;
+};
+
+template <int D>
+struct BwdCfg {
+  static constexpr int PANELS = D / 64;
+  static constexpr int PANEL_BYTES = 128 * 128;
+  static constexpr int TILE_BYTES = PANELS * PANEL_BYTES;
+  static constexpr int NST = 2;
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = TILE_BYTES;
+  static constexpr int Q_OFF = 2 * TILE_BYTES;
+  static constexpr int DO_OFF = Q_OFF + NST * TILE_BYTES;
+  static constexpr int DS_OFF = DO_OFF + NST * TILE_BYTES;  // 128 keys x 128 queries bf16, two 64-query panels
+  static constexpr int VEC_OFF = DS_OFF + 2 * PANEL_BYTES;  // per stage: L2[128], D[128]
+  static constexpr int BAR_OFF = VEC_OFF + NST * 1024;
+  static constexpr int SMEM_BYTES = BAR_OFF + 256;
+  static constexpr int THREADS = 512;
+  static constexpr int STAGE_TX = 2 * TILE_BYTES + 1024;
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 128, T_DV = 256, T_DK = 256 + D;
+  static_assert(T_DK + D <= 512, "TMEM budget");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+struct BwdBars {
+  uint64_t kv_full;
+  uint64_t full[2];
+  uint64_t empty[2];
+  uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_free, acc_done, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+enum : uint32_t {
+  SITE_B_EMPTY = 0x31,
+  SITE_B_KV = 0x32,
+  SITE_B_FULL = 0x33,
+  SITE_B_DQFREE = 0x34,
+  SITE_B_P = 0x35,
+  SITE_B_DS = 0x36,
+  SITE_B_S = 0x37,
+  SITE_B_DP = 0x38,
+  SITE_B_DQ = 0x39,
+  SITE_B_ACC = 0x3A,
+  SITE_B_SEM = 0x3B,
+  SITE_B_ALIGN = 0x3C,
+};
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
 }
 
-int bwd_launch(const AttnShape&, const void*, const void*, const void*, const void*, const void*, const float*,
-               void*, void*, void*, void*, int, cudaStream_t) {
-  return FA_ERR_UNSUPPORTED;
+// Fire-and-forget 16-byte fp32 add to global memory (no value returned).
+__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ void drain_wait_b(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) return;
+  }
+}
+
+// Does query tile qt meet key tile kt (does the bounding interval of its rows'
+// live keys intersect the key tile)?
+__device__ __forceinline__ bool qtile_meets(int qt, int kt, const BwdParams& p) {
+  const int r0 = qt * 128;
+  const int r1 = min(p.Sq, r0 + 128) - 1;
+  const int lo = live_range(r0, p.Sq, p.Sk, p.wl, p.wr).lo;
+  const int hi = live_range(r1, p.Sq, p.Sk, p.wl, p.wr).hi;
+  if (hi < lo) return false;
+  return !(hi < kt * 128 || lo > kt * 128 + 127);
+}
+// First key tile that meets query tile qt (its rank base for deterministic ordering).
+__device__ __forceinline__ int first_ktile(int qt, const BwdParams& p) {
+  return live_range(qt * 128, p.Sq, p.Sk, p.wl, p.wr).lo / 128;
+}
+
+template <int D>
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
+    fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {  // the swizzled layouts need 1024-byte alignment
+    if (threadIdx.x == 0) atomicOr(p.status, FA_DEV_TIMEOUT | SITE_B_ALIGN);
+    return;
+  }
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::BAR_OFF);
+  const int warp = int(warp_id());
+  const int lane = int(lane_id());
+  const int kt = blockIdx.x;
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  const int j0 = kt * 128;
+
+  // Live query tiles of this key tile: a contiguous range.
+  const int n_qt = p.n_qt;
+  int qt_first = n_qt, qt_last = -1;
+  for (int qt = 0; qt < n_qt; ++qt) {
+    if (qtile_meets(qt, kt, p)) {
+      qt_first = min(qt_first, qt);
+      qt_last = qt;
+    }
+  }
+  const int n_iter = qt_last >= qt_first ? qt_last - qt_first + 1 : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_ready, 256);
+    mbar_init(&bars->ds_ready, 256);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_free, 128);
+    mbar_init(&bars->acc_done, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const Watch watch{&bars->abort, p.status};
+  const size_t vec_base = (size_t(b) * p.H + h) * p.Sq_pad;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_iter > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(&bars->kv_full, 2 * C::TILE_BYTES);
+      for (int pn = 0; pn < C::PANELS; ++pn) {
+        tma_load_4d(smem + C::K_OFF + pn * C::PANEL_BYTES, &tm_k, &bars->kv_full, pn * 64, h, j0, b);
+        tma_load_4d(smem + C::V_OFF + pn * C::PANEL_BYTES, &tm_v, &bars->kv_full, pn * 64, h, j0, b);
+      }
+      int issued = 0;
+      for (int ii = 0; ii < n_iter; ++ii) {
+        const int s = ii & 1;
+        if (!fa_wait(&bars->empty[s], (uint32_t(ii >> 1) & 1u) ^ 1u, watch, SITE_B_EMPTY)) break;
+        const int i0 = (qt_first + ii) * 128;
+        mbar_arrive_expect_tx(&bars->full[s], C::STAGE_TX);
+        for (int pn = 0; pn < C::PANELS; ++pn) {
+          tma_load_4d(smem + C::Q_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bars->full[s], pn * 64,
+                      h, i0, b);
+          tma_load_4d(smem + C::DO_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_do, &bars->full[s],
+                      pn * 64, h, i0, b);
+        }
+        bulk_load(smem + C::VEC_OFF + s * 1024, p.l2 + vec_base + i0, 512, &bars->full[s]);
+        bulk_load(smem + C::VEC_OFF + s * 1024 + 512, p.dvec + vec_base + i0, 512, &bars->full[s]);
+        issued = ii + 1;
+      }
+      drain_wait_b(&bars->kv_full, 0);
+      for (int ii = (issued > 2 ? issued - 2 : 0); ii < issued; ++ii)
+        drain_wait_b(&bars->full[ii & 1], uint32_t(ii >> 1) & 1u);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_iter > 0) {
+      constexpr uint32_t ID_SS = idesc_bf16_f32(128, 128, 0, 0);  // S^T, dP^T: both operands K-major
+      constexpr uint32_t ID_TN = idesc_bf16_f32(128, D, 0, 1);    // dV, dK: B (dO / Q) MN-major
+      constexpr uint32_t ID_DQ = idesc_bf16_f32(128, D, 1, 1);    // dQ: A (dS) and B (K) MN-major
+      const uint32_t k_a = smem_u32(smem + C::K_OFF);
+      const uint32_t v_a = smem_u32(smem + C::V_OFF);
+      const uint32_t ds_a = smem_u32(smem + C::DS_OFF);
+      bool ok = fa_wait(&bars->kv_full, 0, watch, SITE_B_KV);
+      for (int ii = 0; ii < n_iter && ok; ++ii) {
+        const int s = ii & 1;
+        const uint32_t q_a = smem_u32(smem + C::Q_OFF + s * C::TILE_BYTES);
+        const uint32_t do_a = smem_u32(smem + C::DO_OFF + s * C::TILE_BYTES);
+        if (!(ok = fa_wait(&bars->full[s], uint32_t(ii >> 1) & 1u, watch, SITE_B_FULL))) break;
+        tc_fence_after();
+        // S^T = K Q^T
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
+          mma_ss(tmem + C::T_S, sdesc_sw128(k_a + off, 16, 1024), sdesc_sw128(q_a + off, 16, 1024), ID_SS,
+                 kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->s_full);
+        // dP^T = V dO^T, into the columns dQ of the previous tile occupied
+        if (ii > 0) {
+          if (!(ok = fa_wait(&bars->dq_free, uint32_t(ii - 1) & 1u, watch, SITE_B_DQFREE))) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
+          mma_ss(tmem + C::T_DP, sdesc_sw128(v_a + off, 16, 1024), sdesc_sw128(do_a + off, 16, 1024), ID_SS,
+                 kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->dp_full);
+        // dV += P^T dO
+        if (!(ok = fa_wait(&bars->p_ready, uint32_t(ii) & 1u, watch, SITE_B_P))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // queries 16kk.. live at column 64*(kk/4) + 8*(kk%4)
+          mma_ts(tmem + C::T_DV, tmem + C::T_S + (kk / 4) * 64 + (kk % 4) * 8,
+                 sdesc_sw128(do_a + kk * 2048, C::PANEL_BYTES, 1024), ID_TN, (ii > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q ; dQ = dS K
+        if (!(ok = fa_wait(&bars->ds_ready, uint32_t(ii) & 1u, watch, SITE_B_DS))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
+          mma_ss(tmem + C::T_DK, sdesc_sw128(ds_a + off, 16, 1024),
+                 sdesc_sw128(q_a + kk * 2048, C::PANEL_BYTES, 1024), ID_TN, (ii > 0 || kk > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + C::T_DQ, sdesc_sw128(ds_a + kk * 2048, C::PANEL_BYTES, 1024),
+                 sdesc_sw128(k_a + kk * 2048, C::PANEL_BYTES, 1024), ID_DQ, kk > 0 ? 1u : 0u);
+        mma_commit(&bars->dq_full);
+        mma_commit(&bars->empty[s]);
+      }
+      if (ok) {
+        mma_commit(&bars->acc_done);
+      } else {
+        mma_commit(&bars->drain);
+        drain_wait_b(&bars->drain, 0);
+      }
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ------------------------------------------------------------ compute (thread = key row)
+    const int w = (warp - 4) / 4;  // query-column half
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const int j = j0 + r;
+    const uint32_t lane_addr = uint32_t(wq * 32) << 16;
+    const int off = p.Sk - p.Sq;
+    // live queries of key j: i in [qlo, qhi]
+    auto qbounds = [&](int jj, int& lo, int& hi) {
+      lo = (p.wr >= 0) ? jj - off - p.wr : 0;
+      hi = (p.wl >= 0) ? jj - off + p.wl : p.Sq - 1;
+      lo = max(lo, 0);
+      hi = min(hi, p.Sq - 1);
+      if (jj >= p.Sk) {
+        lo = 1;
+        hi = 0;
+      }
+    };
+    int qlo, qhi;
+    qbounds(j, qlo, qhi);
+    int qlo_max, dummy, qhi_min;
+    qbounds(min(p.Sk - 1, j0 + 127), qlo_max, dummy);
+    qbounds(j0, dummy, qhi_min);
+    const bool tile_keys_ok = j0 + 127 < p.Sk;
+    const bool has_alibi = p.alibi != nullptr;
+    const float slope_log2 = has_alibi ? p.alibi[b * p.alibi_bstride + h] * 1.4426950408889634f : 0.0f;
+    const float sl = p.scale_log2;
+    bool ok = true;
+    for (int ii = 0; ii < n_iter; ++ii) {
+      const int s = ii & 1;
+      const int i0 = (qt_first + ii) * 128;
+      const int ib = i0 + w * 64;  // first query of this half
+      const float* l2s = reinterpret_cast<const float*>(smem + C::VEC_OFF + s * 1024) + w * 64;
+      const float* dvs = l2s + 128;
+      if (!(ok = fa_wait_warp(&bars->s_full, uint32_t(ii) & 1u, watch, SITE_B_S))) break;
+      tc_fence_after();
+      float pv[64];
+      tmem_ld_x64f(tmem + lane_addr + C::T_S + w * 64, pv);
+      const bool need_mask = !(tile_keys_ok && i0 >= qlo_max && i0 + 127 <= qhi_min);
+      if (has_alibi) {
+        const float d0 = float(ib + off - j);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) pv[c] = fmaf(pv[c], sl, -slope_log2 * fabsf(d0 + float(c)) - l2s[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) pv[c] = fmaf(pv[c], sl, -l2s[c]);
+      }
+#pragma unroll
+      for (int c = 0; c < 64; ++c) pv[c] = ex2_approx(pv[c]);
+      if (need_mask) {
+        const int lo = qlo - ib, hi = qhi - ib;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) pv[c] = (c >= lo && c <= hi) ? pv[c] : 0.0f;
+      }
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
+        tmem_st_x32(tmem + lane_addr + C::T_S + w * 64, pk);  // inside this group's own S^T columns
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->p_ready);
+
+      if (!(ok = fa_wait_warp(&bars->dp_full, uint32_t(ii) & 1u, watch, SITE_B_DP))) break;
+      tc_fence_after();
+      uint8_t* ds_row = smem + C::DS_OFF + w * C::PANEL_BYTES + r * 128;
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        float dp[32];
+        uint32_t pb[16];  // P^T of these 32 queries, bf16 pairs, as the dV MMA used it
+        tmem_ld_x32f(tmem + lane_addr + C::T_DP + w * 64 + c2 * 32, dp);
+        tmem_ld_x16(tmem + lane_addr + C::T_S + w * 64 + c2 * 16, pb);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c = c2 * 32 + 2 * e;
+          const float p0 = __uint_as_float(pb[e] << 16), p1 = __uint_as_float(pb[e] & 0xFFFF0000u);
+          pk[e] = pack_bf16x2(p0 * (dp[2 * e] - dvs[c]), p1 * (dp[2 * e + 1] - dvs[c + 1]));
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int chunk = (c2 * 4 + e) ^ (r & 7);
+          *reinterpret_cast<uint4*>(ds_row + chunk * 16) =
+              make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->ds_ready);
+    }
+    // ------------------------------------------------------------ dK / dV epilogue
+    const bool row_ok = j < p.Sk;
+    __nv_bfloat16* dst = (w == 0 ? p.dv : p.dk) + ((size_t(b) * p.Sk + size_t(j)) * p.H + h) * size_t(D);
+    const float mul = (w == 0) ? 1.0f : p.scale;
+    if (n_iter == 0) {
+      if (row_ok)
+        for (int e = 0; e < D / 8; ++e) reinterpret_cast<uint4*>(dst)[e] = make_uint4(0, 0, 0, 0);
+    } else if (ok && fa_wait_warp(&bars->acc_done, 0, watch, SITE_B_ACC)) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        float a[32];
+        tmem_ld_x32f(tmem + lane_addr + (w == 0 ? C::T_DV : C::T_DK) + cc * 32, a);
+        if (row_ok) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(a[2 * e] * mul, a[2 * e + 1] * mul);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            reinterpret_cast<uint4*>(dst + cc * 32)[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+      }
+    }
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------ dQ drain (thread = query row)
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_addr = uint32_t(wq * 32) << 16;
+    for (int ii = 0; ii < n_iter; ++ii) {
+      const int qt = qt_first + ii;
+      const int i = qt * 128 + r;
+      if (!fa_wait_warp(&bars->dq_full, uint32_t(ii) & 1u, watch, SITE_B_DQ)) break;
+      tc_fence_after();
+      // Deterministic mode: warp wq adds its 32 rows of this query tile only after
+      // warp wq of every earlier key tile has (counter per (query tile, quarter)).
+      int* sem = p.sem + ((size_t(b) * p.H + h) * p.n_qt + qt) * 4 + wq;
+      if (p.deterministic) {
+        bool turn = true;
+        if (lane == 0) {
+          const int rank = kt - first_ktile(qt, p);
+          const uint64_t t0 = globaltimer_ns();
+          int v;
+          for (;;) {
+            asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(sem) : "memory");
+            if (v == rank) break;
+            if (*watch.abort || globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) {
+              *watch.abort = 1;
+              atomicOr(p.status, FA_DEV_TIMEOUT | SITE_B_SEM);
+              turn = false;
+              break;
+            }
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, turn ? 1 : 0, 0)) break;
+      }
+      float* dst = p.dq_acc + ((size_t(b) * p.Sq + size_t(i)) * p.H + h) * size_t(D);
+      const bool row_ok = i < p.Sq;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        float a[32];
+        tmem_ld_x32f(tmem + lane_addr + C::T_DQ + cc * 32, a);
+        if (row_ok) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) red_add_v4(dst + cc * 32 + 4 * e, a[4 * e], a[4 * e + 1], a[4 * e + 2], a[4 * e + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->dq_free);
+      if (p.deterministic) {
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// D_i = rowsum(dO * O), L2 = L*log2(e) (+inf where L = -inf or on padding),
+// dQ accumulator rows zeroed, counters zeroed. One warp per (b, h, row).
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
+  constexpr int PER = D / 32;
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  if (blockIdx.x == 0 && p.deterministic)
+    for (int t = threadIdx.x; t < p.n_qt * 4; t += blockDim.x) p.sem[(size_t(b) * p.H + h) * p.n_qt * 4 + t] = 0;
+  if (row >= p.Sq_pad) return;
+  const size_t vi = (size_t(b) * p.H + h) * p.Sq_pad + row;
+  if (row >= p.Sq) {
+    if (lane == 0) {
+      p.dvec[vi] = 0.0f;
+      p.l2[vi] = INFINITY;
+    }
+    return;
+  }
+  const size_t ro = ((size_t(b) * p.Sq + row) * p.H + h) * size_t(D) + lane * PER;
+  float acc = 0.0f;
+#pragma unroll
+  for (int e = 0; e < PER; e += 2) {
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(p.dout + ro + e);
+    const __nv_bfloat162 o = *reinterpret_cast<const __nv_bfloat162*>(p.out + ro + e);
+    acc = fmaf(__low2float(a), __low2float(o), acc);
+    acc = fmaf(__high2float(a), __high2float(o), acc);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+#pragma unroll
+  for (int e = 0; e < PER; e += 2) *reinterpret_cast<float2*>(p.dq_acc + ro + e) = make_float2(0.0f, 0.0f);
+  if (lane == 0) {
+    p.dvec[vi] = acc;
+    const float L = p.lse[(size_t(b) * p.H + h) * p.Sq + row];
+    p.l2[vi] = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
+  }
+}
+
+__global__ void __launch_bounds__(256) fa_bwd_convert_kernel(const float* __restrict__ acc,
+                                                              __nv_bfloat16* __restrict__ dq, size_t n8,
+                                                              float scale) {
+  for (size_t t = blockIdx.x * size_t(blockDim.x) + threadIdx.x; t < n8; t += size_t(gridDim.x) * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * t];
+    const float4 c = reinterpret_cast<const float4*>(acc)[2 * t + 1];
+    reinterpret_cast<uint4*>(dq)[t] = make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
+                                                 pack_bf16x2(c.x * scale, c.y * scale), pack_bf16x2(c.z * scale, c.w * scale));
+  }
+}
+
+static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t bwd_workspace_bytes(int B, int Sq, int Sk, int H, int D, int deterministic) {
+  (void)Sk;
+  const size_t sq_pad = size_t((Sq + 127) / 128) * 128;
+  const size_t n_qt = sq_pad / 128;
+  size_t n = al256(size_t(B) * Sq * H * D * 4);  // dQ accumulator
+  n += 2 * al256(size_t(B) * H * sq_pad * 4);    // L2, D
+  if (deterministic) n += al256(size_t(B) * H * n_qt * 4 * 4);
+  return n;
+}
+
+template <int D>
+static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, const void* k, const void* v,
+                        const void* out, const float* lse, void* dq, void* dk, void* dv, void* ws,
+                        int deterministic, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_bshd_map(&mq, q, s.B, s.Sq, s.H, D, 128) || !make_bshd_map(&mk, k, s.B, s.Sk, s.H, D, 128) ||
+      !make_bshd_map(&mv, v, s.B, s.Sk, s.H, D, 128) || !make_bshd_map(&mdo, dout, s.B, s.Sq, s.H, D, 128))
+    return FA_ERR_CUDA;
+  BwdParams p;
+  p.B = s.B;
+  p.Sq = s.Sq;
+  p.Sk = s.Sk;
+  p.H = s.H;
+  p.Sq_pad = ((s.Sq + 127) / 128) * 128;
+  p.n_qt = p.Sq_pad / 128;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  p.dq_acc = reinterpret_cast<float*>(w);
+  w += al256(size_t(s.B) * s.Sq * s.H * D * 4);
+  p.l2 = reinterpret_cast<float*>(w);
+  w += al256(size_t(s.B) * s.H * p.Sq_pad * 4);
+  p.dvec = reinterpret_cast<float*>(w);
+  w += al256(size_t(s.B) * s.H * p.Sq_pad * 4);
+  p.sem = deterministic ? reinterpret_cast<int*>(w) : nullptr;
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  p.out = static_cast<const __nv_bfloat16*>(out);
+  p.lse = lse;
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.alibi = s.alibi;
+  p.alibi_bstride = s.alibi_bstride;
+  p.wl = s.wl;
+  p.wr = s.wr;
+  p.scale = s.scale;
+  p.scale_log2 = s.scale * 1.4426950408889634f;
+  p.deterministic = deterministic ? 1 : 0;
+  p.status = device_status_word();
+  if (!p.status) return FA_ERR_CUDA;
+  if (s.B > 65535 || s.H > 65535) return FA_ERR_UNSUPPORTED;
+
+  fa_bwd_pre_kernel<D><<<dim3(p.Sq_pad / 8, s.H, s.B), 256, 0, stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  auto kern = fa_bwd_main_kernel<D>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+    return FA_ERR_CUDA;
+  kern<<<dim3((s.Sk + 127) / 128, s.H, s.B), C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  const size_t n8 = size_t(s.B) * s.Sq * s.H * D / 8;
+  size_t nb = (n8 + 255) / 256;
+  const size_t cap = size_t(device_sm_count()) * 8;
+  if (nb > cap) nb = cap;
+  if (nb < 1) nb = 1;
+  const int blocks = int(nb);
+  fa_bwd_convert_kernel<<<blocks, 256, 0, stream>>>(p.dq_acc, p.dq, n8, s.scale);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int bwd_launch(const AttnShape& s, const void* dout, const void* q, const void* k, const void* v, const void* out,
+               const float* lse, void* dq, void* dk, void* dv, void* workspace, int deterministic,
+               cudaStream_t stream) {
+  switch (s.D) {
+    case 64:
+      return launch_bwd_t<64>(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, deterministic, stream);
+    case 128:
+      return launch_bwd_t<128>(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, deterministic, stream);
+    default:
+      return FA_ERR_UNSUPPORTED;
+  }
 }
 
 }  // namespace fa

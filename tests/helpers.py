@@ -17,8 +17,15 @@ def to_f64(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
+# Relative RMS needs a non-vanishing reference: where the exact result is ~0
+# (e.g. a one-key window, where dS = P o (dP - D) cancels exactly) the
+# denominator is floored at an RMS of 1e-3, about one bf16 step at unit scale.
+REF_RMS_FLOOR = 1e-3
+
+
 def rel_rms(x, ref):
-    return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), 1e-30))
+    floor = REF_RMS_FLOOR * np.sqrt(max(ref.size, 1))
+    return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), floor))
 
 
 def assert_bf16_close(got, ref, what=""):
