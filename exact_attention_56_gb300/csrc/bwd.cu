@@ -12,17 +12,23 @@
 //                   deterministic-mode counters.
 //   fa_bwd_main     one CTA per (128-key tile, head, batch); loops over the
 //                   live 128-row query tiles:
-//                     S^T  = K Q^T            -> TMEM [0,128)       (tcgen05)
-//                     dP^T = V dO^T           -> TMEM [128,256)
-//                     P^T  = 2^(S^T*scale*log2e + bias - L2)  (bf16, each half over its own S^T half)
-//                     dV  += P^T dO           (A = P^T from TMEM)
-//                     dS^T = P^T o (dP^T - D) (bf16, to shared memory)
-//                     dK  += dS^T Q           (A = dS^T, K-major view)
-//                     dQ   = dS K             (A = the same buffer, MN-major view) -> TMEM [128,128+D)
-//                   and drains dQ into the fp32 accumulator with 16-byte atomic
-//                   adds (deterministic mode: in key-tile order, behind a
-//                   per-query-tile counter).
+//                     S^T  = K Q^T                 -> TMEM [0,128)     (tcgen05)
+//                     dP^T = V dO^T                -> TMEM [128,256)
+//                     P^T  = 2^(S^T*scale*log2e + bias - L2), stored over S^T as
+//                            bf16 hi/lo pairs (P = hi + lo to ~2^-16)
+//                     dV  += P_hi^T dO + P_lo^T dO (A from TMEM)
+//                     dS^T = P^T o (dP^T - D): bf16 hi/lo pairs over dP^T, and
+//                            fp16 to shared memory
+//                     dK  += dS_hi^T Q + dS_lo^T Q (A from TMEM)
+//                     dQ   = dS K in fp16 (K converted once per CTA) -> TMEM [128,128+D)
+//                   and drains dQ into the fp32 accumulator with 16-byte
+//                   reductions (deterministic mode: in key-tile order, behind
+//                   per-warp counters).
 //   fa_bwd_convert  dQ = bf16(scale * dQ_acc).
+// Precision: the gradients are compared against an fp64 reference with an
+// absolute bound close to bf16's own output rounding at |x| ~ 5, so the
+// operands of every gradient product carry ~16 significant bits (hi/lo bf16
+// pairs or fp16) rather than bf16's 8.
 // Warp roles in fa_bwd_main (512 threads): warp 0 TMA producer, warp 1 TMEM
 // allocator + MMA issuer, warps 4-11 two compute warpgroups (thread = key row,
 // each group one half of the 128 query columns), warps 12-15 dQ warpgroup
@@ -64,17 +70,19 @@ struct BwdCfg {
   static constexpr int PANELS = D / 64;
   static constexpr int PANEL_BYTES = 128 * 128;
   static constexpr int TILE_BYTES = PANELS * PANEL_BYTES;
-  static constexpr int NST = 2;
+  static constexpr int NQ = 2;                  // Q (+ L2, D) stages
+  static constexpr int NDO = D == 64 ? 2 : 1;   // dO stages
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = TILE_BYTES;
-  static constexpr int Q_OFF = 2 * TILE_BYTES;
-  static constexpr int DO_OFF = Q_OFF + NST * TILE_BYTES;
-  static constexpr int DS_OFF = DO_OFF + NST * TILE_BYTES;  // 128 keys x 128 queries bf16, two 64-query panels
-  static constexpr int VEC_OFF = DS_OFF + 2 * PANEL_BYTES;  // per stage: L2[128], D[128]
-  static constexpr int BAR_OFF = VEC_OFF + NST * 1024;
+  static constexpr int K16_OFF = 2 * TILE_BYTES;  // fp16 copy of K for the dQ product
+  static constexpr int Q_OFF = 3 * TILE_BYTES;
+  static constexpr int DO_OFF = Q_OFF + NQ * TILE_BYTES;
+  static constexpr int DS_OFF = DO_OFF + NDO * TILE_BYTES;  // 128 keys x 128 queries fp16, two 64-query panels
+  static constexpr int VEC_OFF = DS_OFF + 2 * PANEL_BYTES;  // per Q stage: L2[128], D[128]
+  static constexpr int BAR_OFF = VEC_OFF + NQ * 1024;
   static constexpr int SMEM_BYTES = BAR_OFF + 256;
   static constexpr int THREADS = 512;
-  static constexpr int STAGE_TX = 2 * TILE_BYTES + 1024;
+  static constexpr int Q_TX = TILE_BYTES + 1024;
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 128, T_DV = 256, T_DK = 256 + D;
   static_assert(T_DK + D <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -82,8 +90,8 @@ struct BwdCfg {
 
 struct BwdBars {
   uint64_t kv_full;
-  uint64_t full[2];
-  uint64_t empty[2];
+  uint64_t q_full[2], q_empty[2];
+  uint64_t do_full[2], do_empty[2];
   uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_free, acc_done, drain;
   uint32_t tmem_base;
   int abort;
@@ -102,6 +110,8 @@ enum : uint32_t {
   SITE_B_ACC = 0x3A,
   SITE_B_SEM = 0x3B,
   SITE_B_ALIGN = 0x3C,
+  SITE_B_DOEMPTY = 0x3D,
+  SITE_B_DOFULL = 0x3E,
 };
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -174,8 +184,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], 1);
+      mbar_init(&bars->q_full[s], 1);
+      mbar_init(&bars->q_empty[s], 1);
+      mbar_init(&bars->do_full[s], 1);
+      mbar_init(&bars->do_empty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
@@ -211,41 +223,50 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         tma_load_4d(smem + C::K_OFF + pn * C::PANEL_BYTES, &tm_k, &bars->kv_full, pn * 64, h, j0, b);
         tma_load_4d(smem + C::V_OFF + pn * C::PANEL_BYTES, &tm_v, &bars->kv_full, pn * 64, h, j0, b);
       }
-      int issued = 0;
+      int q_issued = 0, do_issued = 0;
       for (int ii = 0; ii < n_iter; ++ii) {
-        const int s = ii & 1;
-        if (!fa_wait(&bars->empty[s], (uint32_t(ii >> 1) & 1u) ^ 1u, watch, SITE_B_EMPTY)) break;
+        const int s = ii % C::NQ;
         const int i0 = (qt_first + ii) * 128;
-        mbar_arrive_expect_tx(&bars->full[s], C::STAGE_TX);
-        for (int pn = 0; pn < C::PANELS; ++pn) {
-          tma_load_4d(smem + C::Q_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bars->full[s], pn * 64,
+        if (!fa_wait(&bars->q_empty[s], (uint32_t(ii / C::NQ) & 1u) ^ 1u, watch, SITE_B_EMPTY)) break;
+        mbar_arrive_expect_tx(&bars->q_full[s], C::Q_TX);
+        for (int pn = 0; pn < C::PANELS; ++pn)
+          tma_load_4d(smem + C::Q_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bars->q_full[s], pn * 64,
                       h, i0, b);
-          tma_load_4d(smem + C::DO_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_do, &bars->full[s],
+        bulk_load(smem + C::VEC_OFF + s * 1024, p.l2 + vec_base + i0, 512, &bars->q_full[s]);
+        bulk_load(smem + C::VEC_OFF + s * 1024 + 512, p.dvec + vec_base + i0, 512, &bars->q_full[s]);
+        q_issued = ii + 1;
+        const int d = ii % C::NDO;
+        if (!fa_wait(&bars->do_empty[d], (uint32_t(ii / C::NDO) & 1u) ^ 1u, watch, SITE_B_DOEMPTY)) break;
+        mbar_arrive_expect_tx(&bars->do_full[d], C::TILE_BYTES);
+        for (int pn = 0; pn < C::PANELS; ++pn)
+          tma_load_4d(smem + C::DO_OFF + d * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_do, &bars->do_full[d],
                       pn * 64, h, i0, b);
-        }
-        bulk_load(smem + C::VEC_OFF + s * 1024, p.l2 + vec_base + i0, 512, &bars->full[s]);
-        bulk_load(smem + C::VEC_OFF + s * 1024 + 512, p.dvec + vec_base + i0, 512, &bars->full[s]);
-        issued = ii + 1;
+        do_issued = ii + 1;
       }
+      // every copy must land before the CTA may exit
       drain_wait_b(&bars->kv_full, 0);
-      for (int ii = (issued > 2 ? issued - 2 : 0); ii < issued; ++ii)
-        drain_wait_b(&bars->full[ii & 1], uint32_t(ii >> 1) & 1u);
+      for (int ii = (q_issued > C::NQ ? q_issued - C::NQ : 0); ii < q_issued; ++ii)
+        drain_wait_b(&bars->q_full[ii % C::NQ], uint32_t(ii / C::NQ) & 1u);
+      for (int ii = (do_issued > C::NDO ? do_issued - C::NDO : 0); ii < do_issued; ++ii)
+        drain_wait_b(&bars->do_full[ii % C::NDO], uint32_t(ii / C::NDO) & 1u);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_iter > 0) {
       constexpr uint32_t ID_SS = idesc_bf16_f32(128, 128, 0, 0);  // S^T, dP^T: both operands K-major
-      constexpr uint32_t ID_TN = idesc_bf16_f32(128, D, 0, 1);    // dV, dK: B (dO / Q) MN-major
-      constexpr uint32_t ID_DQ = idesc_bf16_f32(128, D, 1, 1);    // dQ: A (dS) and B (K) MN-major
+      constexpr uint32_t ID_TN = idesc_bf16_f32(128, D, 0, 1);    // dV, dK: A from TMEM, B (dO / Q) MN-major
+      constexpr uint32_t ID_DQ = idesc_f16_f32(128, D, 1, 1);     // dQ: fp16 A (dS) and B (K), MN-major
       const uint32_t k_a = smem_u32(smem + C::K_OFF);
       const uint32_t v_a = smem_u32(smem + C::V_OFF);
+      const uint32_t k16_a = smem_u32(smem + C::K16_OFF);
       const uint32_t ds_a = smem_u32(smem + C::DS_OFF);
       bool ok = fa_wait(&bars->kv_full, 0, watch, SITE_B_KV);
       for (int ii = 0; ii < n_iter && ok; ++ii) {
-        const int s = ii & 1;
+        const int s = ii % C::NQ;
+        const int d = ii % C::NDO;
         const uint32_t q_a = smem_u32(smem + C::Q_OFF + s * C::TILE_BYTES);
-        const uint32_t do_a = smem_u32(smem + C::DO_OFF + s * C::TILE_BYTES);
-        if (!(ok = fa_wait(&bars->full[s], uint32_t(ii >> 1) & 1u, watch, SITE_B_FULL))) break;
+        const uint32_t do_a = smem_u32(smem + C::DO_OFF + d * C::TILE_BYTES);
+        if (!(ok = fa_wait(&bars->q_full[s], uint32_t(ii / C::NQ) & 1u, watch, SITE_B_FULL))) break;
         tc_fence_after();
         // S^T = K Q^T
 #pragma unroll
@@ -258,8 +279,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         // dP^T = V dO^T, into the columns dQ of the previous tile occupied
         if (ii > 0) {
           if (!(ok = fa_wait(&bars->dq_free, uint32_t(ii - 1) & 1u, watch, SITE_B_DQFREE))) break;
-          tc_fence_after();
         }
+        if (!(ok = fa_wait(&bars->do_full[d], uint32_t(ii / C::NDO) & 1u, watch, SITE_B_DOFULL))) break;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
@@ -267,28 +289,33 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                  kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars->dp_full);
-        // dV += P^T dO
+        // dV += P_hi^T dO + P_lo^T dO ; queries 16kk.. sit at column 64*(kk/4) + 16*(kk%4) (hi), +8 (lo)
         if (!(ok = fa_wait(&bars->p_ready, uint32_t(ii) & 1u, watch, SITE_B_P))) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // queries 16kk.. live at column 64*(kk/4) + 8*(kk%4)
-          mma_ts(tmem + C::T_DV, tmem + C::T_S + (kk / 4) * 64 + (kk % 4) * 8,
-                 sdesc_sw128(do_a + kk * 2048, C::PANEL_BYTES, 1024), ID_TN, (ii > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q ; dQ = dS K
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t pa = tmem + C::T_S + (kk / 4) * 64 + (kk % 4) * 16;
+          const uint64_t bd = sdesc_sw128(do_a + kk * 2048, C::PANEL_BYTES, 1024);
+          mma_ts(tmem + C::T_DV, pa, bd, ID_TN, (ii > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::T_DV, pa + 8, bd, ID_TN, 1u);
+        }
+        mma_commit(&bars->do_empty[d]);
+        // dK += dS_hi^T Q + dS_lo^T Q ; dQ = dS K (fp16)
         if (!(ok = fa_wait(&bars->ds_ready, uint32_t(ii) & 1u, watch, SITE_B_DS))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
-          mma_ss(tmem + C::T_DK, sdesc_sw128(ds_a + off, 16, 1024),
-                 sdesc_sw128(q_a + kk * 2048, C::PANEL_BYTES, 1024), ID_TN, (ii > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t da = tmem + C::T_DP + (kk / 4) * 64 + (kk % 4) * 16;
+          const uint64_t bd = sdesc_sw128(q_a + kk * 2048, C::PANEL_BYTES, 1024);
+          mma_ts(tmem + C::T_DK, da, bd, ID_TN, (ii > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::T_DK, da + 8, bd, ID_TN, 1u);
         }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ss(tmem + C::T_DQ, sdesc_sw128(ds_a + kk * 2048, C::PANEL_BYTES, 1024),
-                 sdesc_sw128(k_a + kk * 2048, C::PANEL_BYTES, 1024), ID_DQ, kk > 0 ? 1u : 0u);
+                 sdesc_sw128(k16_a + kk * 2048, C::PANEL_BYTES, 1024), ID_DQ, kk > 0 ? 1u : 0u);
         mma_commit(&bars->dq_full);
-        mma_commit(&bars->empty[s]);
+        mma_commit(&bars->q_empty[s]);
       }
       if (ok) {
         mma_commit(&bars->acc_done);
@@ -326,37 +353,69 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const float slope_log2 = has_alibi ? p.alibi[b * p.alibi_bstride + h] * 1.4426950408889634f : 0.0f;
     const float sl = p.scale_log2;
     bool ok = true;
-    for (int ii = 0; ii < n_iter; ++ii) {
-      const int s = ii & 1;
+    // fp16 copy of K for the dQ product: same swizzled byte layout, element by element.
+    if (n_iter > 0) {
+      ok = fa_wait_warp(&bars->kv_full, 0, watch, SITE_B_KV);
+      if (ok) {
+        constexpr int CHUNKS = C::PANELS * 8;  // 16-byte chunks per K row
+        const uint8_t* src = smem + C::K_OFF;
+        uint8_t* dst = smem + C::K16_OFF;
+#pragma unroll
+        for (int cidx = w * (CHUNKS / 2); cidx < (w + 1) * (CHUNKS / 2); ++cidx) {
+          const int off = (cidx / 8) * C::PANEL_BYTES + r * 128 + (cidx % 8) * 16;
+          const uint4 u = *reinterpret_cast<const uint4*>(src + off);
+          const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            o[e] = pack_f16x2(__uint_as_float(wv[e] << 16), __uint_as_float(wv[e] & 0xFFFF0000u));
+          *reinterpret_cast<uint4*>(dst + off) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        fence_proxy_async_smem();
+      }
+    }
+    for (int ii = 0; ii < n_iter && ok; ++ii) {
+      const int s = ii % C::NQ;
       const int i0 = (qt_first + ii) * 128;
       const int ib = i0 + w * 64;  // first query of this half
-      const float* l2s = reinterpret_cast<const float*>(smem + C::VEC_OFF + s * 1024) + w * 64;
-      const float* dvs = l2s + 128;
+      const float4* l2v = reinterpret_cast<const float4*>(smem + C::VEC_OFF + s * 1024) + w * 16;
+      const float4* dvv = l2v + 32;
       if (!(ok = fa_wait_warp(&bars->s_full, uint32_t(ii) & 1u, watch, SITE_B_S))) break;
       tc_fence_after();
-      float pv[64];
-      tmem_ld_x64f(tmem + lane_addr + C::T_S + w * 64, pv);
-      const bool need_mask = !(tile_keys_ok && i0 >= qlo_max && i0 + 127 <= qhi_min);
-      if (has_alibi) {
-        const float d0 = float(ib + off - j);
-#pragma unroll
-        for (int c = 0; c < 64; ++c) pv[c] = fmaf(pv[c], sl, -slope_log2 * fabsf(d0 + float(c)) - l2s[c]);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) pv[c] = fmaf(pv[c], sl, -l2s[c]);
-      }
-#pragma unroll
-      for (int c = 0; c < 64; ++c) pv[c] = ex2_approx(pv[c]);
-      if (need_mask) {
-        const int lo = qlo - ib, hi = qhi - ib;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) pv[c] = (c >= lo && c <= hi) ? pv[c] : 0.0f;
-      }
       {
-        uint32_t pk[32];
+        float pv[64];
+        tmem_ld_x64f(tmem + lane_addr + C::T_S + w * 64, pv);
+        const bool need_mask = !(tile_keys_ok && i0 >= qlo_max && i0 + 127 <= qhi_min);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
-        tmem_st_x32(tmem + lane_addr + C::T_S + w * 64, pk);  // inside this group's own S^T columns
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 l4 = l2v[c4];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 4 * c4 + e;
+            float bias = -lv[e];
+            if (has_alibi) bias -= slope_log2 * fabsf(float(ib + off - j + c));
+            pv[c] = ex2_approx(fmaf(pv[c], sl, bias));
+          }
+        }
+        if (need_mask) {
+          const int lo = qlo - ib, hi = qhi - ib;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) pv[c] = (c >= lo && c <= hi) ? pv[c] : 0.0f;
+        }
+        // P as bf16 hi/lo pairs; 16-query chunk c4 -> columns [16*c4, 16*c4+8) hi, [+8, +16) lo
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t hl[16];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float a0 = pv[16 * c4 + 2 * e], a1 = pv[16 * c4 + 2 * e + 1];
+            const uint32_t hp = pack_bf16x2(a0, a1);
+            hl[e] = hp;
+            hl[8 + e] = pack_bf16x2(a0 - __uint_as_float(hp << 16), a1 - __uint_as_float(hp & 0xFFFF0000u));
+          }
+          tmem_st_x16(tmem + lane_addr + C::T_S + w * 64 + 16 * c4, hl);
+        }
       }
       tmem_st_wait();
       tc_fence_before();
@@ -366,26 +425,40 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tc_fence_after();
       uint8_t* ds_row = smem + C::DS_OFF + w * C::PANEL_BYTES + r * 128;
 #pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        float dp[32];
-        uint32_t pb[16];  // P^T of these 32 queries, bf16 pairs, as the dV MMA used it
-        tmem_ld_x32f(tmem + lane_addr + C::T_DP + w * 64 + c2 * 32, dp);
-        tmem_ld_x16(tmem + lane_addr + C::T_S + w * 64 + c2 * 16, pb);
-        uint32_t pk[16];
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float dp[16];
+        uint32_t ph[16];  // P hi (8) then lo (8) for these 16 queries
+        tmem_ld_x16f(tmem + lane_addr + C::T_DP + w * 64 + 16 * c4, dp);
+        tmem_ld_x16(tmem + lane_addr + C::T_S + w * 64 + 16 * c4, ph);
+        uint32_t hl[16];
+        uint32_t h16[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c = c2 * 32 + 2 * e;
-          const float p0 = __uint_as_float(pb[e] << 16), p1 = __uint_as_float(pb[e] & 0xFFFF0000u);
-          pk[e] = pack_bf16x2(p0 * (dp[2 * e] - dvs[c]), p1 * (dp[2 * e + 1] - dvs[c + 1]));
+        for (int e = 0; e < 8; ++e) {
+          const int c = 16 * c4 + 2 * e;
+          const float4 d4 = dvv[c / 4];
+          const float dv0 = (c % 4 == 0) ? d4.x : d4.z;
+          const float dv1 = (c % 4 == 0) ? d4.y : d4.w;
+          const float p0 = __uint_as_float(ph[e] << 16) + __uint_as_float(ph[8 + e] << 16);
+          const float p1 = __uint_as_float(ph[e] & 0xFFFF0000u) + __uint_as_float(ph[8 + e] & 0xFFFF0000u);
+          const float s0 = p0 * (dp[2 * e] - dv0);
+          const float s1 = p1 * (dp[2 * e + 1] - dv1);
+          const uint32_t hp = pack_bf16x2(s0, s1);
+          hl[e] = hp;
+          hl[8 + e] = pack_bf16x2(s0 - __uint_as_float(hp << 16), s1 - __uint_as_float(hp & 0xFFFF0000u));
+          h16[e] = pack_f16x2(s0, s1);
         }
+        // dS^T hi/lo over this chunk's own (already read) dP^T columns
+        tmem_st_x16(tmem + lane_addr + C::T_DP + w * 64 + 16 * c4, hl);
+        // fp16 dS for the dQ product: 16 queries = two 16-byte chunks of row r
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int chunk = (c2 * 4 + e) ^ (r & 7);
+        for (int e = 0; e < 2; ++e) {
+          const int chunk = (2 * c4 + e) ^ (r & 7);
           *reinterpret_cast<uint4*>(ds_row + chunk * 16) =
-              make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+              make_uint4(h16[4 * e], h16[4 * e + 1], h16[4 * e + 2], h16[4 * e + 3]);
         }
       }
       fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars->ds_ready);
     }

@@ -312,13 +312,17 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < 128; ++c) x[c] = (c >= lo && c <= hi) ? x[c] : -INFINITY;
       }
-      float mx0 = x[0], mx1 = x[1];
+      // row max: four independent chains of three-input max over x[0..127]
+      float mq[4];
 #pragma unroll
-      for (int c = 2; c < 128; c += 2) {
-        mx0 = fmaxf(mx0, x[c]);
-        mx1 = fmaxf(mx1, x[c + 1]);
+      for (int k = 0; k < 4; ++k) mq[k] = fmaxf(x[2 * k], x[2 * k + 1]);
+#pragma unroll
+      for (int c = 8; c < 128; c += 8) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mq[k] = max3f(mq[k], x[c + 2 * k], x[c + 2 * k + 1]);
       }
-      const float mx = fmaxf(mx0, mx1);
+      static_assert(8 + 15 * 8 == 128, "max loop covers exactly 128 columns");
+      const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       // block max in log2 units (without ALiBi, x still holds raw q.k)
       const float m_blk = has_alibi ? mx : mx * sl;
       const float m_new = fmaxf(m, m_blk);
@@ -335,7 +339,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
       const float m_use = (m == -INFINITY) ? 0.0f : m;
       // without ALiBi: p = 2^(x*sl - m); with ALiBi x is already in log2 units
       const float mul = has_alibi ? 1.0f : sl;
-      float rs0 = 0.0f, rs1 = 0.0f;
+      float rs[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t pk[16];
@@ -344,13 +348,13 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
           const int c = q4 * 32 + 2 * e;
           const float p0 = ex2_approx(fmaf(x[c], mul, -m_use));
           const float p1 = ex2_approx(fmaf(x[c + 1], mul, -m_use));
-          rs0 += p0;
-          rs1 += p1;
+          rs[(e & 1) * 2] += p0;
+          rs[(e & 1) * 2 + 1] += p1;
           pk[e] = pack_bf16x2(p0, p1);
         }
         tmem_st_x16(tmem + lane_addr + sb * 128 + q4 * 16, pk);
       }
-      l += rs0 + rs1;
+      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
       const bool rescale = alpha != 1.0f;
       if (__any_sync(0xffffffffu, rescale) && jj > 0) {
         // O must hold P_{j-1} V_{j-1} before it is rescaled (P_j is already in TMEM).

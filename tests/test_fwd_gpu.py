@@ -88,3 +88,26 @@ def test_fully_masked_rows_zero():
     o = to_f64(out)
     assert np.all(o[:, :150] == 0.0)
     assert np.all(np.isneginf(lse.cpu().numpy()[:, :, :150]))
+
+
+@pytest.mark.parametrize("Sq,Sk,D", [(400, 512, 128), (300, 300, 64), (129, 700, 256)])
+def test_one_key_window_returns_that_value_exactly(Sq, Sk, D):
+    # With window (0, 0) each query row i sees only key c(i) = i + Sk - Sq, so
+    # softmax weighs it 1 and O_i must equal V_c(i) bit for bit (bf16 V times
+    # exactly 1), with L_i = scale * q_i . k_c(i).
+    import torch
+
+    import exact_attention_56_gb300 as fa
+
+    inp = attention_inputs(1, Sq, Sk, 2, D, Sq + Sk)
+    q, k, v = (to_dev(inp[n]) for n in ("q", "k", "v"))
+    out, lse = fa.fa_fwd(q, k, v, window_size=(0, 0))
+    torch.cuda.synchronize()
+    c = np.arange(Sq) + Sk - Sq
+    live = c >= 0
+    vv = v.view(torch.int16).cpu().numpy()[0][c[live]]
+    oo = out.view(torch.int16).cpu().numpy()[0][live]
+    assert np.array_equal(oo, vv)
+    q64, k64 = bf16_bits_to_f64(inp["q"])[0], bf16_bits_to_f64(inp["k"])[0]
+    l_ref = np.einsum("ihd,ihd->hi", q64[live], k64[c[live]]) / math.sqrt(D)
+    assert np.max(np.abs(lse.cpu().numpy()[0][:, live] - l_ref)) <= 1e-3
