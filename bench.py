@@ -158,6 +158,28 @@ def _cpu_cores_used():
     return os.cpu_count() or 1
 
 
+def _traffic_per_launch(group, steps, launches_per_step):
+    """DRAM bytes per launch of a kernel group, from the committed ncu summary
+    (profiles/traffic.json), or None once the kernel source has changed since
+    the capture."""
+    import hashlib
+
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)[group]
+        with open(os.path.join(ROOT, t["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != t["source_sha256"]:
+                return None
+    except Exception:
+        return None
+    if "bytes_per_launch" in t:
+        return float(t["bytes_per_launch"])
+    if "bytes_per_key" in t:  # decode: per launch over the decode cache sizes
+        keys = sum(DECODE_B * DECODE_H * Sk for Sk in DECODE_SK) / len(DECODE_SK)
+        return float(t["bytes_per_key"]) * keys
+    return None
+
+
 def oracle_sample(budget_s=12.0, points=None):
     """Time the fp64 oracle (fwd + bwd of single heads) on a bounded sample of the sweep.
 
@@ -345,7 +367,7 @@ def run_ours(args):
         peak = float(peaks.get("hbm_gbs", PEAK_FALLBACK["hbm_gbs"]))
         unit = "GB/s"
     roofline = {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": None, "peak_source": f"{peak_src} (sustained bf16)"
+                "frac": achieved / peak, "traffic": _traffic_per_launch(dom, K, launches_per_step), "peak_source": f"{peak_src} (sustained bf16)"
                 if bound == "tensor" else f"{peak_src} (copy bandwidth)", "per_launch_ms_avg": per_launch_ms}
 
     sweep = []
