@@ -127,6 +127,28 @@ int fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, v
                       int alibi_batch_stride, int num_splits, fa_stream_t stream);
 
 /*
+ * Split-KV decode that allocates nothing and takes no workspace. The pages
+ * have no counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory where they run decode (an allocation-free serving
+ * loop, a runtime that owns all device memory through its own allocator, a
+ * host that forbids allocation after start-up). Arguments, layouts and
+ * results are those of fa_decode_splitkv minus the workspace: the split
+ * partials live in an 8 MiB array of the library's own device memory, which
+ * every GPU that loads the library holds until the process exits.
+ * - Returns FA_ERR_WORKSPACE if fa_decode_workspace_size() for the request
+ *   exceeds 8 MiB (8388608 bytes).
+ * - The first call on a device looks up the array's device address (with
+ *   that device current); make it before any stream capture.
+ * - All calls share the array: calls whose kernels may overlap on the GPU
+ *   (other streams, other host threads) race; serialise them. No part of the
+ *   array has to start at zero: each call writes every partial it reads.
+ */
+int fa_decode_splitkv_noalloc(const void* q, const void* k_cache, const void* v_cache, void* out, float* lse,
+                              int B, int Sq, int Sk, int H, int D, float scale, int causal, int window_left,
+                              int window_right, const float* alibi_slopes, int alibi_batch_stride, int num_splits,
+                              fa_stream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word of
  * the current device. Returns FA_OK, FA_ERR_TIMEOUT (a kernel's bounded
  * wait expired; *detail receives the raw word: wait-site code in the low
