@@ -21,9 +21,11 @@
 //                            fp16 to shared memory
 //                     dK  += dS_hi^T Q + dS_lo^T Q (A from TMEM)
 //                     dQ   = dS K in fp16 (K converted once per CTA) -> TMEM [128,128+D)
-//                   and drains dQ into the fp32 accumulator with 16-byte
-//                   reductions (deterministic mode: in key-tile order, behind
-//                   per-warp counters).
+//                   and drains dQ from TMEM into a swizzled shared-memory stage
+//                   (the dS buffer, free once the dQ MMA has read it), from where
+//                   TMA bulk reduce-adds it into the fp32 accumulator in L2
+//                   (deterministic mode: in key-tile order, behind a counter per
+//                   query tile).
 //   fa_bwd_convert  dQ = bf16(scale * dQ_acc).
 // Precision: the gradients are compared against an fp64 reference with an
 // absolute bound close to bf16's own output rounding at |x| ~ 5, so the
@@ -93,6 +95,7 @@ struct BwdBars {
   uint64_t q_full[2], q_empty[2];
   uint64_t do_full[2], do_empty[2];
   uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_free, acc_done, drain;
+  uint64_t staged[2], half_free[2], stage_done;
   uint32_t tmem_base;
   int abort;
 };
@@ -112,6 +115,7 @@ enum : uint32_t {
   SITE_B_ALIGN = 0x3C,
   SITE_B_DOEMPTY = 0x3D,
   SITE_B_DOFULL = 0x3E,
+  SITE_B_STAGE = 0x3F,
 };
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -120,12 +124,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
           smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
-}
-
-// Fire-and-forget 16-byte fp32 add to global memory (no value returned).
-__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
 }
 
 __device__ __forceinline__ void drain_wait_b(uint64_t* bar, uint32_t parity) {
@@ -155,7 +153,7 @@ template <int D>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                       const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {  // the swizzled layouts need 1024-byte alignment
@@ -197,6 +195,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(&bars->dq_free, 128);
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->drain, 1);
+    for (int hh = 0; hh < 2; ++hh) {
+      mbar_init(&bars->staged[hh], 128);
+      mbar_init(&bars->half_free[hh], 1);
+    }
+    mbar_init(&bars->stage_done, 1);
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -422,6 +425,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       mbar_arrive(&bars->p_ready);
 
       if (!(ok = fa_wait_warp(&bars->dp_full, uint32_t(ii) & 1u, watch, SITE_B_DP))) break;
+      // the dS buffer doubles as the previous tile's dQ stage: wait until TMA has read it
+      if (ii > 0 && !(ok = fa_wait_warp(&bars->stage_done, uint32_t(ii - 1) & 1u, watch, SITE_B_STAGE))) break;
       tc_fence_after();
       uint8_t* ds_row = smem + C::DS_OFF + w * C::PANEL_BYTES + r * 128;
 #pragma unroll
@@ -487,55 +492,82 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
   } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ drain (thread = query row)
+    // TMEM -> shared stage (two 16 KB halves of 128 rows x 32 fp32, 128-byte
+    // swizzle, in the dS buffer) -> TMA reduce-add into dQ_acc. Thread r == 0
+    // issues the bulk operations; the handshakes are bounded mbarrier waits.
+    constexpr int NCH = D / 32;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const uint32_t lane_addr = uint32_t(wq * 32) << 16;
+    uint8_t* stage = smem + C::DS_OFF;
+    uint32_t staged_ph[2] = {0u, 0u};
     for (int ii = 0; ii < n_iter; ++ii) {
       const int qt = qt_first + ii;
-      const int i = qt * 128 + r;
       if (!fa_wait_warp(&bars->dq_full, uint32_t(ii) & 1u, watch, SITE_B_DQ)) break;
       tc_fence_after();
-      // Deterministic mode: warp wq adds its 32 rows of this query tile only after
-      // warp wq of every earlier key tile has (counter per (query tile, quarter)).
-      int* sem = p.sem + ((size_t(b) * p.H + h) * p.n_qt + qt) * 4 + wq;
-      if (p.deterministic) {
-        bool turn = true;
-        if (lane == 0) {
-          const int rank = kt - first_ktile(qt, p);
-          const uint64_t t0 = globaltimer_ns();
-          int v;
-          for (;;) {
-            asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(sem) : "memory");
-            if (v == rank) break;
-            if (*watch.abort || globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) {
-              *watch.abort = 1;
-              atomicOr(p.status, FA_DEV_TIMEOUT | SITE_B_SEM);
-              turn = false;
-              break;
+      bool ok = true;
+#pragma unroll 1
+      for (int cc = 0; cc < NCH && ok; ++cc) {
+        const int hh = cc & 1;
+        if (cc >= 2 && !(ok = fa_wait_warp(&bars->half_free[hh], uint32_t(ii) & 1u, watch, SITE_B_STAGE))) break;
+        float a[32];
+        tmem_ld_x32f(tmem + lane_addr + C::T_DQ + cc * 32, a);
+        uint8_t* row = stage + hh * C::PANEL_BYTES + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<float4*>(row + ((c ^ (r & 7)) << 4)) =
+              make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
+        if (cc == NCH - 1) {  // TMEM fully read: the next dP^T may overwrite it
+          tc_fence_before();
+          mbar_arrive(&bars->dq_free);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->staged[hh]);
+        if (r == 0) {
+          ok = fa_wait(&bars->staged[hh], staged_ph[hh], watch, SITE_B_STAGE);
+          if (ok && p.deterministic && cc == 0) {
+            // wait for every earlier key tile of this query tile to have finished its adds
+            int* sem = p.sem + ((size_t(b) * p.H + h) * p.n_qt + qt) * 4;
+            const int rank = kt - first_ktile(qt, p);
+            const uint64_t t0 = globaltimer_ns();
+            int v;
+            for (;;) {
+              asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(sem) : "memory");
+              if (v == rank) break;
+              if (*watch.abort || globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) {
+                *watch.abort = 1;
+                atomicOr(p.status, FA_DEV_TIMEOUT | SITE_B_SEM);
+                ok = false;
+                break;
+              }
+            }
+          }
+          if (ok) {
+            tma_reduce_add_4d(&tm_dq, stage + hh * C::PANEL_BYTES, cc * 32, h, qt * 128, b);
+            bulk_commit_group();
+            if (cc >= 1 && cc + 1 < NCH) {  // chunk cc-1 read out: its half is free for chunk cc+1
+              bulk_wait_group_read<1>();
+              mbar_arrive(&bars->half_free[(cc - 1) & 1]);
             }
           }
         }
-        if (!__shfl_sync(0xffffffffu, turn ? 1 : 0, 0)) break;
+        staged_ph[hh] ^= 1u;
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0 && !*watch.abort;
       }
-      float* dst = p.dq_acc + ((size_t(b) * p.Sq + size_t(i)) * p.H + h) * size_t(D);
-      const bool row_ok = i < p.Sq;
-#pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
-        float a[32];
-        tmem_ld_x32f(tmem + lane_addr + C::T_DQ + cc * 32, a);
-        if (row_ok) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) red_add_v4(dst + cc * 32 + 4 * e, a[4 * e], a[4 * e + 1], a[4 * e + 2], a[4 * e + 3]);
+      if (!ok) break;
+      if (r == 0) {
+        bulk_wait_group_read<0>();
+        if (p.deterministic) {
+          bulk_wait_group<0>();
+          __threadfence();
+          int* sem = p.sem + ((size_t(b) * p.H + h) * p.n_qt + qt) * 4;
+          asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
         }
+        mbar_arrive(&bars->stage_done);
       }
-      tc_fence_before();
-      mbar_arrive(&bars->dq_free);
-      if (p.deterministic) {
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
-      }
+      __syncwarp();
     }
+    if (lane == 0) bulk_wait_group<0>();  // no bulk operation may outlive the CTA
   }
 
   tc_fence_before();
@@ -656,7 +688,9 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
   auto kern = fa_bwd_main_kernel<D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
     return FA_ERR_CUDA;
-  kern<<<dim3((s.Sk + 127) / 128, s.H, s.B), C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
+  CUtensorMap mdq;
+  if (!make_bshd_f32_map(&mdq, p.dq_acc, s.B, s.Sq, s.H, D)) return FA_ERR_CUDA;
+  kern<<<dim3((s.Sk + 127) / 128, s.H, s.B), C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, mdq, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   const size_t n8 = size_t(s.B) * s.Sq * s.H * D / 8;
   size_t nb = (n8 + 255) / 256;

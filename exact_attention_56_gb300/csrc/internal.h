@@ -27,6 +27,10 @@ int device_sm_count();
 // x 1 batch. Returns false if the driver rejects it.
 bool make_bshd_map(CUtensorMap* map, const void* base, int B, int S, int H, int D, int box_rows);
 
+// Encodes a 4-D tiled TMA map over a (B, S, H, D) fp32 tensor: box of 32
+// elements (128 B, 128-byte swizzle) x 1 head x 128 rows x 1 batch.
+bool make_bshd_f32_map(CUtensorMap* map, const void* base, int B, int S, int H, int D);
+
 // Kernel launchers (return an fa_status value).
 int fwd_launch(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,
                cudaStream_t stream);
