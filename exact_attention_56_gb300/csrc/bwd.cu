@@ -2,39 +2,44 @@
 //
 // Method (page "FlashAttention：快速且内存高效的准确注意力机制", sections
 // "反向传播" and "并行性 / 反向传播"): only the row logsumexp L is kept from
-// the forward; P is recomputed tile by tile from it; the work is parallel over
-// key/value column blocks, and dQ is accumulated across blocks by atomic adds.
-// Section "2.4" adds a deterministic variant.
+// the forward and P is recomputed tile by tile from it. Section "2.4" asks
+// for a deterministic variant.
 //
-// Three kernels:
-//   fa_bwd_pre      D_i = rowsum(dO_i * O_i), L2_i = L_i*log2(e) (padded to
-//                   128-row tiles), zeroes the fp32 dQ accumulator and the
-//                   deterministic-mode counters.
-//   fa_bwd_main     one CTA per (128-key tile, head, batch); loops over the
-//                   live 128-row query tiles:
-//                     S^T  = K Q^T                 -> TMEM [0,128)     (tcgen05)
-//                     dP^T = V dO^T                -> TMEM [128,256)
-//                     P^T  = 2^(S^T*scale*log2e + bias - L2), stored over S^T as
-//                            bf16 hi/lo pairs (P = hi + lo to ~2^-16)
-//                     dV  += P_hi^T dO + P_lo^T dO (A from TMEM)
-//                     dS^T = P^T o (dP^T - D): bf16 hi/lo pairs over dP^T, and
-//                            fp16 to shared memory
-//                     dK  += dS_hi^T Q + dS_lo^T Q (A from TMEM)
-//                     dQ   = dS K in fp16 (K converted once per CTA) -> TMEM [128,128+D)
-//                   and drains dQ from TMEM into a swizzled shared-memory stage
-//                   (the dS buffer, free once the dQ MMA has read it), from where
-//                   TMA bulk reduce-adds it into the fp32 accumulator in L2
-//                   (deterministic mode: in key-tile order, behind a counter per
-//                   query tile).
-//   fa_bwd_convert  dQ = bf16(scale * dQ_acc).
+// The page's own design parallelises over key/value column blocks and adds
+// dQ across blocks with atomics. On GB300 the fp32 reductions for dQ
+// (64 KB per 128x128 tile pair) saturate L2's reduction rate well before the
+// tensor cores, so this backward never reduces across CTAs:
+//
+//   fa_bwd_pre       D_i = rowsum(dO_i * O_i) and L2_i = L_i*log2(e), padded to
+//                    128-row tiles (+inf on padding and on rows without keys).
+//   fa_bwd_dkdv      one CTA per (128-key tile, head, batch), looping over the
+//                    live 128-row query tiles:
+//                      S^T  = K Q^T                 -> TMEM [0,128)      (tcgen05)
+//                      dP^T = V dO^T                -> TMEM [128,256)
+//                      P^T  = 2^(S^T*scale*log2e + bias - L2): bf16 hi/lo pairs
+//                             written over S^T (P = hi + lo to ~2^-16); P itself
+//                             stays in registers for dS
+//                    issued in the order dP^T(i), dV(i), S^T(i+1), dK(i), so the
+//                    next tile's S^T and P overlap this tile's dS and dK.
+//                      dV  += P_hi^T dO + P_lo^T dO (A from TMEM)
+//                      dS^T = P^T o (dP^T - D): bf16 hi/lo pairs over dP^T
+//                      dK  += dS_hi^T Q + dS_lo^T Q
+//                    then writes dK (times scale) and dV.
+//   fa_bwd_dq        one CTA per (128-row query tile, head, batch), looping over
+//                    the live key tiles (the forward's shape, thread = query row):
+//                      S  = Q K^T -> TMEM (double-buffered), P = 2^(S*... - L2)
+//                      dP = dO V^T, dS = P o (dP - D): hi/lo pairs over the
+//                             consumed S buffer
+//                      dQ += dS_hi K + dS_lo K (A from TMEM, K as MN-major B)
+//                    issued in the order dP(j+1), dQ(j), S(j+2) once dS(j) is formed.
+//                    then writes dQ (times scale) once.
+// Every output element is produced by one CTA in a fixed order, so every run
+// is bitwise reproducible; the deterministic flag costs nothing.
+//
 // Precision: the gradients are compared against an fp64 reference with an
 // absolute bound close to bf16's own output rounding at |x| ~ 5, so the
-// operands of every gradient product carry ~16 significant bits (hi/lo bf16
-// pairs or fp16) rather than bf16's 8.
-// Warp roles in fa_bwd_main (512 threads): warp 0 TMA producer, warp 1 TMEM
-// allocator + MMA issuer, warps 4-11 two compute warpgroups (thread = key row,
-// each group one half of the 128 query columns), warps 12-15 dQ warpgroup
-// (thread = query row).
+// operands the gradient products read from TMEM carry ~16 significant bits
+// (bf16 hi/lo pairs) rather than bf16's 8.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -50,10 +55,8 @@ struct BwdParams {
   const __nv_bfloat16* dout;
   const __nv_bfloat16* out;
   const float* lse;
-  float* dq_acc;   // (B, Sq, H, D) fp32
-  float* l2;       // (B, H, Sq_pad): L * log2(e); +inf on rows without keys and on padding
-  float* dvec;     // (B, H, Sq_pad): rowsum(dO * O)
-  int* sem;        // (B, H, n_qt, 4) ordering counters (deterministic mode)
+  float* l2;    // (B, H, Sq_pad): L * log2(e); +inf on rows without keys and on padding
+  float* dvec;  // (B, H, Sq_pad): rowsum(dO * O)
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -63,59 +66,30 @@ struct BwdParams {
   int wl, wr;
   float scale;
   float scale_log2;
-  int deterministic;
   unsigned int* status;
 };
 
-template <int D>
-struct BwdCfg {
-  static constexpr int PANELS = D / 64;
-  static constexpr int PANEL_BYTES = 128 * 128;
-  static constexpr int TILE_BYTES = PANELS * PANEL_BYTES;
-  static constexpr int NQ = 2;                  // Q (+ L2, D) stages
-  static constexpr int NDO = D == 64 ? 2 : 1;   // dO stages
-  static constexpr int K_OFF = 0;
-  static constexpr int V_OFF = TILE_BYTES;
-  static constexpr int K16_OFF = 2 * TILE_BYTES;  // fp16 copy of K for the dQ product
-  static constexpr int Q_OFF = 3 * TILE_BYTES;
-  static constexpr int DO_OFF = Q_OFF + NQ * TILE_BYTES;
-  static constexpr int DS_OFF = DO_OFF + NDO * TILE_BYTES;  // 128 keys x 128 queries fp16, two 64-query panels
-  static constexpr int VEC_OFF = DS_OFF + 2 * PANEL_BYTES;  // per Q stage: L2[128], D[128]
-  static constexpr int BAR_OFF = VEC_OFF + NQ * 1024;
-  static constexpr int SMEM_BYTES = BAR_OFF + 256;
-  static constexpr int THREADS = 512;
-  static constexpr int Q_TX = TILE_BYTES + 1024;
-  static constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 128, T_DV = 256, T_DK = 256 + D;
-  static_assert(T_DK + D <= 512, "TMEM budget");
-  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-};
-
-struct BwdBars {
-  uint64_t kv_full;
-  uint64_t q_full[2], q_empty[2];
-  uint64_t do_full[2], do_empty[2];
-  uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_free, acc_done, drain;
-  uint64_t staged[2], half_free[2], stage_done;
-  uint32_t tmem_base;
-  int abort;
-};
-
 enum : uint32_t {
-  SITE_B_EMPTY = 0x31,
-  SITE_B_KV = 0x32,
-  SITE_B_FULL = 0x33,
-  SITE_B_DQFREE = 0x34,
-  SITE_B_P = 0x35,
-  SITE_B_DS = 0x36,
-  SITE_B_S = 0x37,
-  SITE_B_DP = 0x38,
-  SITE_B_DQ = 0x39,
-  SITE_B_ACC = 0x3A,
-  SITE_B_SEM = 0x3B,
-  SITE_B_ALIGN = 0x3C,
-  SITE_B_DOEMPTY = 0x3D,
-  SITE_B_DOFULL = 0x3E,
-  SITE_B_STAGE = 0x3F,
+  SITE_KV_EMPTY = 0x31,
+  SITE_KV_KV = 0x32,
+  SITE_KV_QFULL = 0x33,
+  SITE_KV_DOFULL = 0x34,
+  SITE_KV_P = 0x35,
+  SITE_KV_DS = 0x36,
+  SITE_KV_S = 0x37,
+  SITE_KV_DP = 0x38,
+  SITE_KV_ACC = 0x39,
+  SITE_KV_DOEMPTY = 0x3A,
+  SITE_KV_ALIGN = 0x3B,
+  SITE_DQ_EMPTY = 0x41,
+  SITE_DQ_Q = 0x42,
+  SITE_DQ_K = 0x43,
+  SITE_DQ_V = 0x44,
+  SITE_DQ_DS = 0x45,
+  SITE_DQ_S = 0x46,
+  SITE_DQ_DP = 0x47,
+  SITE_DQ_ACC = 0x48,
+  SITE_DQ_ALIGN = 0x49,
 };
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -126,6 +100,7 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// Timeout-only wait used while draining after an abort.
 __device__ __forceinline__ void drain_wait_b(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
   const uint64_t t0 = globaltimer_ns();
@@ -144,23 +119,63 @@ __device__ __forceinline__ bool qtile_meets(int qt, int kt, const BwdParams& p) 
   if (hi < lo) return false;
   return !(hi < kt * 128 || lo > kt * 128 + 127);
 }
-// First key tile that meets query tile qt (its rank base for deterministic ordering).
-__device__ __forceinline__ int first_ktile(int qt, const BwdParams& p) {
-  return live_range(qt * 128, p.Sq, p.Sk, p.wl, p.wr).lo / 128;
+
+// Splits an fp32 pair into bf16 hi (x rounded) and lo (x - hi rounded) packs.
+__device__ __forceinline__ void split_hilo(float a0, float a1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16x2(a0, a1);
+  float r0, r1;
+  f2_unpack(f2_sub(f2_pack(a0, a1), f2_pack(__uint_as_float(hi << 16), __uint_as_float(hi & 0xFFFF0000u))), r0, r1);
+  lo = pack_bf16x2(r0, r1);
+}
+// dS pair = P * (dP - D) with packed ops.
+__device__ __forceinline__ void ds_pair(float p0, float p1, float dp0, float dp1, float d0, float d1, float& s0,
+                                        float& s1) {
+  f2_unpack(f2_mul(f2_pack(p0, p1), f2_sub(f2_pack(dp0, dp1), f2_pack(d0, d1))), s0, s1);
 }
 
+// ============================================================================ dK / dV
 template <int D>
-__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
-    fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+struct KvCfg {
+  static constexpr int PANELS = D / 64;
+  static constexpr int PANEL_BYTES = 128 * 128;
+  static constexpr int TILE_BYTES = PANELS * PANEL_BYTES;
+  static constexpr int NQ = 2;   // Q (+ L2, D) stages
+  static constexpr int NDO = 2;  // dO stages
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = TILE_BYTES;
+  static constexpr int Q_OFF = 2 * TILE_BYTES;
+  static constexpr int DO_OFF = Q_OFF + NQ * TILE_BYTES;
+  static constexpr int VEC_OFF = DO_OFF + NDO * TILE_BYTES;  // per Q stage: L2[128], D[128]
+  static constexpr int BAR_OFF = VEC_OFF + NQ * 1024;
+  static constexpr int SMEM_BYTES = BAR_OFF + 256;
+  static constexpr int THREADS = 384;
+  static constexpr int Q_TX = TILE_BYTES + 1024;
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
+  static_assert(T_DK + D <= 512, "TMEM budget");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+struct KvBars {
+  uint64_t kv_full;
+  uint64_t q_full[2], q_empty[2];
+  uint64_t do_full[2], do_empty[2];
+  uint64_t s_full, dp_full, p_ready, ds_ready, acc_done, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int D>
+__global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
+    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                       const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
-  using C = BwdCfg<D>;
+                       const BwdParams p) {
+  using C = KvCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {  // the swizzled layouts need 1024-byte alignment
-    if (threadIdx.x == 0) atomicOr(p.status, FA_DEV_TIMEOUT | SITE_B_ALIGN);
+    if (threadIdx.x == 0) atomicOr(p.status, FA_DEV_TIMEOUT | SITE_KV_ALIGN);
     return;
   }
-  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::BAR_OFF);
+  KvBars* bars = reinterpret_cast<KvBars*>(smem + C::BAR_OFF);
   const int warp = int(warp_id());
   const int lane = int(lane_id());
   const int kt = blockIdx.x;
@@ -169,9 +184,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const int j0 = kt * 128;
 
   // Live query tiles of this key tile: a contiguous range.
-  const int n_qt = p.n_qt;
-  int qt_first = n_qt, qt_last = -1;
-  for (int qt = 0; qt < n_qt; ++qt) {
+  int qt_first = p.n_qt, qt_last = -1;
+  for (int qt = 0; qt < p.n_qt; ++qt) {
     if (qtile_meets(qt, kt, p)) {
       qt_first = min(qt_first, qt);
       qt_last = qt;
@@ -191,15 +205,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_ready, 256);
     mbar_init(&bars->ds_ready, 256);
-    mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_free, 128);
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->drain, 1);
-    for (int hh = 0; hh < 2; ++hh) {
-      mbar_init(&bars->staged[hh], 128);
-      mbar_init(&bars->half_free[hh], 1);
-    }
-    mbar_init(&bars->stage_done, 1);
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -230,7 +237,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       for (int ii = 0; ii < n_iter; ++ii) {
         const int s = ii % C::NQ;
         const int i0 = (qt_first + ii) * 128;
-        if (!fa_wait(&bars->q_empty[s], (uint32_t(ii / C::NQ) & 1u) ^ 1u, watch, SITE_B_EMPTY)) break;
+        if (!fa_wait(&bars->q_empty[s], (uint32_t(ii / C::NQ) & 1u) ^ 1u, watch, SITE_KV_EMPTY)) break;
         mbar_arrive_expect_tx(&bars->q_full[s], C::Q_TX);
         for (int pn = 0; pn < C::PANELS; ++pn)
           tma_load_4d(smem + C::Q_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bars->q_full[s], pn * 64,
@@ -239,7 +246,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         bulk_load(smem + C::VEC_OFF + s * 1024 + 512, p.dvec + vec_base + i0, 512, &bars->q_full[s]);
         q_issued = ii + 1;
         const int d = ii % C::NDO;
-        if (!fa_wait(&bars->do_empty[d], (uint32_t(ii / C::NDO) & 1u) ^ 1u, watch, SITE_B_DOEMPTY)) break;
+        if (!fa_wait(&bars->do_empty[d], (uint32_t(ii / C::NDO) & 1u) ^ 1u, watch, SITE_KV_DOEMPTY)) break;
         mbar_arrive_expect_tx(&bars->do_full[d], C::TILE_BYTES);
         for (int pn = 0; pn < C::PANELS; ++pn)
           tma_load_4d(smem + C::DO_OFF + d * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_do, &bars->do_full[d],
@@ -258,20 +265,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     if (lane == 0 && n_iter > 0) {
       constexpr uint32_t ID_SS = idesc_bf16_f32(128, 128, 0, 0);  // S^T, dP^T: both operands K-major
       constexpr uint32_t ID_TN = idesc_bf16_f32(128, D, 0, 1);    // dV, dK: A from TMEM, B (dO / Q) MN-major
-      constexpr uint32_t ID_DQ = idesc_f16_f32(128, D, 1, 1);     // dQ: fp16 A (dS) and B (K), MN-major
       const uint32_t k_a = smem_u32(smem + C::K_OFF);
       const uint32_t v_a = smem_u32(smem + C::V_OFF);
-      const uint32_t k16_a = smem_u32(smem + C::K16_OFF);
-      const uint32_t ds_a = smem_u32(smem + C::DS_OFF);
-      bool ok = fa_wait(&bars->kv_full, 0, watch, SITE_B_KV);
-      for (int ii = 0; ii < n_iter && ok; ++ii) {
-        const int s = ii % C::NQ;
-        const int d = ii % C::NDO;
-        const uint32_t q_a = smem_u32(smem + C::Q_OFF + s * C::TILE_BYTES);
-        const uint32_t do_a = smem_u32(smem + C::DO_OFF + d * C::TILE_BYTES);
-        if (!(ok = fa_wait(&bars->q_full[s], uint32_t(ii / C::NQ) & 1u, watch, SITE_B_FULL))) break;
-        tc_fence_after();
-        // S^T = K Q^T
+      auto issue_st = [&](int ii) {  // S^T = K Q^T (overwrites P^T of tile ii-1: its dV was issued earlier)
+        const uint32_t q_a = smem_u32(smem + C::Q_OFF + (ii % C::NQ) * C::TILE_BYTES);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
@@ -279,11 +276,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                  kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars->s_full);
-        // dP^T = V dO^T, into the columns dQ of the previous tile occupied
-        if (ii > 0) {
-          if (!(ok = fa_wait(&bars->dq_free, uint32_t(ii - 1) & 1u, watch, SITE_B_DQFREE))) break;
-        }
-        if (!(ok = fa_wait(&bars->do_full[d], uint32_t(ii / C::NDO) & 1u, watch, SITE_B_DOFULL))) break;
+      };
+      bool ok = fa_wait(&bars->kv_full, 0, watch, SITE_KV_KV);
+      if (ok && (ok = fa_wait(&bars->q_full[0], 0, watch, SITE_KV_QFULL))) {
+        tc_fence_after();
+        issue_st(0);
+      }
+      // Order per tile ii: dP^T(ii), dV(ii), S^T(ii+1), dK(ii). S^T of the next tile
+      // is computed while this tile's dS is formed, and its P while dK runs.
+      for (int ii = 0; ii < n_iter && ok; ++ii) {
+        const int s = ii % C::NQ;
+        const int d = ii % C::NDO;
+        const uint32_t q_a = smem_u32(smem + C::Q_OFF + s * C::TILE_BYTES);
+        const uint32_t do_a = smem_u32(smem + C::DO_OFF + d * C::TILE_BYTES);
+        // dP^T = V dO^T (overwrites dS^T of tile ii-1: its dK was issued earlier)
+        if (!(ok = fa_wait(&bars->do_full[d], uint32_t(ii / C::NDO) & 1u, watch, SITE_KV_DOFULL))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -293,7 +300,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
         mma_commit(&bars->dp_full);
         // dV += P_hi^T dO + P_lo^T dO ; queries 16kk.. sit at column 64*(kk/4) + 16*(kk%4) (hi), +8 (lo)
-        if (!(ok = fa_wait(&bars->p_ready, uint32_t(ii) & 1u, watch, SITE_B_P))) break;
+        if (!(ok = fa_wait(&bars->p_ready, uint32_t(ii) & 1u, watch, SITE_KV_P))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -303,8 +310,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           mma_ts(tmem + C::T_DV, pa + 8, bd, ID_TN, 1u);
         }
         mma_commit(&bars->do_empty[d]);
-        // dK += dS_hi^T Q + dS_lo^T Q ; dQ = dS K (fp16)
-        if (!(ok = fa_wait(&bars->ds_ready, uint32_t(ii) & 1u, watch, SITE_B_DS))) break;
+        if (ii + 1 < n_iter) {
+          if (!(ok = fa_wait(&bars->q_full[(ii + 1) % C::NQ], uint32_t((ii + 1) / C::NQ) & 1u, watch,
+                             SITE_KV_QFULL)))
+            break;
+          tc_fence_after();
+          issue_st(ii + 1);
+        }
+        // dK += dS_hi^T Q + dS_lo^T Q
+        if (!(ok = fa_wait(&bars->ds_ready, uint32_t(ii) & 1u, watch, SITE_KV_DS))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -313,11 +327,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           mma_ts(tmem + C::T_DK, da, bd, ID_TN, (ii > 0 || kk > 0) ? 1u : 0u);
           mma_ts(tmem + C::T_DK, da + 8, bd, ID_TN, 1u);
         }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + C::T_DQ, sdesc_sw128(ds_a + kk * 2048, C::PANEL_BYTES, 1024),
-                 sdesc_sw128(k16_a + kk * 2048, C::PANEL_BYTES, 1024), ID_DQ, kk > 0 ? 1u : 0u);
-        mma_commit(&bars->dq_full);
         mma_commit(&bars->q_empty[s]);
       }
       if (ok) {
@@ -327,7 +336,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         drain_wait_b(&bars->drain, 0);
       }
     }
-  } else if (warp >= 4 && warp < 12) {
+  } else if (warp >= 4) {
     // ------------------------------------------------------------ compute (thread = key row)
     const int w = (warp - 4) / 4;  // query-column half
     const int wq = warp & 3;
@@ -356,113 +365,76 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const float slope_log2 = has_alibi ? p.alibi[b * p.alibi_bstride + h] * 1.4426950408889634f : 0.0f;
     const float sl = p.scale_log2;
     bool ok = true;
-    // fp16 copy of K for the dQ product: same swizzled byte layout, element by element.
-    if (n_iter > 0) {
-      ok = fa_wait_warp(&bars->kv_full, 0, watch, SITE_B_KV);
-      if (ok) {
-        constexpr int CHUNKS = C::PANELS * 8;  // 16-byte chunks per K row
-        const uint8_t* src = smem + C::K_OFF;
-        uint8_t* dst = smem + C::K16_OFF;
-#pragma unroll
-        for (int cidx = w * (CHUNKS / 2); cidx < (w + 1) * (CHUNKS / 2); ++cidx) {
-          const int off = (cidx / 8) * C::PANEL_BYTES + r * 128 + (cidx % 8) * 16;
-          const uint4 u = *reinterpret_cast<const uint4*>(src + off);
-          const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-          uint32_t o[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            o[e] = pack_f16x2(__uint_as_float(wv[e] << 16), __uint_as_float(wv[e] & 0xFFFF0000u));
-          *reinterpret_cast<uint4*>(dst + off) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-        fence_proxy_async_smem();
-      }
-    }
     for (int ii = 0; ii < n_iter && ok; ++ii) {
       const int s = ii % C::NQ;
       const int i0 = (qt_first + ii) * 128;
       const int ib = i0 + w * 64;  // first query of this half
       const float4* l2v = reinterpret_cast<const float4*>(smem + C::VEC_OFF + s * 1024) + w * 16;
       const float4* dvv = l2v + 32;
-      if (!(ok = fa_wait_warp(&bars->s_full, uint32_t(ii) & 1u, watch, SITE_B_S))) break;
+      if (!(ok = fa_wait_warp(&bars->s_full, uint32_t(ii) & 1u, watch, SITE_KV_S))) break;
       tc_fence_after();
-      {
-        float pv[64];
-        tmem_ld_x64f(tmem + lane_addr + C::T_S + w * 64, pv);
-        const bool need_mask = !(tile_keys_ok && i0 >= qlo_max && i0 + 127 <= qhi_min);
+      // P stays in registers: S^T of the next tile overwrites these TMEM columns
+      // as soon as this tile's dV has read the hi/lo pairs.
+      float pv[64];
+      tmem_ld_x64f(tmem + lane_addr + C::T_S + w * 64, pv);
+      const bool need_mask = !(tile_keys_ok && i0 >= qlo_max && i0 + 127 <= qhi_min);
+      const uint64_t sl2 = f2_pack(sl, sl);
 #pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {
-          const float4 l4 = l2v[c4];
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 4 * c4 + e;
-            float bias = -lv[e];
-            if (has_alibi) bias -= slope_log2 * fabsf(float(ib + off - j + c));
-            pv[c] = ex2_approx(fmaf(pv[c], sl, bias));
-          }
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 l4 = l2v[c4];
+        float b0 = -l4.x, b1 = -l4.y, b2 = -l4.z, b3 = -l4.w;
+        if (has_alibi) {
+          const float d = float(ib + off - j + 4 * c4);
+          b0 -= slope_log2 * fabsf(d);
+          b1 -= slope_log2 * fabsf(d + 1.0f);
+          b2 -= slope_log2 * fabsf(d + 2.0f);
+          b3 -= slope_log2 * fabsf(d + 3.0f);
         }
-        if (need_mask) {
-          const int lo = qlo - ib, hi = qhi - ib;
+        float a0, a1, a2, a3;
+        f2_unpack(f2_fma(f2_pack(pv[4 * c4], pv[4 * c4 + 1]), sl2, f2_pack(b0, b1)), a0, a1);
+        f2_unpack(f2_fma(f2_pack(pv[4 * c4 + 2], pv[4 * c4 + 3]), sl2, f2_pack(b2, b3)), a2, a3);
+        pv[4 * c4] = ex2_approx(a0);
+        pv[4 * c4 + 1] = ex2_approx(a1);
+        pv[4 * c4 + 2] = ex2_approx(a2);
+        pv[4 * c4 + 3] = ex2_approx(a3);
+      }
+      if (need_mask) {
+        const int lo = qlo - ib, hi = qhi - ib;
 #pragma unroll
-          for (int c = 0; c < 64; ++c) pv[c] = (c >= lo && c <= hi) ? pv[c] : 0.0f;
-        }
-        // P as bf16 hi/lo pairs; 16-query chunk c4 -> columns [16*c4, 16*c4+8) hi, [+8, +16) lo
+        for (int c = 0; c < 64; ++c) pv[c] = (c >= lo && c <= hi) ? pv[c] : 0.0f;
+      }
+      // P as bf16 hi/lo pairs; 16-query chunk c4 -> columns [16*c4, 16*c4+8) hi, [+8, +16) lo
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t hl[16];
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t hl[16];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float a0 = pv[16 * c4 + 2 * e], a1 = pv[16 * c4 + 2 * e + 1];
-            const uint32_t hp = pack_bf16x2(a0, a1);
-            hl[e] = hp;
-            hl[8 + e] = pack_bf16x2(a0 - __uint_as_float(hp << 16), a1 - __uint_as_float(hp & 0xFFFF0000u));
-          }
-          tmem_st_x16(tmem + lane_addr + C::T_S + w * 64 + 16 * c4, hl);
-        }
+        for (int e = 0; e < 8; ++e) split_hilo(pv[16 * c4 + 2 * e], pv[16 * c4 + 2 * e + 1], hl[e], hl[8 + e]);
+        tmem_st_x16(tmem + lane_addr + C::T_S + w * 64 + 16 * c4, hl);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars->p_ready);
 
-      if (!(ok = fa_wait_warp(&bars->dp_full, uint32_t(ii) & 1u, watch, SITE_B_DP))) break;
-      // the dS buffer doubles as the previous tile's dQ stage: wait until TMA has read it
-      if (ii > 0 && !(ok = fa_wait_warp(&bars->stage_done, uint32_t(ii - 1) & 1u, watch, SITE_B_STAGE))) break;
+      if (!(ok = fa_wait_warp(&bars->dp_full, uint32_t(ii) & 1u, watch, SITE_KV_DP))) break;
       tc_fence_after();
-      uint8_t* ds_row = smem + C::DS_OFF + w * C::PANEL_BYTES + r * 128;
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
         float dp[16];
-        uint32_t ph[16];  // P hi (8) then lo (8) for these 16 queries
         tmem_ld_x16f(tmem + lane_addr + C::T_DP + w * 64 + 16 * c4, dp);
-        tmem_ld_x16(tmem + lane_addr + C::T_S + w * 64 + 16 * c4, ph);
         uint32_t hl[16];
-        uint32_t h16[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int c = 16 * c4 + 2 * e;
           const float4 d4 = dvv[c / 4];
           const float dv0 = (c % 4 == 0) ? d4.x : d4.z;
           const float dv1 = (c % 4 == 0) ? d4.y : d4.w;
-          const float p0 = __uint_as_float(ph[e] << 16) + __uint_as_float(ph[8 + e] << 16);
-          const float p1 = __uint_as_float(ph[e] & 0xFFFF0000u) + __uint_as_float(ph[8 + e] & 0xFFFF0000u);
-          const float s0 = p0 * (dp[2 * e] - dv0);
-          const float s1 = p1 * (dp[2 * e + 1] - dv1);
-          const uint32_t hp = pack_bf16x2(s0, s1);
-          hl[e] = hp;
-          hl[8 + e] = pack_bf16x2(s0 - __uint_as_float(hp << 16), s1 - __uint_as_float(hp & 0xFFFF0000u));
-          h16[e] = pack_f16x2(s0, s1);
+          float s0, s1;
+          ds_pair(pv[c], pv[c + 1], dp[2 * e], dp[2 * e + 1], dv0, dv1, s0, s1);
+          split_hilo(s0, s1, hl[e], hl[8 + e]);
         }
         // dS^T hi/lo over this chunk's own (already read) dP^T columns
         tmem_st_x16(tmem + lane_addr + C::T_DP + w * 64 + 16 * c4, hl);
-        // fp16 dS for the dQ product: 16 queries = two 16-byte chunks of row r
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int chunk = (2 * c4 + e) ^ (r & 7);
-          *reinterpret_cast<uint4*>(ds_row + chunk * 16) =
-              make_uint4(h16[4 * e], h16[4 * e + 1], h16[4 * e + 2], h16[4 * e + 3]);
-        }
       }
-      fence_proxy_async_smem();
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars->ds_ready);
@@ -474,7 +446,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     if (n_iter == 0) {
       if (row_ok)
         for (int e = 0; e < D / 8; ++e) reinterpret_cast<uint4*>(dst)[e] = make_uint4(0, 0, 0, 0);
-    } else if (ok && fa_wait_warp(&bars->acc_done, 0, watch, SITE_B_ACC)) {
+    } else if (ok && fa_wait_warp(&bars->acc_done, 0, watch, SITE_KV_ACC)) {
       tc_fence_after();
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
@@ -490,84 +462,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
       }
     }
-  } else if (warp >= 12) {
-    // ------------------------------------------------------------ dQ drain (thread = query row)
-    // TMEM -> shared stage (two 16 KB halves of 128 rows x 32 fp32, 128-byte
-    // swizzle, in the dS buffer) -> TMA reduce-add into dQ_acc. Thread r == 0
-    // issues the bulk operations; the handshakes are bounded mbarrier waits.
-    constexpr int NCH = D / 32;
-    const int wq = warp & 3;
-    const int r = wq * 32 + lane;
-    const uint32_t lane_addr = uint32_t(wq * 32) << 16;
-    uint8_t* stage = smem + C::DS_OFF;
-    uint32_t staged_ph[2] = {0u, 0u};
-    for (int ii = 0; ii < n_iter; ++ii) {
-      const int qt = qt_first + ii;
-      if (!fa_wait_warp(&bars->dq_full, uint32_t(ii) & 1u, watch, SITE_B_DQ)) break;
-      tc_fence_after();
-      bool ok = true;
-#pragma unroll 1
-      for (int cc = 0; cc < NCH && ok; ++cc) {
-        const int hh = cc & 1;
-        if (cc >= 2 && !(ok = fa_wait_warp(&bars->half_free[hh], uint32_t(ii) & 1u, watch, SITE_B_STAGE))) break;
-        float a[32];
-        tmem_ld_x32f(tmem + lane_addr + C::T_DQ + cc * 32, a);
-        uint8_t* row = stage + hh * C::PANEL_BYTES + r * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<float4*>(row + ((c ^ (r & 7)) << 4)) =
-              make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
-        if (cc == NCH - 1) {  // TMEM fully read: the next dP^T may overwrite it
-          tc_fence_before();
-          mbar_arrive(&bars->dq_free);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&bars->staged[hh]);
-        if (r == 0) {
-          ok = fa_wait(&bars->staged[hh], staged_ph[hh], watch, SITE_B_STAGE);
-          if (ok && p.deterministic && cc == 0) {
-            // wait for every earlier key tile of this query tile to have finished its adds
-            int* sem = p.sem + ((size_t(b) * p.H + h) * p.n_qt + qt) * 4;
-            const int rank = kt - first_ktile(qt, p);
-            const uint64_t t0 = globaltimer_ns();
-            int v;
-            for (;;) {
-              asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(sem) : "memory");
-              if (v == rank) break;
-              if (*watch.abort || globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) {
-                *watch.abort = 1;
-                atomicOr(p.status, FA_DEV_TIMEOUT | SITE_B_SEM);
-                ok = false;
-                break;
-              }
-            }
-          }
-          if (ok) {
-            tma_reduce_add_4d(&tm_dq, stage + hh * C::PANEL_BYTES, cc * 32, h, qt * 128, b);
-            bulk_commit_group();
-            if (cc >= 1 && cc + 1 < NCH) {  // chunk cc-1 read out: its half is free for chunk cc+1
-              bulk_wait_group_read<1>();
-              mbar_arrive(&bars->half_free[(cc - 1) & 1]);
-            }
-          }
-        }
-        staged_ph[hh] ^= 1u;
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0 && !*watch.abort;
-      }
-      if (!ok) break;
-      if (r == 0) {
-        bulk_wait_group_read<0>();
-        if (p.deterministic) {
-          bulk_wait_group<0>();
-          __threadfence();
-          int* sem = p.sem + ((size_t(b) * p.H + h) * p.n_qt + qt) * 4;
-          asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(sem) : "memory");
-        }
-        mbar_arrive(&bars->stage_done);
-      }
-      __syncwarp();
-    }
-    if (lane == 0) bulk_wait_group<0>();  // no bulk operation may outlive the CTA
   }
 
   tc_fence_before();
@@ -579,8 +473,300 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   }
 }
 
-// D_i = rowsum(dO * O), L2 = L*log2(e) (+inf where L = -inf or on padding),
-// dQ accumulator rows zeroed, counters zeroed. One warp per (b, h, row).
+// ============================================================================ dQ
+template <int D>
+struct DqCfg {
+  static constexpr int PANELS = D / 64;
+  static constexpr int PANEL_BYTES = 128 * 128;
+  static constexpr int TILE_BYTES = PANELS * PANEL_BYTES;
+  static constexpr int NSLOT = D == 64 ? 8 : 5;  // ring of K_j, V_j tiles
+  static constexpr int Q_OFF = 0;
+  static constexpr int DO_OFF = TILE_BYTES;
+  static constexpr int KV_OFF = 2 * TILE_BYTES;
+  static constexpr int BAR_OFF = KV_OFF + NSLOT * TILE_BYTES;
+  static constexpr int SMEM_BYTES = BAR_OFF + 256;
+  static constexpr int THREADS = 384;
+  // TMEM: S/dS double buffer at [0,128) and [384,512), dP at [128,256), dQ at [256,256+D)
+  static constexpr uint32_t T_S0 = 0, T_S1 = 384, T_DP = 128, T_DQ = 256;
+  static_assert(T_DQ + D <= T_S1, "TMEM budget");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+struct DqBars {
+  uint64_t q_full;
+  uint64_t kv_full[8], kv_empty[8];
+  uint64_t s_full[2], dp_full, ds_ready, acc_done, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int D>
+__global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const BwdParams p) {
+  using C = DqCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.status, FA_DEV_TIMEOUT | SITE_DQ_ALIGN);
+    return;
+  }
+  DqBars* bars = reinterpret_cast<DqBars*>(smem + C::BAR_OFF);
+  const int warp = int(warp_id());
+  const int lane = int(lane_id());
+  const int n_qt = p.n_qt;
+  // Query tiles with more live keys first (causal / right-bounded windows).
+  const int qt = (p.wr >= 0) ? (n_qt - 1 - int(blockIdx.x)) : int(blockIdx.x);
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  const int row0 = qt * 128;
+  const int last_row = min(p.Sq, row0 + 128) - 1;
+  const int kv_lo = live_range(row0, p.Sq, p.Sk, p.wl, p.wr).lo;
+  const int kv_hi = live_range(last_row, p.Sq, p.Sk, p.wl, p.wr).hi;
+  const int jb = kv_lo / 128;
+  const int n_blocks = (kv_hi >= kv_lo) ? (kv_hi / 128 + 1 - jb) : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < C::NSLOT; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    mbar_init(&bars->s_full[0], 1);
+    mbar_init(&bars->s_full[1], 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->ds_ready, 256);
+    mbar_init(&bars->acc_done, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const Watch watch{&bars->abort, p.status};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_blocks > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(&bars->q_full, 2 * C::TILE_BYTES);
+      for (int pn = 0; pn < C::PANELS; ++pn) {
+        tma_load_4d(smem + C::Q_OFF + pn * C::PANEL_BYTES, &tm_q, &bars->q_full, pn * 64, h, row0, b);
+        tma_load_4d(smem + C::DO_OFF + pn * C::PANEL_BYTES, &tm_do, &bars->q_full, pn * 64, h, row0, b);
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int jj = 0; jj < n_blocks && ok; ++jj) {
+        for (int kv = 0; kv < 2; ++kv) {
+          const int it = 2 * jj + kv;
+          const int s = it % C::NSLOT;
+          if (!fa_wait(&bars->kv_empty[s], (uint32_t(it / C::NSLOT) & 1u) ^ 1u, watch, SITE_DQ_EMPTY)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->kv_full[s], C::TILE_BYTES);
+          const CUtensorMap* m = kv ? &tm_v : &tm_k;
+          for (int pn = 0; pn < C::PANELS; ++pn)
+            tma_load_4d(smem + C::KV_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, m, &bars->kv_full[s],
+                        pn * 64, h, (jb + jj) * 128, b);
+          issued = it + 1;
+        }
+      }
+      drain_wait_b(&bars->q_full, 0);
+      for (int it = (issued > C::NSLOT ? issued - C::NSLOT : 0); it < issued; ++it)
+        drain_wait_b(&bars->kv_full[it % C::NSLOT], uint32_t(it / C::NSLOT) & 1u);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_blocks > 0) {
+      constexpr uint32_t ID_SS = idesc_bf16_f32(128, 128, 0, 0);  // S = Q K^T, dP = dO V^T
+      constexpr uint32_t ID_DQ = idesc_bf16_f32(128, D, 0, 1);    // dQ: A = dS from TMEM, B = K MN-major
+      const uint32_t q_a = smem_u32(smem + C::Q_OFF);
+      const uint32_t do_a = smem_u32(smem + C::DO_OFF);
+      const uint32_t kv_base = smem_u32(smem + C::KV_OFF);
+      auto slot_addr = [&](int it) { return kv_base + (it % C::NSLOT) * C::TILE_BYTES; };
+      auto wait_full = [&](int it, uint32_t site) {
+        return fa_wait(&bars->kv_full[it % C::NSLOT], uint32_t(it / C::NSLOT) & 1u, watch, site);
+      };
+      auto issue_s = [&](int jj) {
+        const uint32_t ka = slot_addr(2 * jj);
+        const uint32_t ts = (jj & 1) ? C::T_S1 : C::T_S0;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
+          mma_ss(tmem + ts, sdesc_sw128(q_a + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), ID_SS,
+                 kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->s_full[jj & 1]);
+      };
+      auto issue_dp = [&](int jj) {
+        const uint32_t va = slot_addr(2 * jj + 1);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
+          mma_ss(tmem + C::T_DP, sdesc_sw128(do_a + off, 16, 1024), sdesc_sw128(va + off, 16, 1024), ID_SS,
+                 kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->dp_full);
+        mma_commit(&bars->kv_empty[(2 * jj + 1) % C::NSLOT]);  // V_j: only dP reads it
+      };
+      bool ok = fa_wait(&bars->q_full, 0, watch, SITE_DQ_Q);
+      for (int jj = 0; jj < 2 && jj < n_blocks && ok; ++jj) {
+        if ((ok = wait_full(2 * jj, SITE_DQ_K))) {
+          tc_fence_after();
+          issue_s(jj);
+        }
+      }
+      if (ok && (ok = wait_full(1, SITE_DQ_V))) {
+        tc_fence_after();
+        issue_dp(0);
+      }
+      // Order per key tile jj: [dS(jj) formed] dP(jj+1), dQ(jj), S(jj+2). dS(jj) sits
+      // over the consumed S(jj) buffer, so the dP columns are free as soon as dS(jj)
+      // has been formed, and S(jj+2) reuses the buffer after dQ(jj) has read it.
+      for (int jj = 0; jj < n_blocks && ok; ++jj) {
+        if (!(ok = fa_wait(&bars->ds_ready, uint32_t(jj) & 1u, watch, SITE_DQ_DS))) break;
+        tc_fence_after();
+        if (jj + 1 < n_blocks) {
+          if (!(ok = wait_full(2 * (jj + 1) + 1, SITE_DQ_V))) break;
+          tc_fence_after();
+          issue_dp(jj + 1);
+        }
+        // dQ += dS_hi K + dS_lo K ; keys 16kk.. of dS sit at column 64*(kk/4) + 16*(kk%4) (hi), +8 (lo)
+        const uint32_t ka = slot_addr(2 * jj);
+        const uint32_t ts = (jj & 1) ? C::T_S1 : C::T_S0;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t da = tmem + ts + (kk / 4) * 64 + (kk % 4) * 16;
+          const uint64_t bd = sdesc_sw128(ka + kk * 2048, C::PANEL_BYTES, 1024);
+          mma_ts(tmem + C::T_DQ, da, bd, ID_DQ, (jj > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::T_DQ, da + 8, bd, ID_DQ, 1u);
+        }
+        mma_commit(&bars->kv_empty[(2 * jj) % C::NSLOT]);  // K_j: read by S_j and this dQ
+        if (jj + 2 < n_blocks) {
+          if (!(ok = wait_full(2 * (jj + 2), SITE_DQ_K))) break;
+          tc_fence_after();
+          issue_s(jj + 2);  // into the buffer dQ(jj) just read (in-order)
+        }
+      }
+      if (ok) {
+        mma_commit(&bars->acc_done);
+      } else {
+        mma_commit(&bars->drain);
+        drain_wait_b(&bars->drain, 0);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ compute (thread = query row)
+    const int w = (warp - 4) / 4;  // key-column half
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const int i = row0 + r;
+    const uint32_t lane_addr = uint32_t(wq * 32) << 16;
+    const RowRange rr = live_range(i, p.Sq, p.Sk, p.wl, p.wr);
+    const int tile_lo_max = live_range(last_row, p.Sq, p.Sk, p.wl, p.wr).lo;
+    const int tile_hi_min = live_range(row0, p.Sq, p.Sk, p.wl, p.wr).hi;
+    const size_t vi = (size_t(b) * p.H + h) * p.Sq_pad + i;  // i < Sq_pad always
+    const float l2 = p.l2[vi];
+    const float dval = p.dvec[vi];
+    const bool has_alibi = p.alibi != nullptr;
+    const float slope_log2 = has_alibi ? p.alibi[b * p.alibi_bstride + h] * 1.4426950408889634f : 0.0f;
+    const int c_i = i + p.Sk - p.Sq;
+    const float sl = p.scale_log2;
+    bool ok = true;
+    for (int jj = 0; jj < n_blocks && ok; ++jj) {
+      const int sb = jj & 1;
+      const int kb = (jb + jj) * 128 + w * 64;  // first key of this half
+      if (!(ok = fa_wait_warp(&bars->s_full[sb], uint32_t(jj >> 1) & 1u, watch, SITE_DQ_S))) break;
+      tc_fence_after();
+      float pv[64];
+      tmem_ld_x64f(tmem + lane_addr + (sb ? C::T_S1 : C::T_S0) + w * 64, pv);
+      const int kbase = (jb + jj) * 128;
+      const bool need_mask = !(kbase >= tile_lo_max && kbase + 127 <= tile_hi_min);
+      if (has_alibi) {
+        const float d0 = float(c_i - kb);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) pv[c] = ex2_approx(fmaf(pv[c], sl, -slope_log2 * fabsf(d0 - float(c)) - l2));
+      } else {
+        const uint64_t sl2 = f2_pack(sl, sl), nl2 = f2_pack(-l2, -l2);
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          float a0, a1;
+          f2_unpack(f2_fma(f2_pack(pv[c], pv[c + 1]), sl2, nl2), a0, a1);
+          pv[c] = ex2_approx(a0);
+          pv[c + 1] = ex2_approx(a1);
+        }
+      }
+      if (need_mask) {
+        const int lo = rr.lo - kb, hi = rr.hi - kb;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) pv[c] = (c >= lo && c <= hi) ? pv[c] : 0.0f;
+      }
+      if (!(ok = fa_wait_warp(&bars->dp_full, uint32_t(jj) & 1u, watch, SITE_DQ_DP))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float dp[16];
+        tmem_ld_x16f(tmem + lane_addr + C::T_DP + w * 64 + 16 * c4, dp);
+        uint32_t hl[16];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int c = 16 * c4 + 2 * e;
+          float s0, s1;
+          ds_pair(pv[c], pv[c + 1], dp[2 * e], dp[2 * e + 1], dval, dval, s0, s1);
+          split_hilo(s0, s1, hl[e], hl[8 + e]);
+        }
+        // dS hi/lo over the consumed S columns of this buffer (S is in registers)
+        tmem_st_x16(tmem + lane_addr + (sb ? C::T_S1 : C::T_S0) + w * 64 + 16 * c4, hl);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->ds_ready);
+    }
+    // ------------------------------------------------------------ dQ epilogue (each group half of D)
+    const bool row_ok = i < p.Sq;
+    __nv_bfloat16* dst = p.dq + ((size_t(b) * p.Sq + size_t(i)) * p.H + h) * size_t(D) + w * (D / 2);
+    if (n_blocks == 0) {
+      if (row_ok)
+        for (int e = 0; e < D / 16; ++e) reinterpret_cast<uint4*>(dst)[e] = make_uint4(0, 0, 0, 0);
+    } else if (ok && fa_wait_warp(&bars->acc_done, 0, watch, SITE_DQ_ACC)) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int cc = 0; cc < D / 64; ++cc) {
+        float a[32];
+        tmem_ld_x32f(tmem + lane_addr + C::T_DQ + w * (D / 2) + cc * 32, a);
+        if (row_ok) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(a[2 * e] * p.scale, a[2 * e + 1] * p.scale);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            reinterpret_cast<uint4*>(dst + cc * 32)[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// D_i = rowsum(dO * O), L2 = L*log2(e) (+inf where L = -inf or on padding).
+// One warp per (b, h, row).
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
   constexpr int PER = D / 32;
@@ -588,8 +774,6 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
   const int lane = threadIdx.x & 31;
   const int h = blockIdx.y;
   const int b = blockIdx.z;
-  if (blockIdx.x == 0 && p.deterministic)
-    for (int t = threadIdx.x; t < p.n_qt * 4; t += blockDim.x) p.sem[(size_t(b) * p.H + h) * p.n_qt * 4 + t] = 0;
   if (row >= p.Sq_pad) return;
   const size_t vi = (size_t(b) * p.H + h) * p.Sq_pad + row;
   if (row >= p.Sq) {
@@ -610,8 +794,6 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-#pragma unroll
-  for (int e = 0; e < PER; e += 2) *reinterpret_cast<float2*>(p.dq_acc + ro + e) = make_float2(0.0f, 0.0f);
   if (lane == 0) {
     p.dvec[vi] = acc;
     const float L = p.lse[(size_t(b) * p.H + h) * p.Sq + row];
@@ -619,34 +801,20 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
   }
 }
 
-__global__ void __launch_bounds__(256) fa_bwd_convert_kernel(const float* __restrict__ acc,
-                                                              __nv_bfloat16* __restrict__ dq, size_t n8,
-                                                              float scale) {
-  for (size_t t = blockIdx.x * size_t(blockDim.x) + threadIdx.x; t < n8; t += size_t(gridDim.x) * blockDim.x) {
-    const float4 a = reinterpret_cast<const float4*>(acc)[2 * t];
-    const float4 c = reinterpret_cast<const float4*>(acc)[2 * t + 1];
-    reinterpret_cast<uint4*>(dq)[t] = make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
-                                                 pack_bf16x2(c.x * scale, c.y * scale), pack_bf16x2(c.z * scale, c.w * scale));
-  }
-}
-
 static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
 size_t bwd_workspace_bytes(int B, int Sq, int Sk, int H, int D, int deterministic) {
   (void)Sk;
+  (void)D;
+  (void)deterministic;  // every run is deterministic: no cross-CTA reductions
   const size_t sq_pad = size_t((Sq + 127) / 128) * 128;
-  const size_t n_qt = sq_pad / 128;
-  size_t n = al256(size_t(B) * Sq * H * D * 4);  // dQ accumulator
-  n += 2 * al256(size_t(B) * H * sq_pad * 4);    // L2, D
-  if (deterministic) n += al256(size_t(B) * H * n_qt * 4 * 4);
-  return n;
+  return 2 * al256(size_t(B) * H * sq_pad * 4);  // L2, D
 }
 
 template <int D>
 static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, const void* k, const void* v,
                         const void* out, const float* lse, void* dq, void* dk, void* dv, void* ws,
-                        int deterministic, cudaStream_t stream) {
-  using C = BwdCfg<D>;
+                        cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mdo;
   if (!make_bshd_map(&mq, q, s.B, s.Sq, s.H, D, 128) || !make_bshd_map(&mk, k, s.B, s.Sk, s.H, D, 128) ||
       !make_bshd_map(&mv, v, s.B, s.Sk, s.H, D, 128) || !make_bshd_map(&mdo, dout, s.B, s.Sq, s.H, D, 128))
@@ -659,13 +827,9 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
   p.Sq_pad = ((s.Sq + 127) / 128) * 128;
   p.n_qt = p.Sq_pad / 128;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  p.dq_acc = reinterpret_cast<float*>(w);
-  w += al256(size_t(s.B) * s.Sq * s.H * D * 4);
   p.l2 = reinterpret_cast<float*>(w);
   w += al256(size_t(s.B) * s.H * p.Sq_pad * 4);
   p.dvec = reinterpret_cast<float*>(w);
-  w += al256(size_t(s.B) * s.H * p.Sq_pad * 4);
-  p.sem = deterministic ? reinterpret_cast<int*>(w) : nullptr;
   p.dout = static_cast<const __nv_bfloat16*>(dout);
   p.out = static_cast<const __nv_bfloat16*>(out);
   p.lse = lse;
@@ -678,38 +842,33 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
   p.wr = s.wr;
   p.scale = s.scale;
   p.scale_log2 = s.scale * 1.4426950408889634f;
-  p.deterministic = deterministic ? 1 : 0;
   p.status = device_status_word();
   if (!p.status) return FA_ERR_CUDA;
   if (s.B > 65535 || s.H > 65535) return FA_ERR_UNSUPPORTED;
 
   fa_bwd_pre_kernel<D><<<dim3(p.Sq_pad / 8, s.H, s.B), 256, 0, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  auto kern = fa_bwd_main_kernel<D>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+  auto kv = fa_bwd_dkdv_kernel<D>;
+  if (cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, KvCfg<D>::SMEM_BYTES) != cudaSuccess)
     return FA_ERR_CUDA;
-  CUtensorMap mdq;
-  if (!make_bshd_f32_map(&mdq, p.dq_acc, s.B, s.Sq, s.H, D)) return FA_ERR_CUDA;
-  kern<<<dim3((s.Sk + 127) / 128, s.H, s.B), C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, mdq, p);
+  kv<<<dim3((s.Sk + 127) / 128, s.H, s.B), KvCfg<D>::THREADS, KvCfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  const size_t n8 = size_t(s.B) * s.Sq * s.H * D / 8;
-  size_t nb = (n8 + 255) / 256;
-  const size_t cap = size_t(device_sm_count()) * 8;
-  if (nb > cap) nb = cap;
-  if (nb < 1) nb = 1;
-  const int blocks = int(nb);
-  fa_bwd_convert_kernel<<<blocks, 256, 0, stream>>>(p.dq_acc, p.dq, n8, s.scale);
+  auto dqk = fa_bwd_dq_kernel<D>;
+  if (cudaFuncSetAttribute(dqk, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::SMEM_BYTES) != cudaSuccess)
+    return FA_ERR_CUDA;
+  dqk<<<dim3(p.n_qt, s.H, s.B), DqCfg<D>::THREADS, DqCfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int bwd_launch(const AttnShape& s, const void* dout, const void* q, const void* k, const void* v, const void* out,
                const float* lse, void* dq, void* dk, void* dv, void* workspace, int deterministic,
                cudaStream_t stream) {
+  (void)deterministic;
   switch (s.D) {
     case 64:
-      return launch_bwd_t<64>(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, deterministic, stream);
+      return launch_bwd_t<64>(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, stream);
     case 128:
-      return launch_bwd_t<128>(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, deterministic, stream);
+      return launch_bwd_t<128>(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, stream);
     default:
       return FA_ERR_UNSUPPORTED;
   }

@@ -78,8 +78,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, i
            int alibi_batch_stride, fa_stream_t stream);
 
 /*
- * Bytes of device workspace fa_bwd needs (fp32 dQ accumulator, the per-row
- * D_i = rowsum(dO * O) vector and, for deterministic mode, ordering counters).
+ * Bytes of device workspace fa_bwd needs: the per-row D_i = rowsum(dO * O)
+ * and L*log2(e) vectors, (B, H, Sq rounded up to 128) fp32 each.
  * Returns 0 for arguments fa_bwd would reject.
  */
 size_t fa_bwd_workspace_size(int B, int Sq, int Sk, int H, int D, int deterministic);
@@ -89,9 +89,10 @@ size_t fa_bwd_workspace_size(int B, int Sq, int Sk, int H, int D, int determinis
  * stored attention matrix). Inputs: dout, q, k, v, out (bf16) and lse (fp32)
  * from fa_fwd with the same arguments. Writes dq (B,Sq,H,D), dk, dv
  * (B,Sk,H,D) bf16; they are overwritten, not accumulated.
- * deterministic != 0 makes dq/dk/dv bitwise reproducible from run to run
- * (section "2.4": slightly slower, more workspace); 0 accumulates dQ with
- * fp32 atomic adds in arbitrary order.
+ * deterministic: accepted for the page's interface (section "2.4"). Every
+ * run is bitwise reproducible in either mode, because no output element is
+ * accumulated across thread blocks: one kernel per 128-key tile produces dK
+ * and dV, another per 128-row query tile produces dQ.
  * workspace: caller-owned device buffer of at least fa_bwd_workspace_size()
  * bytes, 256-byte aligned; its contents on entry are ignored.
  * Supported: D in {64, 128}.
