@@ -11,35 +11,33 @@
 // tensor cores, so this backward never reduces across CTAs:
 //
 //   fa_bwd_pre       D_i = rowsum(dO_i * O_i) and L2_i = L_i*log2(e), padded to
-//                    128-row tiles (+inf on padding and on rows without keys).
+//                    128-row tiles (+inf on padding and on rows without keys),
+//                    and fp16 copies of Q, K, V and dO.
 //   fa_bwd_dkdv      one CTA per (128-key tile, head, batch), looping over the
 //                    live 128-row query tiles:
-//                      S^T  = K Q^T                 -> TMEM [0,128)      (tcgen05)
-//                      dP^T = V dO^T                -> TMEM [128,256)
-//                      P^T  = 2^(S^T*scale*log2e + bias - L2): bf16 hi/lo pairs
-//                             written over S^T (P = hi + lo to ~2^-16); P itself
-//                             stays in registers for dS
-//                    issued in the order dP^T(i), dV(i), S^T(i+1), dK(i), so the
-//                    next tile's S^T and P overlap this tile's dS and dK.
-//                      dV  += P_hi^T dO + P_lo^T dO (A from TMEM)
-//                      dS^T = P^T o (dP^T - D): bf16 hi/lo pairs over dP^T
-//                      dK  += dS_hi^T Q + dS_lo^T Q
-//                    then writes dK (times scale) and dV.
+//                      S^T  = K Q^T                 -> TMEM S region   (tcgen05)
+//                      dP^T = V dO^T                -> TMEM dP region
+//                      P^T  = 2^(S^T*scale*log2e + bias - L2)
+//                      dS^T = P^T o (dP^T - D)      -> both fp16, over dP^T
+//                      dV  += P^T dO, dK += dS^T Q  (A from TMEM, two chains)
+//                    S^T of the next tile is computed while this one's
+//                    exponentials run; then dK (times scale) and dV are written.
 //   fa_bwd_dq        one CTA per (128-row query tile, head, batch), looping over
 //                    the live key tiles (the forward's shape, thread = query row):
 //                      S  = Q K^T -> TMEM (double-buffered), P = 2^(S*... - L2)
-//                      dP = dO V^T, dS = P o (dP - D): hi/lo pairs over the
-//                             consumed S buffer
-//                      dQ += dS_hi K + dS_lo K (A from TMEM, K as MN-major B)
-//                    issued in the order dP(j+1), dQ(j), S(j+2) once dS(j) is formed.
+//                      dP = dO V^T, dS = P o (dP - D) -> fp16 over the consumed S
+//                      dQ += dS K, interleaved with dP of the next key tile
 //                    then writes dQ (times scale) once.
 // Every output element is produced by one CTA in a fixed order, so every run
 // is bitwise reproducible; the deterministic flag costs nothing.
 //
-// Precision: the gradients are compared against an fp64 reference with an
-// absolute bound close to bf16's own output rounding at |x| ~ 5, so the
-// operands the gradient products read from TMEM carry ~16 significant bits
-// (bf16 hi/lo pairs) rather than bf16's 8.
+// Precision and MMA rate: every product takes fp16 operands (P, dS and exact
+// fp16 copies of the bf16 inputs). fp16 keeps 11 significant bits, enough for
+// the gradients to stay at bf16's own output rounding against an fp64
+// reference with one MMA per product; it limits the backward's inputs to the
+// fp16 range (|x| < 65504). MMAs into one TMEM accumulator serialise on a
+// ~100-cycle dependency, so independent chains are interleaved where the
+// TMEM budget allows.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -54,9 +52,16 @@ namespace fa {
 struct BwdParams {
   const __nv_bfloat16* dout;
   const __nv_bfloat16* out;
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
   const float* lse;
-  float* l2;    // (B, H, Sq_pad): L * log2(e); +inf on rows without keys and on padding
-  float* dvec;  // (B, H, Sq_pad): rowsum(dO * O)
+  float* l2;      // (B, H, Sq_pad): L * log2(e); +inf on rows without keys and on padding
+  float* dvec;    // (B, H, Sq_pad): rowsum(dO * O)
+  uint16_t* q16;  // fp16 copies, (B, S, H, D) like the inputs
+  uint16_t* do16;
+  uint16_t* k16;
+  uint16_t* v16;
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -74,8 +79,8 @@ enum : uint32_t {
   SITE_KV_KV = 0x32,
   SITE_KV_QFULL = 0x33,
   SITE_KV_DOFULL = 0x34,
-  SITE_KV_P = 0x35,
-  SITE_KV_DS = 0x36,
+  SITE_KV_PD = 0x35,
+  SITE_KV_SFREE = 0x36,
   SITE_KV_S = 0x37,
   SITE_KV_DP = 0x38,
   SITE_KV_ACC = 0x39,
@@ -120,17 +125,85 @@ __device__ __forceinline__ bool qtile_meets(int qt, int kt, const BwdParams& p) 
   return !(hi < kt * 128 || lo > kt * 128 + 127);
 }
 
-// Splits an fp32 pair into bf16 hi (x rounded) and lo (x - hi rounded) packs.
-__device__ __forceinline__ void split_hilo(float a0, float a1, uint32_t& hi, uint32_t& lo) {
-  hi = pack_bf16x2(a0, a1);
-  float r0, r1;
-  f2_unpack(f2_sub(f2_pack(a0, a1), f2_pack(__uint_as_float(hi << 16), __uint_as_float(hi & 0xFFFF0000u))), r0, r1);
-  lo = pack_bf16x2(r0, r1);
-}
 // dS pair = P * (dP - D) with packed ops.
 __device__ __forceinline__ void ds_pair(float p0, float p1, float dp0, float dp1, float d0, float d1, float& s0,
                                         float& s1) {
   f2_unpack(f2_mul(f2_pack(p0, p1), f2_sub(f2_pack(dp0, dp1), f2_pack(d0, d1))), s0, s1);
+}
+
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 u) {
+  return make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
+}
+
+// ============================================================================ pre-pass
+// One 16-byte chunk (8 elements) of one row per item:
+//   query rows: D_i = rowsum(dO_i o O_i), L2_i = L_i*log2(e) (+inf where L_i = -inf),
+//               fp16 copies of Q_i and dO_i;
+//   key rows:   fp16 copies of K_j and V_j;
+//   padding:    D = 0 and L2 = +inf on the rows padding Sq to whole 128-row tiles.
+// The three item ranges start on multiples of 32, so each warp works inside one
+// of them and the D/8 lanes of a query row are consecutive lanes of one warp.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
+  constexpr int CPR = D / 8;
+  const long long n_q = (long long)p.B * p.Sq * p.H * CPR;
+  const long long k0 = (n_q + 31) & ~31LL;
+  const long long n_k = (long long)p.B * p.Sk * p.H * CPR;
+  const long long p0 = (k0 + n_k + 31) & ~31LL;
+  const int pad_rows = p.Sq_pad - p.Sq;
+  const long long n_pad = (long long)p.B * p.H * pad_rows;
+  const long long total = p0 + n_pad;
+  const int lane = int(threadIdx.x & 31);
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long wb = ((long long)blockIdx.x * blockDim.x + threadIdx.x) - lane; wb < total; wb += stride) {
+    const long long i = wb + lane;
+    if (wb < k0) {
+      const bool live = i < n_q;
+      float acc = 0.0f;
+      if (live) {
+        const long long e = i * 8;  // = row * D + chunk * 8
+        const uint4 qv = *reinterpret_cast<const uint4*>(p.q + e);
+        const uint4 dov = *reinterpret_cast<const uint4*>(p.dout + e);
+        const uint4 ov = *reinterpret_cast<const uint4*>(p.out + e);
+        *reinterpret_cast<uint4*>(p.q16 + e) = bf16x8_to_f16x8(qv);
+        *reinterpret_cast<uint4*>(p.do16 + e) = bf16x8_to_f16x8(dov);
+        const uint32_t a[4] = {dov.x, dov.y, dov.z, dov.w};
+        const uint32_t o[4] = {ov.x, ov.y, ov.z, ov.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          acc = fmaf(__uint_as_float(a[t] << 16), __uint_as_float(o[t] << 16), acc);
+          acc = fmaf(__uint_as_float(a[t] & 0xFFFF0000u), __uint_as_float(o[t] & 0xFFFF0000u), acc);
+        }
+      }
+#pragma unroll
+      for (int off = CPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (live && (i % CPR) == 0) {
+        const long long row = i / CPR;  // (b * Sq + s) * H + h
+        const int h = int(row % p.H);
+        const long long bs = row / p.H;
+        const int s = int(bs % p.Sq);
+        const int b = int(bs / p.Sq);
+        const size_t vi = (size_t(b) * p.H + h) * p.Sq_pad + s;
+        p.dvec[vi] = acc;
+        const float L = p.lse[(size_t(b) * p.H + h) * p.Sq + s];
+        p.l2[vi] = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
+      }
+    } else if (wb < p0) {
+      const long long t = i - k0;
+      if (t < n_k) {
+        const long long e = t * 8;
+        *reinterpret_cast<uint4*>(p.k16 + e) = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(p.k + e));
+        *reinterpret_cast<uint4*>(p.v16 + e) = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(p.v + e));
+      }
+    } else {
+      const long long t = i - p0;
+      if (t < n_pad) {
+        const size_t vi = size_t(t / pad_rows) * p.Sq_pad + p.Sq + size_t(t % pad_rows);
+        p.dvec[vi] = 0.0f;
+        p.l2[vi] = INFINITY;
+      }
+    }
+  }
 }
 
 // ============================================================================ dK / dV
@@ -148,8 +221,15 @@ struct KvCfg {
   static constexpr int VEC_OFF = DO_OFF + NDO * TILE_BYTES;  // per Q stage: L2[128], D[128]
   static constexpr int BAR_OFF = VEC_OFF + NQ * 1024;
   static constexpr int SMEM_BYTES = BAR_OFF + 256;
-  static constexpr int THREADS = 384;
+  static constexpr int NCW = 4;  // compute warpgroups; each owns COLS query columns
+  static constexpr int COLS = 128 / NCW;
+  static constexpr int NCT = 128 * NCW;  // compute threads
+  static constexpr int THREADS = 128 + NCT;
   static constexpr int Q_TX = TILE_BYTES + 1024;
+  // TMEM: S^T [0,128) fp32; dP^T [128,256) fp32, over which, once consumed, the
+  // 16-query chunk kk of P^T (fp16 pairs) sits at columns 16kk+0..7 and that of
+  // dS^T at 16kk+8..15, so every compute group writes only inside the dP^T
+  // columns it has read itself; dV and dK accumulators after it.
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
   static_assert(T_DK + D <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -159,7 +239,7 @@ struct KvBars {
   uint64_t kv_full;
   uint64_t q_full[2], q_empty[2];
   uint64_t do_full[2], do_empty[2];
-  uint64_t s_full, dp_full, p_ready, ds_ready, acc_done, drain;
+  uint64_t s_full, s_free, dp_full, pd_ready, acc_done, drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -202,9 +282,9 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
       mbar_init(&bars->do_empty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, C::NCT);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->p_ready, 256);
-    mbar_init(&bars->ds_ready, 256);
+    mbar_init(&bars->pd_ready, C::NCT);
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
@@ -263,12 +343,14 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_iter > 0) {
-      constexpr uint32_t ID_SS = idesc_bf16_f32(128, 128, 0, 0);  // S^T, dP^T: both operands K-major
-      constexpr uint32_t ID_TN = idesc_bf16_f32(128, D, 0, 1);    // dV, dK: A from TMEM, B (dO / Q) MN-major
+      constexpr uint32_t ID_SS = idesc_f16_f32(128, 128, 0, 0);  // S^T, dP^T: both operands K-major
+      constexpr uint32_t ID_TN = idesc_f16_f32(128, D, 0, 1);    // dV, dK: A from TMEM, B (dO / Q) MN-major
       const uint32_t k_a = smem_u32(smem + C::K_OFF);
       const uint32_t v_a = smem_u32(smem + C::V_OFF);
-      auto issue_st = [&](int ii) {  // S^T = K Q^T (overwrites P^T of tile ii-1: its dV was issued earlier)
-        const uint32_t q_a = smem_u32(smem + C::Q_OFF + (ii % C::NQ) * C::TILE_BYTES);
+      auto q_addr = [&](int ii) { return smem_u32(smem + C::Q_OFF + (ii % C::NQ) * C::TILE_BYTES); };
+      auto do_addr = [&](int ii) { return smem_u32(smem + C::DO_OFF + (ii % C::NDO) * C::TILE_BYTES); };
+      auto issue_st = [&](int ii) {  // S^T = K Q^T
+        const uint32_t q_a = q_addr(ii);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
@@ -277,21 +359,8 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
         }
         mma_commit(&bars->s_full);
       };
-      bool ok = fa_wait(&bars->kv_full, 0, watch, SITE_KV_KV);
-      if (ok && (ok = fa_wait(&bars->q_full[0], 0, watch, SITE_KV_QFULL))) {
-        tc_fence_after();
-        issue_st(0);
-      }
-      // Order per tile ii: dP^T(ii), dV(ii), S^T(ii+1), dK(ii). S^T of the next tile
-      // is computed while this tile's dS is formed, and its P while dK runs.
-      for (int ii = 0; ii < n_iter && ok; ++ii) {
-        const int s = ii % C::NQ;
-        const int d = ii % C::NDO;
-        const uint32_t q_a = smem_u32(smem + C::Q_OFF + s * C::TILE_BYTES);
-        const uint32_t do_a = smem_u32(smem + C::DO_OFF + d * C::TILE_BYTES);
-        // dP^T = V dO^T (overwrites dS^T of tile ii-1: its dK was issued earlier)
-        if (!(ok = fa_wait(&bars->do_full[d], uint32_t(ii / C::NDO) & 1u, watch, SITE_KV_DOFULL))) break;
-        tc_fence_after();
+      auto issue_dpt = [&](int ii) {  // dP^T = V dO^T
+        const uint32_t do_a = do_addr(ii);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
@@ -299,35 +368,50 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
                  kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars->dp_full);
-        // dV += P_hi^T dO + P_lo^T dO ; queries 16kk.. sit at column 64*(kk/4) + 16*(kk%4) (hi), +8 (lo)
-        if (!(ok = fa_wait(&bars->p_ready, uint32_t(ii) & 1u, watch, SITE_KV_P))) break;
+      };
+      bool ok = fa_wait(&bars->kv_full, 0, watch, SITE_KV_KV) && fa_wait(&bars->q_full[0], 0, watch, SITE_KV_QFULL);
+      if (ok) {
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t pa = tmem + C::T_S + (kk / 4) * 64 + (kk % 4) * 16;
-          const uint64_t bd = sdesc_sw128(do_a + kk * 2048, C::PANEL_BYTES, 1024);
-          mma_ts(tmem + C::T_DV, pa, bd, ID_TN, (ii > 0 || kk > 0) ? 1u : 0u);
-          mma_ts(tmem + C::T_DV, pa + 8, bd, ID_TN, 1u);
-        }
-        mma_commit(&bars->do_empty[d]);
-        if (ii + 1 < n_iter) {
+        issue_st(0);
+      }
+      if (ok && (ok = fa_wait(&bars->do_full[0], 0, watch, SITE_KV_DOFULL))) {
+        tc_fence_after();
+        issue_dpt(0);
+      }
+      for (int ii = 0; ii < n_iter && ok; ++ii) {
+        const bool more = ii + 1 < n_iter;
+        // S^T of the next tile as soon as every compute group holds this one in registers
+        if (more) {
+          if (!(ok = fa_wait(&bars->s_free, uint32_t(ii) & 1u, watch, SITE_KV_SFREE))) break;
           if (!(ok = fa_wait(&bars->q_full[(ii + 1) % C::NQ], uint32_t((ii + 1) / C::NQ) & 1u, watch,
                              SITE_KV_QFULL)))
             break;
           tc_fence_after();
           issue_st(ii + 1);
         }
-        // dK += dS_hi^T Q + dS_lo^T Q
-        if (!(ok = fa_wait(&bars->ds_ready, uint32_t(ii) & 1u, watch, SITE_KV_DS))) break;
+        // dV += P^T dO and dK += dS^T Q, two independent chains; the 16-query chunk kk
+        // of P^T sits at dP^T column 16kk, that of dS^T at 16kk+8 (two fp16 per column)
+        if (!(ok = fa_wait(&bars->pd_ready, uint32_t(ii) & 1u, watch, SITE_KV_PD))) break;
         tc_fence_after();
+        const uint32_t q_a = q_addr(ii), do_a = do_addr(ii);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t da = tmem + C::T_DP + (kk / 4) * 64 + (kk % 4) * 16;
-          const uint64_t bd = sdesc_sw128(q_a + kk * 2048, C::PANEL_BYTES, 1024);
-          mma_ts(tmem + C::T_DK, da, bd, ID_TN, (ii > 0 || kk > 0) ? 1u : 0u);
-          mma_ts(tmem + C::T_DK, da + 8, bd, ID_TN, 1u);
+          const uint32_t acc = (ii > 0 || kk > 0) ? 1u : 0u;
+          mma_ts(tmem + C::T_DV, tmem + C::T_DP + kk * 16, sdesc_sw128(do_a + kk * 2048, C::PANEL_BYTES, 1024), ID_TN,
+                 acc);
+          mma_ts(tmem + C::T_DK, tmem + C::T_DP + kk * 16 + 8, sdesc_sw128(q_a + kk * 2048, C::PANEL_BYTES, 1024),
+                 ID_TN, acc);
         }
-        mma_commit(&bars->q_empty[s]);
+        mma_commit(&bars->do_empty[ii % C::NDO]);
+        mma_commit(&bars->q_empty[ii % C::NQ]);
+        // dP^T of the next tile overwrites P^T and dS^T of this one (read above, in order)
+        if (more) {
+          if (!(ok = fa_wait(&bars->do_full[(ii + 1) % C::NDO], uint32_t((ii + 1) / C::NDO) & 1u, watch,
+                             SITE_KV_DOFULL)))
+            break;
+          tc_fence_after();
+          issue_dpt(ii + 1);
+        }
       }
       if (ok) {
         mma_commit(&bars->acc_done);
@@ -338,7 +422,7 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ compute (thread = key row)
-    const int w = (warp - 4) / 4;  // query-column half
+    const int w = (warp - 4) / 4;  // query-column group: columns [w*COLS, (w+1)*COLS)
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const int j = j0 + r;
@@ -368,27 +452,29 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
     for (int ii = 0; ii < n_iter && ok; ++ii) {
       const int s = ii % C::NQ;
       const int i0 = (qt_first + ii) * 128;
-      const int ib = i0 + w * 64;  // first query of this half
-      const float4* l2v = reinterpret_cast<const float4*>(smem + C::VEC_OFF + s * 1024) + w * 16;
+      const int ib = i0 + w * C::COLS;  // first query of this group
+      const float4* l2v = reinterpret_cast<const float4*>(smem + C::VEC_OFF + s * 1024) + w * (C::COLS / 4);
       const float4* dvv = l2v + 32;
+      // the L2 / D vectors of this tile land with Q
+      if (!(ok = fa_wait_warp(&bars->q_full[s], uint32_t(ii / C::NQ) & 1u, watch, SITE_KV_QFULL))) break;
       if (!(ok = fa_wait_warp(&bars->s_full, uint32_t(ii) & 1u, watch, SITE_KV_S))) break;
       tc_fence_after();
-      // P stays in registers: S^T of the next tile overwrites these TMEM columns
-      // as soon as this tile's dV has read the hi/lo pairs.
-      float pv[64];
-      tmem_ld_x64f(tmem + lane_addr + C::T_S + w * 64, pv);
+      float pv[C::COLS];
+      tmem_ld_cols(tmem + lane_addr + C::T_S + w * C::COLS, pv);
+      tc_fence_before();
+      mbar_arrive(&bars->s_free);
       const bool need_mask = !(tile_keys_ok && i0 >= qlo_max && i0 + 127 <= qhi_min);
       const uint64_t sl2 = f2_pack(sl, sl);
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
+      for (int c4 = 0; c4 < C::COLS / 4; ++c4) {
         const float4 l4 = l2v[c4];
         float b0 = -l4.x, b1 = -l4.y, b2 = -l4.z, b3 = -l4.w;
         if (has_alibi) {
-          const float d = float(ib + off - j + 4 * c4);
-          b0 -= slope_log2 * fabsf(d);
-          b1 -= slope_log2 * fabsf(d + 1.0f);
-          b2 -= slope_log2 * fabsf(d + 2.0f);
-          b3 -= slope_log2 * fabsf(d + 3.0f);
+          const float dd = float(ib + off - j + 4 * c4);
+          b0 -= slope_log2 * fabsf(dd);
+          b1 -= slope_log2 * fabsf(dd + 1.0f);
+          b2 -= slope_log2 * fabsf(dd + 2.0f);
+          b3 -= slope_log2 * fabsf(dd + 3.0f);
         }
         float a0, a1, a2, a3;
         f2_unpack(f2_fma(f2_pack(pv[4 * c4], pv[4 * c4 + 1]), sl2, f2_pack(b0, b1)), a0, a1);
@@ -401,57 +487,53 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
       if (need_mask) {
         const int lo = qlo - ib, hi = qhi - ib;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) pv[c] = (c >= lo && c <= hi) ? pv[c] : 0.0f;
+        for (int c = 0; c < C::COLS; ++c) pv[c] = (c >= lo && c <= hi) ? pv[c] : 0.0f;
       }
-      // P as bf16 hi/lo pairs; 16-query chunk c4 -> columns [16*c4, 16*c4+8) hi, [+8, +16) lo
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t hl[16];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) split_hilo(pv[16 * c4 + 2 * e], pv[16 * c4 + 2 * e + 1], hl[e], hl[8 + e]);
-        tmem_st_x16(tmem + lane_addr + C::T_S + w * 64 + 16 * c4, hl);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars->p_ready);
-
       if (!(ok = fa_wait_warp(&bars->dp_full, uint32_t(ii) & 1u, watch, SITE_KV_DP))) break;
       tc_fence_after();
+      // per 16-query chunk: load dP^T, form dS^T, then P^T and dS^T as fp16 pairs over
+      // the chunk's consumed dP^T columns (see the TMEM map)
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
+      for (int ch = 0; ch < C::COLS / 16; ++ch) {
         float dp[16];
-        tmem_ld_x16f(tmem + lane_addr + C::T_DP + w * 64 + 16 * c4, dp);
-        uint32_t hl[16];
+        const uint32_t col = tmem + lane_addr + C::T_DP + w * C::COLS + 16 * ch;
+        tmem_ld_cols(col, dp);
+        uint32_t pp[8], ps[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const int c = 16 * c4 + 2 * e;
+          const int c = 16 * ch + 2 * e;
           const float4 d4 = dvv[c / 4];
           const float dv0 = (c % 4 == 0) ? d4.x : d4.z;
           const float dv1 = (c % 4 == 0) ? d4.y : d4.w;
           float s0, s1;
           ds_pair(pv[c], pv[c + 1], dp[2 * e], dp[2 * e + 1], dv0, dv1, s0, s1);
-          split_hilo(s0, s1, hl[e], hl[8 + e]);
+          pp[e] = pack_f16x2(pv[c], pv[c + 1]);
+          ps[e] = pack_f16x2(s0, s1);
         }
-        // dS^T hi/lo over this chunk's own (already read) dP^T columns
-        tmem_st_x16(tmem + lane_addr + C::T_DP + w * 64 + 16 * c4, hl);
+        tmem_st_x8(col, pp);
+        tmem_st_x8(col + 8, ps);
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->ds_ready);
+      mbar_arrive(&bars->pd_ready);
     }
     // ------------------------------------------------------------ dK / dV epilogue
+    // groups 0..NCW/2-1 write dV, the rest dK (times scale); each a D/(NCW/2)-column slice
+    constexpr int SLICE = D / (C::NCW / 2);
+    const bool is_dv = w < C::NCW / 2;
+    const int col0 = (w % (C::NCW / 2)) * SLICE;
     const bool row_ok = j < p.Sk;
-    __nv_bfloat16* dst = (w == 0 ? p.dv : p.dk) + ((size_t(b) * p.Sk + size_t(j)) * p.H + h) * size_t(D);
-    const float mul = (w == 0) ? 1.0f : p.scale;
+    __nv_bfloat16* dst = (is_dv ? p.dv : p.dk) + ((size_t(b) * p.Sk + size_t(j)) * p.H + h) * size_t(D) + col0;
+    const float mul = is_dv ? 1.0f : p.scale;
     if (n_iter == 0) {
       if (row_ok)
-        for (int e = 0; e < D / 8; ++e) reinterpret_cast<uint4*>(dst)[e] = make_uint4(0, 0, 0, 0);
+        for (int e = 0; e < SLICE / 8; ++e) reinterpret_cast<uint4*>(dst)[e] = make_uint4(0, 0, 0, 0);
     } else if (ok && fa_wait_warp(&bars->acc_done, 0, watch, SITE_KV_ACC)) {
       tc_fence_after();
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = 0; cc < SLICE / 32; ++cc) {
         float a[32];
-        tmem_ld_x32f(tmem + lane_addr + (w == 0 ? C::T_DV : C::T_DK) + cc * 32, a);
+        tmem_ld_x32f(tmem + lane_addr + (is_dv ? C::T_DV : C::T_DK) + col0 + cc * 32, a);
         if (row_ok) {
           uint32_t pk[16];
 #pragma unroll
@@ -485,8 +567,14 @@ struct DqCfg {
   static constexpr int KV_OFF = 2 * TILE_BYTES;
   static constexpr int BAR_OFF = KV_OFF + NSLOT * TILE_BYTES;
   static constexpr int SMEM_BYTES = BAR_OFF + 256;
-  static constexpr int THREADS = 384;
-  // TMEM: S/dS double buffer at [0,128) and [384,512), dP at [128,256), dQ at [256,256+D)
+  static constexpr int NCW = 4;  // compute warpgroups; each owns COLS key columns
+  static constexpr int COLS = 128 / NCW;
+  static constexpr int NCT = 128 * NCW;
+  static constexpr int THREADS = 128 + NCT;
+  // TMEM: S double buffer at [0,128) and [384,512), dP at [128,256), dQ at
+  // [256,256+D). Once S is consumed, the 16-key chunk kk of dS (fp16 pairs)
+  // sits at columns 16kk+0..7 of its buffer, inside the columns its compute
+  // group has read itself.
   static constexpr uint32_t T_S0 = 0, T_S1 = 384, T_DP = 128, T_DQ = 256;
   static_assert(T_DQ + D <= T_S1, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -535,7 +623,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     mbar_init(&bars->s_full[0], 1);
     mbar_init(&bars->s_full[1], 1);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->ds_ready, 256);
+    mbar_init(&bars->ds_ready, C::NCT);
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
@@ -588,8 +676,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_blocks > 0) {
-      constexpr uint32_t ID_SS = idesc_bf16_f32(128, 128, 0, 0);  // S = Q K^T, dP = dO V^T
-      constexpr uint32_t ID_DQ = idesc_bf16_f32(128, D, 0, 1);    // dQ: A = dS from TMEM, B = K MN-major
+      constexpr uint32_t ID_SS = idesc_f16_f32(128, 128, 0, 0);  // S = Q K^T, dP = dO V^T
+      constexpr uint32_t ID_DQ = idesc_f16_f32(128, D, 0, 1);    // dQ: dS from TMEM, K MN-major
       const uint32_t q_a = smem_u32(smem + C::Q_OFF);
       const uint32_t do_a = smem_u32(smem + C::DO_OFF);
       const uint32_t kv_base = smem_u32(smem + C::KV_OFF);
@@ -608,16 +696,10 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         }
         mma_commit(&bars->s_full[jj & 1]);
       };
-      auto issue_dp = [&](int jj) {
-        const uint32_t va = slot_addr(2 * jj + 1);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
-          mma_ss(tmem + C::T_DP, sdesc_sw128(do_a + off, 16, 1024), sdesc_sw128(va + off, 16, 1024), ID_SS,
-                 kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bars->dp_full);
-        mma_commit(&bars->kv_empty[(2 * jj + 1) % C::NSLOT]);  // V_j: only dP reads it
+      auto dp_mma = [&](int jj, int kk) {
+        const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
+        mma_ss(tmem + C::T_DP, sdesc_sw128(do_a + off, 16, 1024), sdesc_sw128(slot_addr(2 * jj + 1) + off, 16, 1024),
+               ID_SS, kk > 0 ? 1u : 0u);
       };
       bool ok = fa_wait(&bars->q_full, 0, watch, SITE_DQ_Q);
       for (int jj = 0; jj < 2 && jj < n_blocks && ok; ++jj) {
@@ -628,34 +710,36 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       }
       if (ok && (ok = wait_full(1, SITE_DQ_V))) {
         tc_fence_after();
-        issue_dp(0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) dp_mma(0, kk);
+        mma_commit(&bars->dp_full);
+        mma_commit(&bars->kv_empty[1 % C::NSLOT]);  // V_0: only dP reads it
       }
-      // Order per key tile jj: [dS(jj) formed] dP(jj+1), dQ(jj), S(jj+2). dS(jj) sits
-      // over the consumed S(jj) buffer, so the dP columns are free as soon as dS(jj)
-      // has been formed, and S(jj+2) reuses the buffer after dQ(jj) has read it.
+      // Per key tile jj, once dS(jj) is formed: dQ(jj) interleaved with dP(jj+1)
+      // (independent accumulators), then S(jj+2) into the buffer dQ(jj) just read.
       for (int jj = 0; jj < n_blocks && ok; ++jj) {
         if (!(ok = fa_wait(&bars->ds_ready, uint32_t(jj) & 1u, watch, SITE_DQ_DS))) break;
+        const bool more = jj + 1 < n_blocks;
+        if (more && !(ok = wait_full(2 * (jj + 1) + 1, SITE_DQ_V))) break;
         tc_fence_after();
-        if (jj + 1 < n_blocks) {
-          if (!(ok = wait_full(2 * (jj + 1) + 1, SITE_DQ_V))) break;
-          tc_fence_after();
-          issue_dp(jj + 1);
-        }
-        // dQ += dS_hi K + dS_lo K ; keys 16kk.. of dS sit at column 64*(kk/4) + 16*(kk%4) (hi), +8 (lo)
+        // dQ += dS K ; keys 16kk..16kk+15 of dS sit at columns 16kk+0..7 of the S buffer
         const uint32_t ka = slot_addr(2 * jj);
         const uint32_t ts = (jj & 1) ? C::T_S1 : C::T_S0;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t da = tmem + ts + (kk / 4) * 64 + (kk % 4) * 16;
-          const uint64_t bd = sdesc_sw128(ka + kk * 2048, C::PANEL_BYTES, 1024);
-          mma_ts(tmem + C::T_DQ, da, bd, ID_DQ, (jj > 0 || kk > 0) ? 1u : 0u);
-          mma_ts(tmem + C::T_DQ, da + 8, bd, ID_DQ, 1u);
+          mma_ts(tmem + C::T_DQ, tmem + ts + kk * 16, sdesc_sw128(ka + kk * 2048, C::PANEL_BYTES, 1024), ID_DQ,
+                 (jj > 0 || kk > 0) ? 1u : 0u);
+          if (more && kk < D / 16) dp_mma(jj + 1, kk);
         }
-        mma_commit(&bars->kv_empty[(2 * jj) % C::NSLOT]);  // K_j: read by S_j and this dQ
+        if (more) {
+          mma_commit(&bars->dp_full);
+          mma_commit(&bars->kv_empty[(2 * (jj + 1) + 1) % C::NSLOT]);  // V_{jj+1}
+        }
+        mma_commit(&bars->kv_empty[(2 * jj) % C::NSLOT]);  // K_jj: read by S_jj and this dQ
         if (jj + 2 < n_blocks) {
           if (!(ok = wait_full(2 * (jj + 2), SITE_DQ_K))) break;
           tc_fence_after();
-          issue_s(jj + 2);  // into the buffer dQ(jj) just read (in-order)
+          issue_s(jj + 2);
         }
       }
       if (ok) {
@@ -667,7 +751,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ compute (thread = query row)
-    const int w = (warp - 4) / 4;  // key-column half
+    const int w = (warp - 4) / 4;  // key-column group: columns [w*COLS, (w+1)*COLS)
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const int i = row0 + r;
@@ -685,21 +769,23 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     bool ok = true;
     for (int jj = 0; jj < n_blocks && ok; ++jj) {
       const int sb = jj & 1;
-      const int kb = (jb + jj) * 128 + w * 64;  // first key of this half
+      const uint32_t ts = sb ? C::T_S1 : C::T_S0;
+      const int kb = (jb + jj) * 128 + w * C::COLS;  // first key of this group
       if (!(ok = fa_wait_warp(&bars->s_full[sb], uint32_t(jj >> 1) & 1u, watch, SITE_DQ_S))) break;
       tc_fence_after();
-      float pv[64];
-      tmem_ld_x64f(tmem + lane_addr + (sb ? C::T_S1 : C::T_S0) + w * 64, pv);
+      float pv[C::COLS];
+      tmem_ld_cols(tmem + lane_addr + ts + w * C::COLS, pv);
       const int kbase = (jb + jj) * 128;
       const bool need_mask = !(kbase >= tile_lo_max && kbase + 127 <= tile_hi_min);
       if (has_alibi) {
         const float d0 = float(c_i - kb);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) pv[c] = ex2_approx(fmaf(pv[c], sl, -slope_log2 * fabsf(d0 - float(c)) - l2));
+        for (int c = 0; c < C::COLS; ++c)
+          pv[c] = ex2_approx(fmaf(pv[c], sl, -slope_log2 * fabsf(d0 - float(c)) - l2));
       } else {
         const uint64_t sl2 = f2_pack(sl, sl), nl2 = f2_pack(-l2, -l2);
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
+        for (int c = 0; c < C::COLS; c += 2) {
           float a0, a1;
           f2_unpack(f2_fma(f2_pack(pv[c], pv[c + 1]), sl2, nl2), a0, a1);
           pv[c] = ex2_approx(a0);
@@ -709,49 +795,46 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       if (need_mask) {
         const int lo = rr.lo - kb, hi = rr.hi - kb;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) pv[c] = (c >= lo && c <= hi) ? pv[c] : 0.0f;
+        for (int c = 0; c < C::COLS; ++c) pv[c] = (c >= lo && c <= hi) ? pv[c] : 0.0f;
       }
       if (!(ok = fa_wait_warp(&bars->dp_full, uint32_t(jj) & 1u, watch, SITE_DQ_DP))) break;
       tc_fence_after();
+      {
+        float dp[C::COLS];
+        tmem_ld_cols(tmem + lane_addr + C::T_DP + w * C::COLS, dp);
+        uint32_t pk[C::COLS / 2];
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        float dp[16];
-        tmem_ld_x16f(tmem + lane_addr + C::T_DP + w * 64 + 16 * c4, dp);
-        uint32_t hl[16];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int c = 16 * c4 + 2 * e;
+        for (int e = 0; e < C::COLS / 2; ++e) {
           float s0, s1;
-          ds_pair(pv[c], pv[c + 1], dp[2 * e], dp[2 * e + 1], dval, dval, s0, s1);
-          split_hilo(s0, s1, hl[e], hl[8 + e]);
+          ds_pair(pv[2 * e], pv[2 * e + 1], dp[2 * e], dp[2 * e + 1], dval, dval, s0, s1);
+          pk[e] = pack_f16x2(s0, s1);
         }
-        // dS hi/lo over the consumed S columns of this buffer (S is in registers)
-        tmem_st_x16(tmem + lane_addr + (sb ? C::T_S1 : C::T_S0) + w * 64 + 16 * c4, hl);
+        // dS fp16 over the consumed S columns of this buffer (S is in registers)
+#pragma unroll
+        for (int c = 0; c < C::COLS / 16; ++c) tmem_st_x8(tmem + lane_addr + ts + w * C::COLS + 16 * c, pk + 8 * c);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars->ds_ready);
     }
-    // ------------------------------------------------------------ dQ epilogue (each group half of D)
+    // ------------------------------------------------------------ dQ epilogue (each group D/NCW columns)
+    constexpr int SLICE = D / C::NCW;  // 16 or 32
     const bool row_ok = i < p.Sq;
-    __nv_bfloat16* dst = p.dq + ((size_t(b) * p.Sq + size_t(i)) * p.H + h) * size_t(D) + w * (D / 2);
+    __nv_bfloat16* dst = p.dq + ((size_t(b) * p.Sq + size_t(i)) * p.H + h) * size_t(D) + w * SLICE;
     if (n_blocks == 0) {
       if (row_ok)
-        for (int e = 0; e < D / 16; ++e) reinterpret_cast<uint4*>(dst)[e] = make_uint4(0, 0, 0, 0);
+        for (int e = 0; e < SLICE / 8; ++e) reinterpret_cast<uint4*>(dst)[e] = make_uint4(0, 0, 0, 0);
     } else if (ok && fa_wait_warp(&bars->acc_done, 0, watch, SITE_DQ_ACC)) {
       tc_fence_after();
-#pragma unroll 1
-      for (int cc = 0; cc < D / 64; ++cc) {
-        float a[32];
-        tmem_ld_x32f(tmem + lane_addr + C::T_DQ + w * (D / 2) + cc * 32, a);
-        if (row_ok) {
-          uint32_t pk[16];
+      float a[SLICE];
+      tmem_ld_cols(tmem + lane_addr + C::T_DQ + w * SLICE, a);
+      if (row_ok) {
+        uint32_t pk[SLICE / 2];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(a[2 * e] * p.scale, a[2 * e + 1] * p.scale);
+        for (int e = 0; e < SLICE / 2; ++e) pk[e] = pack_bf16x2(a[2 * e] * p.scale, a[2 * e + 1] * p.scale);
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            reinterpret_cast<uint4*>(dst + cc * 32)[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-        }
+        for (int e = 0; e < SLICE / 8; ++e)
+          reinterpret_cast<uint4*>(dst)[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
       }
     }
   }
@@ -765,60 +848,23 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
   }
 }
 
-// D_i = rowsum(dO * O), L2 = L*log2(e) (+inf where L = -inf or on padding).
-// One warp per (b, h, row).
-template <int D>
-__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
-  constexpr int PER = D / 32;
-  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  const int h = blockIdx.y;
-  const int b = blockIdx.z;
-  if (row >= p.Sq_pad) return;
-  const size_t vi = (size_t(b) * p.H + h) * p.Sq_pad + row;
-  if (row >= p.Sq) {
-    if (lane == 0) {
-      p.dvec[vi] = 0.0f;
-      p.l2[vi] = INFINITY;
-    }
-    return;
-  }
-  const size_t ro = ((size_t(b) * p.Sq + row) * p.H + h) * size_t(D) + lane * PER;
-  float acc = 0.0f;
-#pragma unroll
-  for (int e = 0; e < PER; e += 2) {
-    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(p.dout + ro + e);
-    const __nv_bfloat162 o = *reinterpret_cast<const __nv_bfloat162*>(p.out + ro + e);
-    acc = fmaf(__low2float(a), __low2float(o), acc);
-    acc = fmaf(__high2float(a), __high2float(o), acc);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) {
-    p.dvec[vi] = acc;
-    const float L = p.lse[(size_t(b) * p.H + h) * p.Sq + row];
-    p.l2[vi] = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
-  }
-}
-
 static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Workspace: L2 and D vectors (B, H, Sq_pad) fp32, then fp16 copies of Q, dO
+// (B, Sq, H, D) and K, V (B, Sk, H, D).
 size_t bwd_workspace_bytes(int B, int Sq, int Sk, int H, int D, int deterministic) {
-  (void)Sk;
-  (void)D;
   (void)deterministic;  // every run is deterministic: no cross-CTA reductions
   const size_t sq_pad = size_t((Sq + 127) / 128) * 128;
-  return 2 * al256(size_t(B) * H * sq_pad * 4);  // L2, D
+  const size_t vec = al256(size_t(B) * H * sq_pad * 4);
+  const size_t qside = al256(size_t(B) * Sq * H * D * 2);
+  const size_t kside = al256(size_t(B) * Sk * H * D * 2);
+  return 2 * vec + 2 * qside + 2 * kside;
 }
 
 template <int D>
 static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, const void* k, const void* v,
                         const void* out, const float* lse, void* dq, void* dk, void* dv, void* ws,
                         cudaStream_t stream) {
-  CUtensorMap mq, mk, mv, mdo;
-  if (!make_bshd_map(&mq, q, s.B, s.Sq, s.H, D, 128) || !make_bshd_map(&mk, k, s.B, s.Sk, s.H, D, 128) ||
-      !make_bshd_map(&mv, v, s.B, s.Sk, s.H, D, 128) || !make_bshd_map(&mdo, dout, s.B, s.Sq, s.H, D, 128))
-    return FA_ERR_CUDA;
   BwdParams p;
   p.B = s.B;
   p.Sq = s.Sq;
@@ -827,11 +873,20 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
   p.Sq_pad = ((s.Sq + 127) / 128) * 128;
   p.n_qt = p.Sq_pad / 128;
   uint8_t* w = static_cast<uint8_t*>(ws);
+  const size_t vec = al256(size_t(s.B) * s.H * p.Sq_pad * 4);
+  const size_t qside = al256(size_t(s.B) * s.Sq * s.H * D * 2);
+  const size_t kside = al256(size_t(s.B) * s.Sk * s.H * D * 2);
   p.l2 = reinterpret_cast<float*>(w);
-  w += al256(size_t(s.B) * s.H * p.Sq_pad * 4);
-  p.dvec = reinterpret_cast<float*>(w);
+  p.dvec = reinterpret_cast<float*>(w + vec);
+  p.q16 = reinterpret_cast<uint16_t*>(w + 2 * vec);
+  p.do16 = reinterpret_cast<uint16_t*>(w + 2 * vec + qside);
+  p.k16 = reinterpret_cast<uint16_t*>(w + 2 * vec + 2 * qside);
+  p.v16 = reinterpret_cast<uint16_t*>(w + 2 * vec + 2 * qside + kside);
   p.dout = static_cast<const __nv_bfloat16*>(dout);
   p.out = static_cast<const __nv_bfloat16*>(out);
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
   p.lse = lse;
   p.dq = static_cast<__nv_bfloat16*>(dq);
   p.dk = static_cast<__nv_bfloat16*>(dk);
@@ -845,9 +900,23 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
   p.status = device_status_word();
   if (!p.status) return FA_ERR_CUDA;
   if (s.B > 65535 || s.H > 65535) return FA_ERR_UNSUPPORTED;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_bshd_map(&mq, p.q16, s.B, s.Sq, s.H, D, 128, true) ||
+      !make_bshd_map(&mk, p.k16, s.B, s.Sk, s.H, D, 128, true) ||
+      !make_bshd_map(&mv, p.v16, s.B, s.Sk, s.H, D, 128, true) ||
+      !make_bshd_map(&mdo, p.do16, s.B, s.Sq, s.H, D, 128, true))
+    return FA_ERR_CUDA;
 
-  fa_bwd_pre_kernel<D><<<dim3(p.Sq_pad / 8, s.H, s.B), 256, 0, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  {
+    const long long cpr = D / 8;
+    const long long n_q = ((long long)s.B * s.Sq * s.H * cpr + 31) & ~31LL;
+    const long long n_k = ((long long)s.B * s.Sk * s.H * cpr + 31) & ~31LL;
+    const long long total = n_q + n_k + (long long)s.B * s.H * (p.Sq_pad - s.Sq);
+    const long long cap = (long long)device_sm_count() * 8;  // 8 blocks of 256 threads per SM
+    const int grid = int(std::max(1LL, std::min(cap, (total + 255) / 256)));
+    fa_bwd_pre_kernel<D><<<grid, 256, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  }
   auto kv = fa_bwd_dkdv_kernel<D>;
   if (cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, KvCfg<D>::SMEM_BYTES) != cudaSuccess)
     return FA_ERR_CUDA;

@@ -22,14 +22,10 @@ unsigned int* device_status_word();
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
-// Encodes a 4-D tiled TMA map over a (B, S, H, D) bf16 tensor: box of
-// 64 head-dim elements (128 B, 128-byte swizzle) x 1 head x `box_rows` rows
-// x 1 batch. Returns false if the driver rejects it.
-bool make_bshd_map(CUtensorMap* map, const void* base, int B, int S, int H, int D, int box_rows);
-
-// Encodes a 4-D tiled TMA map over a (B, S, H, D) fp32 tensor: box of 32
-// elements (128 B, 128-byte swizzle) x 1 head x 128 rows x 1 batch.
-bool make_bshd_f32_map(CUtensorMap* map, const void* base, int B, int S, int H, int D);
+// Encodes a 4-D tiled TMA map over a (B, S, H, D) 16-bit tensor (bf16, or
+// fp16 with `f16` set): box of 64 head-dim elements (128 B, 128-byte swizzle)
+// x 1 head x `box_rows` rows x 1 batch. Returns false if the driver rejects it.
+bool make_bshd_map(CUtensorMap* map, const void* base, int B, int S, int H, int D, int box_rows, bool f16 = false);
 
 // Kernel launchers (return an fa_status value).
 int fwd_launch(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,

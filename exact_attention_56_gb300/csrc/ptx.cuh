@@ -219,6 +219,10 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// bf16 pair -> fp16 pair (exact for |x| in the fp16 normal range).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -305,6 +309,12 @@ __device__ __forceinline__ void tmem_ld_x128(uint32_t taddr, uint32_t (&r)[128])
                : "r"(taddr) : "memory");
 }
 
+// Stores 8 consecutive 32-bit TMEM columns for this warp's 32 lanes (no wait; see tmem_st_wait).
+__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]) : "memory");
+}
+
 // Stores 16 consecutive 32-bit TMEM columns for this warp's 32 lanes (no wait; see tmem_st_wait).
 __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
@@ -353,6 +363,21 @@ __device__ __forceinline__ void tmem_ld_x16f(uint32_t taddr, float (&r)[16]) {
                "tcgen05.wait::ld.sync.aligned;"
                : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]), "=f"(r[7]), "=f"(r[8]), "=f"(r[9]), "=f"(r[10]), "=f"(r[11]), "=f"(r[12]), "=f"(r[13]), "=f"(r[14]), "=f"(r[15])
                : "r"(taddr) : "memory");
+}
+
+// Loads N fp32 TMEM columns (N = 16, 32, 64 or 128) and waits.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&r)[N]) {
+  if constexpr (N == 16) {
+    tmem_ld_x16f(taddr, r);
+  } else if constexpr (N == 32) {
+    tmem_ld_x32f(taddr, r);
+  } else if constexpr (N == 64) {
+    tmem_ld_x64f(taddr, r);
+  } else {
+    static_assert(N == 128, "unsupported TMEM load width");
+    tmem_ld_x128f(taddr, r);
+  }
 }
 
 }  // namespace fa

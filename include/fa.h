@@ -79,8 +79,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, i
 
 /*
  * Bytes of device workspace fa_bwd needs: the per-row D_i = rowsum(dO * O)
- * and L*log2(e) vectors, (B, H, Sq rounded up to 128) fp32 each.
- * Returns 0 for arguments fa_bwd would reject.
+ * and L*log2(e) vectors, (B, H, Sq rounded up to 128) fp32 each, and fp16
+ * copies of q, dout (B, Sq, H, D) and k, v (B, Sk, H, D), each section
+ * rounded up to 256 bytes. Returns 0 for arguments fa_bwd would reject.
  */
 size_t fa_bwd_workspace_size(int B, int Sq, int Sk, int H, int D, int deterministic);
 
@@ -93,6 +94,9 @@ size_t fa_bwd_workspace_size(int B, int Sq, int Sk, int H, int D, int determinis
  * run is bitwise reproducible in either mode, because no output element is
  * accumulated across thread blocks: one kernel per 128-key tile produces dK
  * and dV, another per 128-row query tile produces dQ.
+ * Precision: the products run on fp16 copies of the inputs with fp16 P and
+ * dS and fp32 accumulation, so dout, q, k and v must lie in the fp16 range
+ * (|x| < 65504; larger values become infinite and the gradients non-finite).
  * workspace: caller-owned device buffer of at least fa_bwd_workspace_size()
  * bytes, 256-byte aligned; its contents on entry are ignored.
  * Supported: D in {64, 128}.

@@ -66,8 +66,11 @@ def test_argument_checks_without_gpu(lib):
 def test_workspace_sizes(lib):
     lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
     lib.fa_decode_workspace_size.restype = ctypes.c_size_t
-    # two fp32 per-row vectors (L in log2 units and rowsum(dO*O)), rows padded to 128
-    assert lib.fa_bwd_workspace_size(1, 100, 128, 2, 64, 0) >= 2 * 2 * 128 * 4
+    # two fp32 per-row vectors (L in log2 units and rowsum(dO*O)), rows padded to 128,
+    # and fp16 copies of q, dout (B, Sq, H, D) and k, v (B, Sk, H, D)
+    B, Sq, Sk, H, D = 1, 100, 128, 2, 64
+    assert lib.fa_bwd_workspace_size(B, Sq, Sk, H, D, 0) >= 2 * B * H * 128 * 4 + 2 * B * Sq * H * D * 2 + \
+        2 * B * Sk * H * D * 2
     assert lib.fa_bwd_workspace_size(1, 128, 128, 2, 96, 0) == 0
     assert lib.fa_decode_workspace_size(2, 1, 1000, 4, 128, 3) >= 2 * 4 * 3 * (128 + 1) * 4
     assert lib.fa_decode_workspace_size(2, 17, 1000, 4, 128, 3) == 0
