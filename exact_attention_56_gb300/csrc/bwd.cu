@@ -24,10 +24,11 @@
 //                    exponentials run; then dK (times scale) and dV are written.
 //   fa_bwd_dq        one CTA per (128-row query tile, head, batch), looping over
 //                    the live key tiles (the forward's shape, thread = query row):
-//                      S  = Q K^T -> TMEM (double-buffered), P = 2^(S*... - L2)
-//                      dP = dO V^T, dS = P o (dP - D) -> fp16 over the consumed S
-//                      dQ += dS K, interleaved with dP of the next key tile
-//                    then writes dQ (times scale) once.
+//                      S  = Q K^T -> TMEM, P = 2^(S*scale*log2e + bias - L2)
+//                      dP = dO V^T, dS = P o (dP - D) -> fp16 over dP
+//                      dQ += dS K
+//                    S of the next key tile is computed while this one's
+//                    exponentials run; then dQ (times scale) is written once.
 // Every output element is produced by one CTA in a fixed order, so every run
 // is bitwise reproducible; the deterministic flag costs nothing.
 //
@@ -35,9 +36,12 @@
 // fp16 copies of the bf16 inputs). fp16 keeps 11 significant bits, enough for
 // the gradients to stay at bf16's own output rounding against an fp64
 // reference with one MMA per product; it limits the backward's inputs to the
-// fp16 range (|x| < 65504). MMAs into one TMEM accumulator serialise on a
-// ~100-cycle dependency, so independent chains are interleaved where the
-// TMEM budget allows.
+// fp16 range (|x| < 65504).
+//
+// Both main kernels follow one schedule: the score tile of the next step is
+// issued as soon as the compute warps hold the current one in registers, and
+// the operand rings are deep enough that a tile is loaded about one step
+// before the MMA that reads it.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -212,20 +216,22 @@ struct KvCfg {
   static constexpr int PANELS = D / 64;
   static constexpr int PANEL_BYTES = 128 * 128;
   static constexpr int TILE_BYTES = PANELS * PANEL_BYTES;
-  static constexpr int NQ = 2;   // Q (+ L2, D) stages
-  static constexpr int NDO = 2;  // dO stages
+  // Q of the next tile is read early (S^T of tile ii+1 is issued while tile ii
+  // is still being processed), so Q gets a third stage; dO is read last.
+  static constexpr int NQ = 3;   // Q stages
+  static constexpr int NDO = 2;  // dO (+ L2, D) stages
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = TILE_BYTES;
   static constexpr int Q_OFF = 2 * TILE_BYTES;
   static constexpr int DO_OFF = Q_OFF + NQ * TILE_BYTES;
-  static constexpr int VEC_OFF = DO_OFF + NDO * TILE_BYTES;  // per Q stage: L2[128], D[128]
-  static constexpr int BAR_OFF = VEC_OFF + NQ * 1024;
+  static constexpr int VEC_OFF = DO_OFF + NDO * TILE_BYTES;  // per dO stage: L2[128], D[128]
+  static constexpr int BAR_OFF = VEC_OFF + NDO * 1024;
   static constexpr int SMEM_BYTES = BAR_OFF + 256;
   static constexpr int NCW = 4;  // compute warpgroups; each owns COLS query columns
   static constexpr int COLS = 128 / NCW;
   static constexpr int NCT = 128 * NCW;  // compute threads
   static constexpr int THREADS = 128 + NCT;
-  static constexpr int Q_TX = TILE_BYTES + 1024;
+  static constexpr int DO_TX = TILE_BYTES + 1024;
   // TMEM: S^T [0,128) fp32; dP^T [128,256) fp32, over which, once consumed, the
   // 16-query chunk kk of P^T (fp16 pairs) sits at columns 16kk+0..7 and that of
   // dS^T at 16kk+8..15, so every compute group writes only inside the dP^T
@@ -237,7 +243,7 @@ struct KvCfg {
 
 struct KvBars {
   uint64_t kv_full;
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[3], q_empty[3];
   uint64_t do_full[2], do_empty[2];
   uint64_t s_full, s_free, dp_full, pd_ready, acc_done, drain;
   uint32_t tmem_base;
@@ -275,9 +281,11 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::NQ; ++s) {
       mbar_init(&bars->q_full[s], 1);
       mbar_init(&bars->q_empty[s], 1);
+    }
+    for (int s = 0; s < C::NDO; ++s) {
       mbar_init(&bars->do_full[s], 1);
       mbar_init(&bars->do_empty[s], 1);
     }
@@ -318,19 +326,19 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
         const int s = ii % C::NQ;
         const int i0 = (qt_first + ii) * 128;
         if (!fa_wait(&bars->q_empty[s], (uint32_t(ii / C::NQ) & 1u) ^ 1u, watch, SITE_KV_EMPTY)) break;
-        mbar_arrive_expect_tx(&bars->q_full[s], C::Q_TX);
+        mbar_arrive_expect_tx(&bars->q_full[s], C::TILE_BYTES);
         for (int pn = 0; pn < C::PANELS; ++pn)
           tma_load_4d(smem + C::Q_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bars->q_full[s], pn * 64,
                       h, i0, b);
-        bulk_load(smem + C::VEC_OFF + s * 1024, p.l2 + vec_base + i0, 512, &bars->q_full[s]);
-        bulk_load(smem + C::VEC_OFF + s * 1024 + 512, p.dvec + vec_base + i0, 512, &bars->q_full[s]);
         q_issued = ii + 1;
         const int d = ii % C::NDO;
         if (!fa_wait(&bars->do_empty[d], (uint32_t(ii / C::NDO) & 1u) ^ 1u, watch, SITE_KV_DOEMPTY)) break;
-        mbar_arrive_expect_tx(&bars->do_full[d], C::TILE_BYTES);
+        mbar_arrive_expect_tx(&bars->do_full[d], C::DO_TX);
         for (int pn = 0; pn < C::PANELS; ++pn)
           tma_load_4d(smem + C::DO_OFF + d * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_do, &bars->do_full[d],
                       pn * 64, h, i0, b);
+        bulk_load(smem + C::VEC_OFF + d * 1024, p.l2 + vec_base + i0, 512, &bars->do_full[d]);
+        bulk_load(smem + C::VEC_OFF + d * 1024 + 512, p.dvec + vec_base + i0, 512, &bars->do_full[d]);
         do_issued = ii + 1;
       }
       // every copy must land before the CTA may exit
@@ -342,44 +350,43 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Descriptors are built once; each k-step and stage is a constant added to
+    // the start-address field, so issuing keeps pace with the tensor pipe.
     if (lane == 0 && n_iter > 0) {
       constexpr uint32_t ID_SS = idesc_f16_f32(128, 128, 0, 0);  // S^T, dP^T: both operands K-major
       constexpr uint32_t ID_TN = idesc_f16_f32(128, D, 0, 1);    // dV, dK: A from TMEM, B (dO / Q) MN-major
-      const uint32_t k_a = smem_u32(smem + C::K_OFF);
-      const uint32_t v_a = smem_u32(smem + C::V_OFF);
-      auto q_addr = [&](int ii) { return smem_u32(smem + C::Q_OFF + (ii % C::NQ) * C::TILE_BYTES); };
-      auto do_addr = [&](int ii) { return smem_u32(smem + C::DO_OFF + (ii % C::NDO) * C::TILE_BYTES); };
-      auto issue_st = [&](int ii) {  // S^T = K Q^T
-        const uint32_t q_a = q_addr(ii);
+      const uint64_t k_desc = sdesc_sw128(smem_u32(smem + C::K_OFF), 16, 1024);
+      const uint64_t v_desc = sdesc_sw128(smem_u32(smem + C::V_OFF), 16, 1024);
+      const uint64_t q_kdesc = sdesc_sw128(smem_u32(smem + C::Q_OFF), 16, 1024);     // Q as K-major (S^T)
+      const uint64_t do_kdesc = sdesc_sw128(smem_u32(smem + C::DO_OFF), 16, 1024);   // dO as K-major (dP^T)
+      const uint64_t q_mdesc = sdesc_sw128(smem_u32(smem + C::Q_OFF), C::PANEL_BYTES, 1024);    // MN-major (dK)
+      const uint64_t do_mdesc = sdesc_sw128(smem_u32(smem + C::DO_OFF), C::PANEL_BYTES, 1024);  // MN-major (dV)
+      const uint32_t t_s = tmem + C::T_S, t_dp = tmem + C::T_DP, t_dv = tmem + C::T_DV, t_dk = tmem + C::T_DK;
+      bool ok = fa_wait(&bars->kv_full, 0, watch, SITE_KV_KV) && fa_wait(&bars->q_full[0], 0, watch, SITE_KV_QFULL);
+      if (ok) {  // S^T(0) = K Q^T
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
-          mma_ss(tmem + C::T_S, sdesc_sw128(k_a + off, 16, 1024), sdesc_sw128(q_a + off, 16, 1024), ID_SS,
-                 kk > 0 ? 1u : 0u);
+          mma_ss(t_s, sdesc_adv(k_desc, off), sdesc_adv(q_kdesc, off), ID_SS, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars->s_full);
-      };
-      auto issue_dpt = [&](int ii) {  // dP^T = V dO^T
-        const uint32_t do_a = do_addr(ii);
+      }
+      if (ok && (ok = fa_wait(&bars->do_full[0], 0, watch, SITE_KV_DOFULL))) {  // dP^T(0) = V dO^T
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
-          mma_ss(tmem + C::T_DP, sdesc_sw128(v_a + off, 16, 1024), sdesc_sw128(do_a + off, 16, 1024), ID_SS,
-                 kk > 0 ? 1u : 0u);
+          mma_ss(t_dp, sdesc_adv(v_desc, off), sdesc_adv(do_kdesc, off), ID_SS, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars->dp_full);
-      };
-      bool ok = fa_wait(&bars->kv_full, 0, watch, SITE_KV_KV) && fa_wait(&bars->q_full[0], 0, watch, SITE_KV_QFULL);
-      if (ok) {
-        tc_fence_after();
-        issue_st(0);
-      }
-      if (ok && (ok = fa_wait(&bars->do_full[0], 0, watch, SITE_KV_DOFULL))) {
-        tc_fence_after();
-        issue_dpt(0);
       }
       for (int ii = 0; ii < n_iter && ok; ++ii) {
         const bool more = ii + 1 < n_iter;
+        const uint32_t q_cur = uint32_t(ii % C::NQ) * C::TILE_BYTES;        // Q stage of tile ii
+        const uint32_t q_nxt = uint32_t((ii + 1) % C::NQ) * C::TILE_BYTES;  // Q stage of tile ii + 1
+        const uint32_t do_cur = uint32_t(ii % C::NDO) * C::TILE_BYTES;
+        const uint32_t do_nxt = uint32_t((ii + 1) % C::NDO) * C::TILE_BYTES;
         // S^T of the next tile as soon as every compute group holds this one in registers
         if (more) {
           if (!(ok = fa_wait(&bars->s_free, uint32_t(ii) & 1u, watch, SITE_KV_SFREE))) break;
@@ -387,20 +394,26 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
                              SITE_KV_QFULL)))
             break;
           tc_fence_after();
-          issue_st(ii + 1);
+          const uint64_t qd = sdesc_adv(q_kdesc, q_nxt);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
+            mma_ss(t_s, sdesc_adv(k_desc, off), sdesc_adv(qd, off), ID_SS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars->s_full);
         }
         // dV += P^T dO and dK += dS^T Q, two independent chains; the 16-query chunk kk
         // of P^T sits at dP^T column 16kk, that of dS^T at 16kk+8 (two fp16 per column)
         if (!(ok = fa_wait(&bars->pd_ready, uint32_t(ii) & 1u, watch, SITE_KV_PD))) break;
         tc_fence_after();
-        const uint32_t q_a = q_addr(ii), do_a = do_addr(ii);
+        {
+          const uint64_t dod = sdesc_adv(do_mdesc, do_cur), qd = sdesc_adv(q_mdesc, q_cur);
+          const uint32_t acc0 = ii > 0 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t acc = (ii > 0 || kk > 0) ? 1u : 0u;
-          mma_ts(tmem + C::T_DV, tmem + C::T_DP + kk * 16, sdesc_sw128(do_a + kk * 2048, C::PANEL_BYTES, 1024), ID_TN,
-                 acc);
-          mma_ts(tmem + C::T_DK, tmem + C::T_DP + kk * 16 + 8, sdesc_sw128(q_a + kk * 2048, C::PANEL_BYTES, 1024),
-                 ID_TN, acc);
+          for (int kk = 0; kk < 8; ++kk) {
+            mma_ts(t_dv, t_dp + kk * 16, sdesc_adv(dod, kk * 2048), ID_TN, kk > 0 ? 1u : acc0);
+            mma_ts(t_dk, t_dp + kk * 16 + 8, sdesc_adv(qd, kk * 2048), ID_TN, kk > 0 ? 1u : acc0);
+          }
         }
         mma_commit(&bars->do_empty[ii % C::NDO]);
         mma_commit(&bars->q_empty[ii % C::NQ]);
@@ -410,7 +423,13 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
                              SITE_KV_DOFULL)))
             break;
           tc_fence_after();
-          issue_dpt(ii + 1);
+          const uint64_t dod = sdesc_adv(do_kdesc, do_nxt);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
+            mma_ss(t_dp, sdesc_adv(v_desc, off), sdesc_adv(dod, off), ID_SS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars->dp_full);
         }
       }
       if (ok) {
@@ -450,13 +469,13 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
     const float sl = p.scale_log2;
     bool ok = true;
     for (int ii = 0; ii < n_iter && ok; ++ii) {
-      const int s = ii % C::NQ;
+      const int d = ii % C::NDO;
       const int i0 = (qt_first + ii) * 128;
       const int ib = i0 + w * C::COLS;  // first query of this group
-      const float4* l2v = reinterpret_cast<const float4*>(smem + C::VEC_OFF + s * 1024) + w * (C::COLS / 4);
+      const float4* l2v = reinterpret_cast<const float4*>(smem + C::VEC_OFF + d * 1024) + w * (C::COLS / 4);
       const float4* dvv = l2v + 32;
-      // the L2 / D vectors of this tile land with Q
-      if (!(ok = fa_wait_warp(&bars->q_full[s], uint32_t(ii / C::NQ) & 1u, watch, SITE_KV_QFULL))) break;
+      // the L2 / D vectors of this tile land with dO
+      if (!(ok = fa_wait_warp(&bars->do_full[d], uint32_t(ii / C::NDO) & 1u, watch, SITE_KV_DOFULL))) break;
       if (!(ok = fa_wait_warp(&bars->s_full, uint32_t(ii) & 1u, watch, SITE_KV_S))) break;
       tc_fence_after();
       float pv[C::COLS];
@@ -571,19 +590,19 @@ struct DqCfg {
   static constexpr int COLS = 128 / NCW;
   static constexpr int NCT = 128 * NCW;
   static constexpr int THREADS = 128 + NCT;
-  // TMEM: S double buffer at [0,128) and [384,512), dP at [128,256), dQ at
-  // [256,256+D). Once S is consumed, the 16-key chunk kk of dS (fp16 pairs)
-  // sits at columns 16kk+0..7 of its buffer, inside the columns its compute
-  // group has read itself.
-  static constexpr uint32_t T_S0 = 0, T_S1 = 384, T_DP = 128, T_DQ = 256;
-  static_assert(T_DQ + D <= T_S1, "TMEM budget");
+  // TMEM: S at [0,128), dP at [128,256), dQ at [256,256+D). Once dP is
+  // consumed, the 16-key chunk kk of dS (fp16 pairs) sits at dP columns
+  // 16kk+0..7, inside the columns its compute group has read itself; S is
+  // free as soon as every group holds it in registers.
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 256;
+  static_assert(T_DQ + D <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
 struct DqBars {
   uint64_t q_full;
   uint64_t kv_full[8], kv_empty[8];
-  uint64_t s_full[2], dp_full, ds_ready, acc_done, drain;
+  uint64_t s_full, s_free, dp_full, ds_ready, acc_done, drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -620,8 +639,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
-    mbar_init(&bars->s_full[0], 1);
-    mbar_init(&bars->s_full[1], 1);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, C::NCT);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->ds_ready, C::NCT);
     mbar_init(&bars->acc_done, 1);
@@ -675,71 +694,77 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Per key tile jj: S(jj+1) as soon as every compute group holds S(jj) in
+    // registers (it overlaps the exponentials of tile jj); once dS(jj) is
+    // formed, dQ(jj) and then dP(jj+1), which overwrites dS(jj) (read in
+    // order). Descriptors are built once per tile; each k-step is a constant
+    // added to the start-address field.
     if (lane == 0 && n_blocks > 0) {
       constexpr uint32_t ID_SS = idesc_f16_f32(128, 128, 0, 0);  // S = Q K^T, dP = dO V^T
       constexpr uint32_t ID_DQ = idesc_f16_f32(128, D, 0, 1);    // dQ: dS from TMEM, K MN-major
-      const uint32_t q_a = smem_u32(smem + C::Q_OFF);
-      const uint32_t do_a = smem_u32(smem + C::DO_OFF);
-      const uint32_t kv_base = smem_u32(smem + C::KV_OFF);
-      auto slot_addr = [&](int it) { return kv_base + (it % C::NSLOT) * C::TILE_BYTES; };
+      const uint64_t q_desc = sdesc_sw128(smem_u32(smem + C::Q_OFF), 16, 1024);
+      const uint64_t do_desc = sdesc_sw128(smem_u32(smem + C::DO_OFF), 16, 1024);
+      const uint64_t kv_kdesc = sdesc_sw128(smem_u32(smem + C::KV_OFF), 16, 1024);            // slot 0, K-major
+      const uint64_t kv_mdesc = sdesc_sw128(smem_u32(smem + C::KV_OFF), C::PANEL_BYTES, 1024);  // slot 0, MN-major
+      const uint32_t t_s = tmem + C::T_S, t_dp = tmem + C::T_DP, t_dq = tmem + C::T_DQ;
+      auto slot_bytes = [](int it) { return uint32_t(it % C::NSLOT) * C::TILE_BYTES; };
       auto wait_full = [&](int it, uint32_t site) {
         return fa_wait(&bars->kv_full[it % C::NSLOT], uint32_t(it / C::NSLOT) & 1u, watch, site);
       };
-      auto issue_s = [&](int jj) {
-        const uint32_t ka = slot_addr(2 * jj);
-        const uint32_t ts = (jj & 1) ? C::T_S1 : C::T_S0;
+      auto issue_s = [=](int jj) {  // S(jj) = Q K_jj^T
+        const uint64_t kd = sdesc_adv(kv_kdesc, slot_bytes(2 * jj));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
-          mma_ss(tmem + ts, sdesc_sw128(q_a + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), ID_SS,
-                 kk > 0 ? 1u : 0u);
+          mma_ss(t_s, sdesc_adv(q_desc, off), sdesc_adv(kd, off), ID_SS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bars->s_full[jj & 1]);
       };
-      auto dp_mma = [&](int jj, int kk) {
-        const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
-        mma_ss(tmem + C::T_DP, sdesc_sw128(do_a + off, 16, 1024), sdesc_sw128(slot_addr(2 * jj + 1) + off, 16, 1024),
-               ID_SS, kk > 0 ? 1u : 0u);
-      };
-      bool ok = fa_wait(&bars->q_full, 0, watch, SITE_DQ_Q);
-      for (int jj = 0; jj < 2 && jj < n_blocks && ok; ++jj) {
-        if ((ok = wait_full(2 * jj, SITE_DQ_K))) {
-          tc_fence_after();
-          issue_s(jj);
+      auto issue_dp = [=](int jj) {  // dP(jj) = dO V_jj^T
+        const uint64_t vd = sdesc_adv(kv_kdesc, slot_bytes(2 * jj + 1));
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
+          mma_ss(t_dp, sdesc_adv(do_desc, off), sdesc_adv(vd, off), ID_SS, kk > 0 ? 1u : 0u);
         }
+      };
+      bool ok = fa_wait(&bars->q_full, 0, watch, SITE_DQ_Q) && wait_full(0, SITE_DQ_K);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        mma_commit(&bars->s_full);
       }
       if (ok && (ok = wait_full(1, SITE_DQ_V))) {
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) dp_mma(0, kk);
+        issue_dp(0);
         mma_commit(&bars->dp_full);
         mma_commit(&bars->kv_empty[1 % C::NSLOT]);  // V_0: only dP reads it
       }
-      // Per key tile jj, once dS(jj) is formed: dQ(jj) interleaved with dP(jj+1)
-      // (independent accumulators), then S(jj+2) into the buffer dQ(jj) just read.
       for (int jj = 0; jj < n_blocks && ok; ++jj) {
-        if (!(ok = fa_wait(&bars->ds_ready, uint32_t(jj) & 1u, watch, SITE_DQ_DS))) break;
         const bool more = jj + 1 < n_blocks;
-        if (more && !(ok = wait_full(2 * (jj + 1) + 1, SITE_DQ_V))) break;
-        tc_fence_after();
-        // dQ += dS K ; keys 16kk..16kk+15 of dS sit at columns 16kk+0..7 of the S buffer
-        const uint32_t ka = slot_addr(2 * jj);
-        const uint32_t ts = (jj & 1) ? C::T_S1 : C::T_S0;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          mma_ts(tmem + C::T_DQ, tmem + ts + kk * 16, sdesc_sw128(ka + kk * 2048, C::PANEL_BYTES, 1024), ID_DQ,
-                 (jj > 0 || kk > 0) ? 1u : 0u);
-          if (more && kk < D / 16) dp_mma(jj + 1, kk);
-        }
         if (more) {
-          mma_commit(&bars->dp_full);
-          mma_commit(&bars->kv_empty[(2 * (jj + 1) + 1) % C::NSLOT]);  // V_{jj+1}
+          if (!(ok = fa_wait(&bars->s_free, uint32_t(jj) & 1u, watch, SITE_DQ_S))) break;
+          if (!(ok = wait_full(2 * (jj + 1), SITE_DQ_K))) break;
+          tc_fence_after();
+          issue_s(jj + 1);
+          mma_commit(&bars->s_full);
+        }
+        // dQ += dS K ; keys 16kk..16kk+15 of dS sit at dP columns 16kk+0..7
+        if (!(ok = fa_wait(&bars->ds_ready, uint32_t(jj) & 1u, watch, SITE_DQ_DS))) break;
+        tc_fence_after();
+        {
+          const uint64_t kd = sdesc_adv(kv_mdesc, slot_bytes(2 * jj));
+          const uint32_t acc0 = jj > 0 ? 1u : 0u;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(t_dq, t_dp + kk * 16, sdesc_adv(kd, kk * 2048), ID_DQ, kk > 0 ? 1u : acc0);
         }
         mma_commit(&bars->kv_empty[(2 * jj) % C::NSLOT]);  // K_jj: read by S_jj and this dQ
-        if (jj + 2 < n_blocks) {
-          if (!(ok = wait_full(2 * (jj + 2), SITE_DQ_K))) break;
+        if (more) {
+          if (!(ok = wait_full(2 * (jj + 1) + 1, SITE_DQ_V))) break;
           tc_fence_after();
-          issue_s(jj + 2);
+          issue_dp(jj + 1);
+          mma_commit(&bars->dp_full);
+          mma_commit(&bars->kv_empty[(2 * (jj + 1) + 1) % C::NSLOT]);  // V_{jj+1}
         }
       }
       if (ok) {
@@ -768,13 +793,13 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     const float sl = p.scale_log2;
     bool ok = true;
     for (int jj = 0; jj < n_blocks && ok; ++jj) {
-      const int sb = jj & 1;
-      const uint32_t ts = sb ? C::T_S1 : C::T_S0;
       const int kb = (jb + jj) * 128 + w * C::COLS;  // first key of this group
-      if (!(ok = fa_wait_warp(&bars->s_full[sb], uint32_t(jj >> 1) & 1u, watch, SITE_DQ_S))) break;
+      if (!(ok = fa_wait_warp(&bars->s_full, uint32_t(jj) & 1u, watch, SITE_DQ_S))) break;
       tc_fence_after();
       float pv[C::COLS];
-      tmem_ld_cols(tmem + lane_addr + ts + w * C::COLS, pv);
+      tmem_ld_cols(tmem + lane_addr + C::T_S + w * C::COLS, pv);
+      tc_fence_before();
+      mbar_arrive(&bars->s_free);
       const int kbase = (jb + jj) * 128;
       const bool need_mask = !(kbase >= tile_lo_max && kbase + 127 <= tile_hi_min);
       if (has_alibi) {
@@ -799,19 +824,21 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       }
       if (!(ok = fa_wait_warp(&bars->dp_full, uint32_t(jj) & 1u, watch, SITE_DQ_DP))) break;
       tc_fence_after();
-      {
-        float dp[C::COLS];
-        tmem_ld_cols(tmem + lane_addr + C::T_DP + w * C::COLS, dp);
-        uint32_t pk[C::COLS / 2];
+      // per 16-key chunk: load dP, form dS, store it as fp16 pairs over the chunk's
+      // consumed dP columns (see the TMEM map)
 #pragma unroll
-        for (int e = 0; e < C::COLS / 2; ++e) {
+      for (int ch = 0; ch < C::COLS / 16; ++ch) {
+        float dp[16];
+        const uint32_t col = tmem + lane_addr + C::T_DP + w * C::COLS + 16 * ch;
+        tmem_ld_cols(col, dp);
+        uint32_t pk[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
           float s0, s1;
-          ds_pair(pv[2 * e], pv[2 * e + 1], dp[2 * e], dp[2 * e + 1], dval, dval, s0, s1);
+          ds_pair(pv[16 * ch + 2 * e], pv[16 * ch + 2 * e + 1], dp[2 * e], dp[2 * e + 1], dval, dval, s0, s1);
           pk[e] = pack_f16x2(s0, s1);
         }
-        // dS fp16 over the consumed S columns of this buffer (S is in registers)
-#pragma unroll
-        for (int c = 0; c < C::COLS / 16; ++c) tmem_st_x8(tmem + lane_addr + ts + w * C::COLS + 16 * c, pk + 8 * c);
+        tmem_st_x8(col, pk);
       }
       tmem_st_wait();
       tc_fence_before();

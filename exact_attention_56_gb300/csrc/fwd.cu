@@ -183,30 +183,33 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
     if (lane == 0 && n_blocks > 0) {
       constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
       constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);    // P from TMEM, V MN-major
-      const uint32_t q_base = smem_u32(smem + C::Q_OFF);
-      const uint32_t kv_base = smem_u32(smem + C::KV_OFF);
+      // Descriptors are built once; each k-step, Q tile and ring slot is a
+      // constant added to the start-address field, so issuing keeps pace with
+      // the tensor pipe.
+      const uint64_t q_desc = sdesc_sw128(smem_u32(smem + C::Q_OFF), 16, 1024);
+      const uint64_t kv_kdesc = sdesc_sw128(smem_u32(smem + C::KV_OFF), 16, 1024);            // K-major (K)
+      const uint64_t kv_mdesc = sdesc_sw128(smem_u32(smem + C::KV_OFF), C::PANEL_BYTES, 1024);  // MN-major (V)
 
-      auto slot_of = [&](int it) { return it % C::NSLOT; };
+      auto slot_of = [](int it) { return it % C::NSLOT; };
       auto wait_full = [&](int it, uint32_t site) {
         return fa_wait(&bars->kv_full[slot_of(it)], uint32_t(it / C::NSLOT) & 1u, watch, site);
       };
-      auto issue_s = [&](int jj, int t, int sbuf) {
-        const uint32_t qa = q_base + t * C::TILE_BYTES;
-        const uint32_t ka = kv_base + slot_of(2 * jj) * C::TILE_BYTES;
+      auto issue_s = [=](int jj, int t, int sbuf) {
+        const uint64_t qd = sdesc_adv(q_desc, uint32_t(t) * C::TILE_BYTES);
+        const uint64_t kd = sdesc_adv(kv_kdesc, uint32_t(slot_of(2 * jj)) * C::TILE_BYTES);
+        const uint32_t ts = tmem + uint32_t(sbuf) * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
-          mma_ss(tmem + sbuf * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), IDESC_S,
-                 kk > 0 ? 1u : 0u);
+          mma_ss(ts, sdesc_adv(qd, off), sdesc_adv(kd, off), IDESC_S, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int jj, int t, int sbuf) {
-        const uint32_t va = kv_base + slot_of(2 * jj + 1) * C::TILE_BYTES;
+      auto issue_pv = [=](int jj, int t, int sbuf) {
+        const uint64_t vd = sdesc_adv(kv_mdesc, uint32_t(slot_of(2 * jj + 1)) * C::TILE_BYTES);
+        const uint32_t to = tmem + C::O_COL0 + uint32_t(t) * D, tp = tmem + uint32_t(sbuf) * 128;
+        const uint32_t acc0 = jj > 0 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          mma_ts(tmem + C::O_COL0 + t * D, tmem + sbuf * 128 + kk * 8,
-                 sdesc_sw128(va + kk * 2048, C::PANEL_BYTES, 1024), IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 8; ++kk) mma_ts(to, tp + kk * 8, sdesc_adv(vd, kk * 2048), IDESC_O, kk > 0 ? 1u : acc0);
       };
 
       bool ok = fa_wait(&bars->q_full, 0, watch, SITE_MMA_Q);

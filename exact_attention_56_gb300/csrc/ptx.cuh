@@ -204,6 +204,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Advances a shared-memory descriptor's start address by `bytes` (a multiple of
+// 16). The 14-bit field holds address >> 4 and cannot carry out for addresses
+// inside the 228 KB of shared memory, so this is a plain add; descriptors for
+// every k-step of a tile then cost one add each in the MMA issue loop.
+__device__ __forceinline__ uint64_t sdesc_adv(uint64_t d, uint32_t bytes) { return d + uint64_t(bytes >> 4); }
+
 // Register re-balancing between warpgroups (all warps of a warpgroup execute it).
 template <uint32_t N>
 __device__ __forceinline__ void regs_dec() {
