@@ -38,14 +38,14 @@ _SZ = ctypes.c_size_t
 _SIGS = {
     "fa_version": (_I, []),
     "fa_status_string": (ctypes.c_char_p, [_I]),
-    "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _I, _P]),
-    "fa_bwd_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
-    "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _I,
-                    _I, _P]),
-    "fa_decode_num_splits": (_I, [_I, _I, _I, _I, _I]),
-    "fa_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
-    "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _I, _I,
-                               _P]),
+    "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _I, _P]),
+    "fa_bwd_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P,
+                    _I, _I, _P]),
+    "fa_decode_num_splits": (_I, [_I, _I, _I, _I, _I, _I]),
+    "fa_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _I,
+                               _I, _P]),
     "fa_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
 }
 
@@ -125,15 +125,27 @@ def _alibi(alibi_slopes, B, H, device):
     raise ValueError(f"alibi_slopes must have shape ({H},) or ({B}, {H})")
 
 
+def _kv_heads(k, H):
+    """Key/value heads of a (B, Sk, Hk, D) tensor; H must be a multiple of Hk (query
+    head h reads key/value head h // (H // Hk))."""
+    if not isinstance(k, torch.Tensor) or k.dim() != 4:
+        raise ValueError("k must be a 4-D (B, Sk, Hk, D) tensor")
+    Hk = int(k.shape[2])
+    if Hk < 1 or H % Hk != 0:
+        raise ValueError(f"the query heads ({H}) must be a multiple of the key/value heads ({Hk})")
+    return Hk
+
+
 def fa_fwd(q, k, v, *, softmax_scale=None, causal=False, window_size=(-1, -1), alibi_slopes=None,
            out=None, lse=None, stream=None):
-    """O, L = attention(q, k, v). q (B,Sq,H,D), k/v (B,Sk,H,D) bf16 -> out (B,Sq,H,D) bf16, lse (B,H,Sq) fp32."""
+    """O, L = attention(q, k, v). q (B,Sq,H,D), k/v (B,Sk,Hk,D) bf16 -> out (B,Sq,H,D) bf16, lse (B,H,Sq) fp32."""
     _need(q, "q", torch.bfloat16)
     B, Sq, H, D = q.shape
     Sk = k.shape[1]
+    Hk = _kv_heads(k, H)
     dev = q.device
-    _need(k, "k", torch.bfloat16, (B, Sk, H, D), dev)
-    _need(v, "v", torch.bfloat16, (B, Sk, H, D), dev)
+    _need(k, "k", torch.bfloat16, (B, Sk, Hk, D), dev)
+    _need(v, "v", torch.bfloat16, (B, Sk, Hk, D), dev)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
@@ -141,76 +153,82 @@ def fa_fwd(q, k, v, *, softmax_scale=None, causal=False, window_size=(-1, -1), a
     _need(out, "out", torch.bfloat16, (B, Sq, H, D), dev)
     _need(lse, "lse", torch.float32, (B, H, Sq), dev)
     al, al_stride = _alibi(alibi_slopes, B, H, dev)
-    st = library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Sq, Sk, H, D,
+    st = library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Sq, Sk, H, Hk, D,
                           _scale(softmax_scale, D), int(bool(causal)), int(window_size[0]), int(window_size[1]),
                           _ptr(al), al_stride, _stream_ptr(stream, dev))
     _check("fa_fwd", st)
     return out, lse
 
 
-def fa_bwd_workspace_size(B, Sq, Sk, H, D, deterministic=False) -> int:
-    return int(library().fa_bwd_workspace_size(B, Sq, Sk, H, D, int(bool(deterministic))))
+def fa_bwd_workspace_size(B, Sq, Sk, H, D, deterministic=False, Hk=None) -> int:
+    Hk = H if Hk is None else Hk
+    return int(library().fa_bwd_workspace_size(B, Sq, Sk, H, Hk, D, int(bool(deterministic))))
 
 
 def fa_bwd(dout, q, k, v, out, lse, *, softmax_scale=None, causal=False, window_size=(-1, -1),
            alibi_slopes=None, deterministic=False, dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """dQ, dK, dV of <dout, attention(q, k, v)>; out and lse are fa_fwd's outputs for the same arguments."""
+    """dQ, dK, dV of <dout, attention(q, k, v)>; out and lse are fa_fwd's outputs for the same arguments.
+    With k/v of Hk < H heads, dk/dv (B,Sk,Hk,D) sum over the query heads sharing each key/value head."""
     _need(q, "q", torch.bfloat16)
     B, Sq, H, D = q.shape
     Sk = k.shape[1]
+    Hk = _kv_heads(k, H)
     dev = q.device
-    for name, t, shp in (("k", k, (B, Sk, H, D)), ("v", v, (B, Sk, H, D)), ("dout", dout, (B, Sq, H, D)),
+    for name, t, shp in (("k", k, (B, Sk, Hk, D)), ("v", v, (B, Sk, Hk, D)), ("dout", dout, (B, Sq, H, D)),
                          ("out", out, (B, Sq, H, D))):
         _need(t, name, torch.bfloat16, shp, dev)
     _need(lse, "lse", torch.float32, (B, H, Sq), dev)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    for name, t, shp in (("dq", dq, (B, Sq, H, D)), ("dk", dk, (B, Sk, H, D)), ("dv", dv, (B, Sk, H, D))):
+    for name, t, shp in (("dq", dq, (B, Sq, H, D)), ("dk", dk, (B, Sk, Hk, D)), ("dv", dv, (B, Sk, Hk, D))):
         _need(t, name, torch.bfloat16, shp, dev)
-    need = fa_bwd_workspace_size(B, Sq, Sk, H, D, deterministic)
+    need = fa_bwd_workspace_size(B, Sq, Sk, H, D, deterministic, Hk=Hk)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     _need(workspace, "workspace", torch.uint8, device=dev)
     al, al_stride = _alibi(alibi_slopes, B, H, dev)
     st = library().fa_bwd(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dq), _ptr(dk),
-                          _ptr(dv), _ptr(workspace), workspace.numel(), B, Sq, Sk, H, D,
+                          _ptr(dv), _ptr(workspace), workspace.numel(), B, Sq, Sk, H, Hk, D,
                           _scale(softmax_scale, D), int(bool(causal)), int(window_size[0]), int(window_size[1]),
                           _ptr(al), al_stride, int(bool(deterministic)), _stream_ptr(stream, dev))
     _check("fa_bwd", st)
     return dq, dk, dv
 
 
-def fa_decode_num_splits(B, Sq, Sk, H, D) -> int:
-    return int(library().fa_decode_num_splits(B, Sq, Sk, H, D))
+def fa_decode_num_splits(B, Sq, Sk, H, D, Hk=None) -> int:
+    Hk = H if Hk is None else Hk
+    return int(library().fa_decode_num_splits(B, Sq, Sk, H, Hk, D))
 
 
-def fa_decode_workspace_size(B, Sq, Sk, H, D, num_splits=0) -> int:
-    return int(library().fa_decode_workspace_size(B, Sq, Sk, H, D, int(num_splits)))
+def fa_decode_workspace_size(B, Sq, Sk, H, D, num_splits=0, Hk=None) -> int:
+    Hk = H if Hk is None else Hk
+    return int(library().fa_decode_workspace_size(B, Sq, Sk, H, Hk, D, int(num_splits)))
 
 
 def fa_decode_splitkv(q, k_cache, v_cache, *, softmax_scale=None, causal=False, window_size=(-1, -1),
                       alibi_slopes=None, num_splits=0, workspace=None, out=None, lse=None, stream=None):
-    """Split-KV decode: q (B,Sq<=16,H,D), caches (B,Sk,H,D) bf16 -> out (B,Sq,H,D) bf16, lse (B,H,Sq) fp32."""
+    """Split-KV decode: q (B,Sq<=16,H,D), caches (B,Sk,Hk,D) bf16 -> out (B,Sq,H,D) bf16, lse (B,H,Sq) fp32."""
     _need(q, "q", torch.bfloat16)
     B, Sq, H, D = q.shape
     Sk = k_cache.shape[1]
+    Hk = _kv_heads(k_cache, H)
     dev = q.device
-    _need(k_cache, "k_cache", torch.bfloat16, (B, Sk, H, D), dev)
-    _need(v_cache, "v_cache", torch.bfloat16, (B, Sk, H, D), dev)
+    _need(k_cache, "k_cache", torch.bfloat16, (B, Sk, Hk, D), dev)
+    _need(v_cache, "v_cache", torch.bfloat16, (B, Sk, Hk, D), dev)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, Sq), dtype=torch.float32, device=dev)
     _need(out, "out", torch.bfloat16, (B, Sq, H, D), dev)
     _need(lse, "lse", torch.float32, (B, H, Sq), dev)
-    need = fa_decode_workspace_size(B, Sq, Sk, H, D, num_splits)
+    need = fa_decode_workspace_size(B, Sq, Sk, H, D, num_splits, Hk=Hk)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     _need(workspace, "workspace", torch.uint8, device=dev)
     al, al_stride = _alibi(alibi_slopes, B, H, dev)
     st = library().fa_decode_splitkv(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse),
-                                     _ptr(workspace), workspace.numel(), B, Sq, Sk, H, D,
+                                     _ptr(workspace), workspace.numel(), B, Sq, Sk, H, Hk, D,
                                      _scale(softmax_scale, D), int(bool(causal)), int(window_size[0]),
                                      int(window_size[1]), _ptr(al), al_stride, int(num_splits),
                                      _stream_ptr(stream, dev))

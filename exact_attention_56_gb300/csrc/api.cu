@@ -82,9 +82,10 @@ using fa::AttnShape;
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Shared validation; fills `s`. D support is checked by the caller.
-static int check_common(int B, int Sq, int Sk, int H, int D, float scale, int causal, int wl, int wr,
+static int check_common(int B, int Sq, int Sk, int H, int Hk, int D, float scale, int causal, int wl, int wr,
                         const float* alibi, int alibi_bstride, AttnShape* s) {
   if (B < 1 || Sq < 1 || Sk < 1 || H < 1 || D < 1) return FA_ERR_INVALID;
+  if (Hk < 1 || H % Hk != 0) return FA_ERR_INVALID;
   if (wl < -1 || wr < -1) return FA_ERR_INVALID;
   if (alibi) {
     if (reinterpret_cast<uintptr_t>(alibi) & 3u) return FA_ERR_INVALID;
@@ -96,6 +97,7 @@ static int check_common(int B, int Sq, int Sk, int H, int D, float scale, int ca
   s->Sq = Sq;
   s->Sk = Sk;
   s->H = H;
+  s->Hk = Hk;
   s->D = D;
   s->scale = (scale > 0.0f && isfinite(scale)) ? scale : 1.0f / sqrtf(float(D));
   s->wl = wl;
@@ -128,71 +130,72 @@ const char* fa_status_string(int status) {
   }
 }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Sq, int Sk, int H, int D,
-           float scale, int causal, int window_left, int window_right, const float* alibi_slopes,
+int fa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Sq, int Sk, int H, int Hk,
+           int D, float scale, int causal, int window_left, int window_right, const float* alibi_slopes,
            int alibi_batch_stride, fa_stream_t stream) {
   if (!q || !k || !v || !out || !lse) return FA_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse)) return FA_ERR_INVALID;
   AttnShape s;
-  int st = check_common(B, Sq, Sk, H, D, scale, causal, window_left, window_right, alibi_slopes,
+  int st = check_common(B, Sq, Sk, H, Hk, D, scale, causal, window_left, window_right, alibi_slopes,
                         alibi_batch_stride, &s);
   if (st != FA_OK) return st;
   if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
   return fa::fwd_launch(s, q, k, v, out, lse, reinterpret_cast<cudaStream_t>(stream));
 }
 
-size_t fa_bwd_workspace_size(int B, int Sq, int Sk, int H, int D, int deterministic) {
-  if (B < 1 || Sq < 1 || Sk < 1 || H < 1 || (D != 64 && D != 128)) return 0;
-  return fa::bwd_workspace_bytes(B, Sq, Sk, H, D, deterministic);
+size_t fa_bwd_workspace_size(int B, int Sq, int Sk, int H, int Hk, int D, int deterministic) {
+  if (B < 1 || Sq < 1 || Sk < 1 || H < 1 || Hk < 1 || H % Hk != 0 || (D != 64 && D != 128)) return 0;
+  return fa::bwd_workspace_bytes(B, Sq, Sk, H, Hk, D, deterministic);
 }
 
 int fa_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,
            void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Sq, int Sk, int H,
-           int D, float scale, int causal, int window_left, int window_right, const float* alibi_slopes,
+           int Hk, int D, float scale, int causal, int window_left, int window_right, const float* alibi_slopes,
            int alibi_batch_stride, int deterministic, fa_stream_t stream) {
   if (!dout || !q || !k || !v || !out || !lse || !dq || !dk || !dv) return FA_ERR_INVALID;
   if (!aligned16(dout) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_INVALID;
   AttnShape s;
-  int st = check_common(B, Sq, Sk, H, D, scale, causal, window_left, window_right, alibi_slopes,
+  int st = check_common(B, Sq, Sk, H, Hk, D, scale, causal, window_left, window_right, alibi_slopes,
                         alibi_batch_stride, &s);
   if (st != FA_OK) return st;
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
-  const size_t need = fa::bwd_workspace_bytes(B, Sq, Sk, H, D, deterministic);
+  const size_t need = fa::bwd_workspace_bytes(B, Sq, Sk, H, Hk, D, deterministic);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
     return FA_ERR_WORKSPACE;
   return fa::bwd_launch(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, deterministic,
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
-int fa_decode_num_splits(int B, int Sq, int Sk, int H, int D) {
-  if (B < 1 || Sq < 1 || Sk < 1 || H < 1) return 1;
-  return fa::decode_auto_splits(B, Sq, Sk, H, D);
+int fa_decode_num_splits(int B, int Sq, int Sk, int H, int Hk, int D) {
+  if (B < 1 || Sq < 1 || Sk < 1 || H < 1 || Hk < 1 || H % Hk != 0) return 1;
+  return fa::decode_auto_splits(B, Sq, Sk, H, Hk, D);
 }
 
-size_t fa_decode_workspace_size(int B, int Sq, int Sk, int H, int D, int num_splits) {
+size_t fa_decode_workspace_size(int B, int Sq, int Sk, int H, int Hk, int D, int num_splits) {
   if (B < 1 || Sq < 1 || Sq > 16 || Sk < 1 || H < 1 || (D != 64 && D != 128 && D != 256)) return 0;
+  if (Hk < 1 || H % Hk != 0) return 0;
   if (num_splits < 0 || num_splits > 256) return 0;
-  const int n = num_splits == 0 ? fa::decode_auto_splits(B, Sq, Sk, H, D) : num_splits;
+  const int n = num_splits == 0 ? fa::decode_auto_splits(B, Sq, Sk, H, Hk, D) : num_splits;
   return fa::decode_workspace_bytes(B, Sq, H, D, n);
 }
 
 int fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, void* out, float* lse,
-                      void* workspace, size_t workspace_bytes, int B, int Sq, int Sk, int H, int D, float scale,
-                      int causal, int window_left, int window_right, const float* alibi_slopes,
+                      void* workspace, size_t workspace_bytes, int B, int Sq, int Sk, int H, int Hk, int D,
+                      float scale, int causal, int window_left, int window_right, const float* alibi_slopes,
                       int alibi_batch_stride, int num_splits, fa_stream_t stream) {
   if (!q || !k_cache || !v_cache || !out || !lse) return FA_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(lse))
     return FA_ERR_INVALID;
   AttnShape s;
-  int st = check_common(B, Sq, Sk, H, D, scale, causal, window_left, window_right, alibi_slopes,
+  int st = check_common(B, Sq, Sk, H, Hk, D, scale, causal, window_left, window_right, alibi_slopes,
                         alibi_batch_stride, &s);
   if (st != FA_OK) return st;
   if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
   if (Sq > 16) return FA_ERR_UNSUPPORTED;
   if (num_splits < 0 || num_splits > 256) return FA_ERR_INVALID;
-  const int n = num_splits == 0 ? fa::decode_auto_splits(B, Sq, Sk, H, D) : num_splits;
+  const int n = num_splits == 0 ? fa::decode_auto_splits(B, Sq, Sk, H, Hk, D) : num_splits;
   const size_t need = fa::decode_workspace_bytes(B, Sq, H, D, n);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
     return FA_ERR_WORKSPACE;

@@ -13,8 +13,9 @@
 //   fa_bwd_pre       D_i = rowsum(dO_i * O_i) and L2_i = L_i*log2(e), padded to
 //                    128-row tiles (+inf on padding and on rows without keys),
 //                    and fp16 copies of Q, K, V and dO.
-//   fa_bwd_dkdv      one CTA per (128-key tile, head, batch), looping over the
-//                    live 128-row query tiles:
+//   fa_bwd_dkdv      one CTA per (128-key tile, key/value head, batch), looping
+//                    over the live 128-row query tiles of every query head
+//                    that shares the key/value head:
 //                      S^T  = K Q^T                 -> TMEM S region   (tcgen05)
 //                      dP^T = V dO^T                -> TMEM dP region
 //                      P^T  = 2^(S^T*scale*log2e + bias - L2)
@@ -72,6 +73,7 @@ struct BwdParams {
   const float* alibi;
   int alibi_bstride;
   int B, Sq, Sk, H, Sq_pad, n_qt;
+  int Hk, group;  // key/value heads; query heads per key/value head
   int wl, wr;
   float scale;
   float scale_log2;
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
   constexpr int CPR = D / 8;
   const long long n_q = (long long)p.B * p.Sq * p.H * CPR;
   const long long k0 = (n_q + 31) & ~31LL;
-  const long long n_k = (long long)p.B * p.Sk * p.H * CPR;
+  const long long n_k = (long long)p.B * p.Sk * p.Hk * CPR;
   const long long p0 = (k0 + n_k + 31) & ~31LL;
   const int pad_rows = p.Sq_pad - p.Sq;
   const long long n_pad = (long long)p.B * p.H * pad_rows;
@@ -265,11 +267,13 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
   const int warp = int(warp_id());
   const int lane = int(lane_id());
   const int kt = blockIdx.x;
-  const int h = blockIdx.y;
+  const int hk = blockIdx.y;  // key/value head; its query heads are hk*group .. hk*group + group - 1
   const int b = blockIdx.z;
   const int j0 = kt * 128;
 
-  // Live query tiles of this key tile: a contiguous range.
+  // Live query tiles of this key tile: a contiguous range, the same for every
+  // query head. Iteration ii covers query head hk*group + ii / n_qtl and query
+  // tile qt_first + ii % n_qtl, so the group's dK, dV sums stay in this CTA.
   int qt_first = p.n_qt, qt_last = -1;
   for (int qt = 0; qt < p.n_qt; ++qt) {
     if (qtile_meets(qt, kt, p)) {
@@ -277,7 +281,8 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
       qt_last = qt;
     }
   }
-  const int n_iter = qt_last >= qt_first ? qt_last - qt_first + 1 : 0;
+  const int n_qtl = qt_last >= qt_first ? qt_last - qt_first + 1 : 0;
+  const int n_iter = n_qtl * p.group;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
@@ -307,7 +312,6 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   const Watch watch{&bars->abort, p.status};
-  const size_t vec_base = (size_t(b) * p.H + h) * p.Sq_pad;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -318,25 +322,27 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
       tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(&bars->kv_full, 2 * C::TILE_BYTES);
       for (int pn = 0; pn < C::PANELS; ++pn) {
-        tma_load_4d(smem + C::K_OFF + pn * C::PANEL_BYTES, &tm_k, &bars->kv_full, pn * 64, h, j0, b);
-        tma_load_4d(smem + C::V_OFF + pn * C::PANEL_BYTES, &tm_v, &bars->kv_full, pn * 64, h, j0, b);
+        tma_load_4d(smem + C::K_OFF + pn * C::PANEL_BYTES, &tm_k, &bars->kv_full, pn * 64, hk, j0, b);
+        tma_load_4d(smem + C::V_OFF + pn * C::PANEL_BYTES, &tm_v, &bars->kv_full, pn * 64, hk, j0, b);
       }
       int q_issued = 0, do_issued = 0;
       for (int ii = 0; ii < n_iter; ++ii) {
         const int s = ii % C::NQ;
-        const int i0 = (qt_first + ii) * 128;
+        const int hq = hk * p.group + ii / n_qtl;
+        const int i0 = (qt_first + ii % n_qtl) * 128;
+        const size_t vec_base = (size_t(b) * p.H + hq) * p.Sq_pad;
         if (!fa_wait(&bars->q_empty[s], (uint32_t(ii / C::NQ) & 1u) ^ 1u, watch, SITE_KV_EMPTY)) break;
         mbar_arrive_expect_tx(&bars->q_full[s], C::TILE_BYTES);
         for (int pn = 0; pn < C::PANELS; ++pn)
           tma_load_4d(smem + C::Q_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bars->q_full[s], pn * 64,
-                      h, i0, b);
+                      hq, i0, b);
         q_issued = ii + 1;
         const int d = ii % C::NDO;
         if (!fa_wait(&bars->do_empty[d], (uint32_t(ii / C::NDO) & 1u) ^ 1u, watch, SITE_KV_DOEMPTY)) break;
         mbar_arrive_expect_tx(&bars->do_full[d], C::DO_TX);
         for (int pn = 0; pn < C::PANELS; ++pn)
           tma_load_4d(smem + C::DO_OFF + d * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_do, &bars->do_full[d],
-                      pn * 64, h, i0, b);
+                      pn * 64, hq, i0, b);
         bulk_load(smem + C::VEC_OFF + d * 1024, p.l2 + vec_base + i0, 512, &bars->do_full[d]);
         bulk_load(smem + C::VEC_OFF + d * 1024 + 512, p.dvec + vec_base + i0, 512, &bars->do_full[d]);
         do_issued = ii + 1;
@@ -465,12 +471,13 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
     qbounds(j0, dummy, qhi_min);
     const bool tile_keys_ok = j0 + 127 < p.Sk;
     const bool has_alibi = p.alibi != nullptr;
-    const float slope_log2 = has_alibi ? p.alibi[b * p.alibi_bstride + h] * 1.4426950408889634f : 0.0f;
     const float sl = p.scale_log2;
     bool ok = true;
     for (int ii = 0; ii < n_iter && ok; ++ii) {
       const int d = ii % C::NDO;
-      const int i0 = (qt_first + ii) * 128;
+      const int hq = hk * p.group + ii / n_qtl;
+      const int i0 = (qt_first + ii % n_qtl) * 128;
+      const float slope_log2 = has_alibi ? p.alibi[b * p.alibi_bstride + hq] * 1.4426950408889634f : 0.0f;
       const int ib = i0 + w * C::COLS;  // first query of this group
       const float4* l2v = reinterpret_cast<const float4*>(smem + C::VEC_OFF + d * 1024) + w * (C::COLS / 4);
       const float4* dvv = l2v + 32;
@@ -542,7 +549,7 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
     const bool is_dv = w < C::NCW / 2;
     const int col0 = (w % (C::NCW / 2)) * SLICE;
     const bool row_ok = j < p.Sk;
-    __nv_bfloat16* dst = (is_dv ? p.dv : p.dk) + ((size_t(b) * p.Sk + size_t(j)) * p.H + h) * size_t(D) + col0;
+    __nv_bfloat16* dst = (is_dv ? p.dv : p.dk) + ((size_t(b) * p.Sk + size_t(j)) * p.Hk + hk) * size_t(D) + col0;
     const float mul = is_dv ? 1.0f : p.scale;
     if (n_iter == 0) {
       if (row_ok)
@@ -625,6 +632,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
   // Query tiles with more live keys first (causal / right-bounded windows).
   const int qt = (p.wr >= 0) ? (n_qt - 1 - int(blockIdx.x)) : int(blockIdx.x);
   const int h = blockIdx.y;
+  const int hkv = h / p.group;  // key/value head of this query head
   const int b = blockIdx.z;
   const int row0 = qt * 128;
   const int last_row = min(p.Sq, row0 + 128) - 1;
@@ -684,7 +692,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
           const CUtensorMap* m = kv ? &tm_v : &tm_k;
           for (int pn = 0; pn < C::PANELS; ++pn)
             tma_load_4d(smem + C::KV_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, m, &bars->kv_full[s],
-                        pn * 64, h, (jb + jj) * 128, b);
+                        pn * 64, hkv, (jb + jj) * 128, b);
           issued = it + 1;
         }
       }
@@ -878,13 +886,13 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
 static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Workspace: L2 and D vectors (B, H, Sq_pad) fp32, then fp16 copies of Q, dO
-// (B, Sq, H, D) and K, V (B, Sk, H, D).
-size_t bwd_workspace_bytes(int B, int Sq, int Sk, int H, int D, int deterministic) {
+// (B, Sq, H, D) and K, V (B, Sk, Hk, D).
+size_t bwd_workspace_bytes(int B, int Sq, int Sk, int H, int Hk, int D, int deterministic) {
   (void)deterministic;  // every run is deterministic: no cross-CTA reductions
   const size_t sq_pad = size_t((Sq + 127) / 128) * 128;
   const size_t vec = al256(size_t(B) * H * sq_pad * 4);
   const size_t qside = al256(size_t(B) * Sq * H * D * 2);
-  const size_t kside = al256(size_t(B) * Sk * H * D * 2);
+  const size_t kside = al256(size_t(B) * Sk * Hk * D * 2);
   return 2 * vec + 2 * qside + 2 * kside;
 }
 
@@ -897,12 +905,14 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
   p.Sq = s.Sq;
   p.Sk = s.Sk;
   p.H = s.H;
+  p.Hk = s.Hk;
+  p.group = s.H / s.Hk;
   p.Sq_pad = ((s.Sq + 127) / 128) * 128;
   p.n_qt = p.Sq_pad / 128;
   uint8_t* w = static_cast<uint8_t*>(ws);
   const size_t vec = al256(size_t(s.B) * s.H * p.Sq_pad * 4);
   const size_t qside = al256(size_t(s.B) * s.Sq * s.H * D * 2);
-  const size_t kside = al256(size_t(s.B) * s.Sk * s.H * D * 2);
+  const size_t kside = al256(size_t(s.B) * s.Sk * s.Hk * D * 2);
   p.l2 = reinterpret_cast<float*>(w);
   p.dvec = reinterpret_cast<float*>(w + vec);
   p.q16 = reinterpret_cast<uint16_t*>(w + 2 * vec);
@@ -929,15 +939,15 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
   if (s.B > 65535 || s.H > 65535) return FA_ERR_UNSUPPORTED;
   CUtensorMap mq, mk, mv, mdo;
   if (!make_bshd_map(&mq, p.q16, s.B, s.Sq, s.H, D, 128, true) ||
-      !make_bshd_map(&mk, p.k16, s.B, s.Sk, s.H, D, 128, true) ||
-      !make_bshd_map(&mv, p.v16, s.B, s.Sk, s.H, D, 128, true) ||
+      !make_bshd_map(&mk, p.k16, s.B, s.Sk, s.Hk, D, 128, true) ||
+      !make_bshd_map(&mv, p.v16, s.B, s.Sk, s.Hk, D, 128, true) ||
       !make_bshd_map(&mdo, p.do16, s.B, s.Sq, s.H, D, 128, true))
     return FA_ERR_CUDA;
 
   {
     const long long cpr = D / 8;
     const long long n_q = ((long long)s.B * s.Sq * s.H * cpr + 31) & ~31LL;
-    const long long n_k = ((long long)s.B * s.Sk * s.H * cpr + 31) & ~31LL;
+    const long long n_k = ((long long)s.B * s.Sk * s.Hk * cpr + 31) & ~31LL;
     const long long total = n_q + n_k + (long long)s.B * s.H * (p.Sq_pad - s.Sq);
     const long long cap = (long long)device_sm_count() * 8;  // 8 blocks of 256 threads per SM
     const int grid = int(std::max(1LL, std::min(cap, (total + 255) / 256)));
@@ -947,7 +957,7 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
   auto kv = fa_bwd_dkdv_kernel<D>;
   if (cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, KvCfg<D>::SMEM_BYTES) != cudaSuccess)
     return FA_ERR_CUDA;
-  kv<<<dim3((s.Sk + 127) / 128, s.H, s.B), KvCfg<D>::THREADS, KvCfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
+  kv<<<dim3((s.Sk + 127) / 128, s.Hk, s.B), KvCfg<D>::THREADS, KvCfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   auto dqk = fa_bwd_dq_kernel<D>;
   if (cudaFuncSetAttribute(dqk, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::SMEM_BYTES) != cudaSuccess)

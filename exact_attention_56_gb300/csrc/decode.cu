@@ -54,6 +54,7 @@ struct DecParams {
   const float* alibi;
   int alibi_bstride;
   int B, Sq, Sk, H, n_splits;
+  int group;  // query heads per key/value head (H / Hk)
   int wl, wr;
   float scale_log2;
   unsigned int* status;
@@ -132,8 +133,8 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS)
         const int row = ks + t * C::TK;
 #pragma unroll
         for (int pn = 0; pn < C::PANELS; ++pn) {
-          tma_load_4d(st + pn * C::PANEL_BYTES, &tm_k, &bars->full[s], pn * 64, h, row, b);
-          tma_load_4d(st + C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_v, &bars->full[s], pn * 64, h, row, b);
+          tma_load_4d(st + pn * C::PANEL_BYTES, &tm_k, &bars->full[s], pn * 64, h / p.group, row, b);
+          tma_load_4d(st + C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_v, &bars->full[s], pn * 64, h / p.group, row, b);
         }
         issued = t + 1;
       }
@@ -316,7 +317,8 @@ size_t decode_workspace_bytes(int B, int Sq, int H, int D, int n) {
   return align256(units * D * 4) + align256(units * 4);
 }
 
-int decode_auto_splits(int B, int Sq, int Sk, int H, int D) {
+int decode_auto_splits(int B, int Sq, int Sk, int H, int Hk, int D) {
+  (void)Hk;  // one split CTA per query head and row
   const int tk = (D == 64) ? 128 : (D == 128 ? 64 : 32);
   const long long slots = 2LL * device_sm_count();  // two split CTAs fit per SM
   const long long units = (long long)B * Sq * H;
@@ -343,7 +345,7 @@ static int launch_decode_t(const AttnShape& s, const void* q, const void* k, con
                            void* ws, int n, cudaStream_t stream) {
   using C = DecCfg<D>;
   CUtensorMap mk, mv;
-  if (!make_bshd_map(&mk, k, s.B, s.Sk, s.H, D, C::TK) || !make_bshd_map(&mv, v, s.B, s.Sk, s.H, D, C::TK))
+  if (!make_bshd_map(&mk, k, s.B, s.Sk, s.Hk, D, C::TK) || !make_bshd_map(&mv, v, s.B, s.Sk, s.Hk, D, C::TK))
     return FA_ERR_CUDA;
   auto kern = fa_decode_split_kernel<D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
@@ -359,6 +361,7 @@ static int launch_decode_t(const AttnShape& s, const void* q, const void* k, con
   p.Sq = s.Sq;
   p.Sk = s.Sk;
   p.H = s.H;
+  p.group = s.H / s.Hk;
   p.n_splits = n;
   p.wl = s.wl;
   p.wr = s.wr;

@@ -58,13 +58,14 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 }  // namespace
 
 extern "C" int fa_decode_splitkv_noalloc(const void* q, const void* k_cache, const void* v_cache, void* out,
-                                         float* lse, int B, int Sq, int Sk, int H, int D, float scale, int causal,
-                                         int window_left, int window_right, const float* alibi_slopes,
+                                         float* lse, int B, int Sq, int Sk, int H, int Hk, int D, float scale,
+                                         int causal, int window_left, int window_right, const float* alibi_slopes,
                                          int alibi_batch_stride, int num_splits, fa_stream_t stream) {
   if (!q || !k_cache || !v_cache || !out || !lse) return FA_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(lse))
     return FA_ERR_INVALID;
   if (B < 1 || Sq < 1 || Sk < 1 || H < 1 || D < 1) return FA_ERR_INVALID;
+  if (Hk < 1 || H % Hk != 0) return FA_ERR_INVALID;
   if (window_left < -1 || window_right < -1) return FA_ERR_INVALID;
   if (alibi_slopes) {
     if (reinterpret_cast<uintptr_t>(alibi_slopes) & 3u) return FA_ERR_INVALID;
@@ -73,7 +74,7 @@ extern "C" int fa_decode_splitkv_noalloc(const void* q, const void* k_cache, con
   if (Sq > 16 || Sk > (1 << 30)) return FA_ERR_UNSUPPORTED;
   if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
   if (num_splits < 0 || num_splits > 256) return FA_ERR_INVALID;
-  const int n = num_splits == 0 ? fa::decode_auto_splits(B, Sq, Sk, H, D) : num_splits;
+  const int n = num_splits == 0 ? fa::decode_auto_splits(B, Sq, Sk, H, Hk, D) : num_splits;
   if (fa::decode_workspace_bytes(B, Sq, H, D, n) > kScratchBytes) return FA_ERR_WORKSPACE;
   void* ws = scratch_address();
   if (!ws) return FA_ERR_CUDA;
@@ -82,6 +83,7 @@ extern "C" int fa_decode_splitkv_noalloc(const void* q, const void* k_cache, con
   s.Sq = Sq;
   s.Sk = Sk;
   s.H = H;
+  s.Hk = Hk;
   s.D = D;
   s.scale = (scale > 0.0f && isfinite(scale)) ? scale : 1.0f / sqrtf(float(D));
   s.wl = window_left;

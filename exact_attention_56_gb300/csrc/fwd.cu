@@ -35,6 +35,7 @@ struct FwdParams {
   const float* alibi;
   int alibi_bstride;
   int B, Sq, Sk, H;
+  int group;         // query heads per key/value head (H / Hk)
   int wl, wr;
   float scale_log2;  // softmax scale * log2(e)
   unsigned int* status;
@@ -106,6 +107,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
   // Groups with more live keys first (causal / right-bounded windows).
   const int qg = (p.wr >= 0) ? (n_groups - 1 - int(blockIdx.x)) : int(blockIdx.x);
   const int h = blockIdx.y;
+  const int hkv = h / p.group;  // key/value head of this query head
   const int b = blockIdx.z;
   const int row0 = qg * NT * 128;
   const int last_row = min(p.Sq, row0 + NT * 128) - 1;
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
           const CUtensorMap* m = kv ? &tm_v : &tm_k;
           for (int pn = 0; pn < C::PANELS; ++pn)
             tma_load_4d(smem + C::KV_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, m, &bars->kv_full[s],
-                        pn * 64, h, (jb + jj) * 128, b);
+                        pn * 64, hkv, (jb + jj) * 128, b);
           issued = it + 1;
         }
       }
@@ -436,6 +438,7 @@ static int launch_fwd_t(const AttnShape& s, const CUtensorMap& mq, const CUtenso
   p.Sq = s.Sq;
   p.Sk = s.Sk;
   p.H = s.H;
+  p.group = s.H / s.Hk;
   p.wl = s.wl;
   p.wr = s.wr;
   p.scale_log2 = s.scale * 1.4426950408889634f;
@@ -450,8 +453,8 @@ int fwd_launch(const AttnShape& s, const void* q, const void* k, const void* v, 
                cudaStream_t stream) {
   if (s.B > 65535 || s.H > 65535) return FA_ERR_UNSUPPORTED;
   CUtensorMap mq, mk, mv;
-  if (!make_bshd_map(&mq, q, s.B, s.Sq, s.H, s.D, 128) || !make_bshd_map(&mk, k, s.B, s.Sk, s.H, s.D, 128) ||
-      !make_bshd_map(&mv, v, s.B, s.Sk, s.H, s.D, 128))
+  if (!make_bshd_map(&mq, q, s.B, s.Sq, s.H, s.D, 128) || !make_bshd_map(&mk, k, s.B, s.Sk, s.Hk, s.D, 128) ||
+      !make_bshd_map(&mv, v, s.B, s.Sk, s.Hk, s.D, 128))
     return FA_ERR_CUDA;
   switch (s.D) {
     case 64:

@@ -10,6 +10,7 @@ namespace fa {
 // Arguments common to every attention entry point, after validation.
 struct AttnShape {
   int B, Sq, Sk, H, D;
+  int Hk;             // key/value heads; H is a multiple of Hk, query head h reads kv head h / (H / Hk)
   float scale;        // softmax scale (already defaulted)
   int wl, wr;         // window, causal folded into wr (= 0); -1 unbounded
   const float* alibi; // NULL or fp32 slopes
@@ -33,10 +34,10 @@ int fwd_launch(const AttnShape& s, const void* q, const void* k, const void* v, 
 int decode_launch(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,
                   void* workspace, int num_splits, cudaStream_t stream);
 size_t decode_workspace_bytes(int B, int Sq, int H, int D, int num_splits);
-int decode_auto_splits(int B, int Sq, int Sk, int H, int D);
+int decode_auto_splits(int B, int Sq, int Sk, int H, int Hk, int D);
 int bwd_launch(const AttnShape& s, const void* dout, const void* q, const void* k, const void* v,
                const void* out, const float* lse, void* dq, void* dk, void* dv, void* workspace,
                int deterministic, cudaStream_t stream);
-size_t bwd_workspace_bytes(int B, int Sq, int Sk, int H, int D, int deterministic);
+size_t bwd_workspace_bytes(int B, int Sq, int Sk, int H, int Hk, int D, int deterministic);
 
 }  // namespace fa

@@ -14,8 +14,14 @@
  *   16-byte aligned. The library never allocates, frees or keeps a pointer
  *   after the call returns.
  * - Layouts: q, out, dout, dq: (B, Sq, H, D) bf16; k, v, dk, dv, k_cache,
- *   v_cache: (B, Sk, H, D) bf16; lse: (B, H, Sq) fp32, natural-log row
+ *   v_cache: (B, Sk, Hk, D) bf16; lse: (B, H, Sq) fp32, natural-log row
  *   logsumexp of the masked, scaled scores.
+ * - Hk is the number of key/value heads, 1 <= Hk, H a multiple of Hk. Query
+ *   head h attends key/value head h / (H / Hk): grouped-query attention,
+ *   Hk = 1 is multi-query and Hk = H plain multi-head. The page's
+ *   FlashCrossAttention takes kv of shape (B, Sk, 2, H_k, D) (section
+ *   "代码解读博客：FlashCrossAttention") without saying which query heads share
+ *   a key/value head; consecutive groups of H / Hk is the reading taken.
  * - D (head dim) is 64, 128 or 256 (backward: 64 or 128).
  * - scale <= 0 (or NaN) selects the default 1/sqrt(D) (section "参数说明").
  * - causal != 0 masks key j for query row i unless j <= i + Sk - Sq: the mask
@@ -74,22 +80,24 @@ const char* fa_status_string(int status);
  * Supported: D in {64, 128, 256}; any Sq, Sk >= 1.
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Sq, int Sk, int H,
-           int D, float scale, int causal, int window_left, int window_right, const float* alibi_slopes,
+           int Hk, int D, float scale, int causal, int window_left, int window_right, const float* alibi_slopes,
            int alibi_batch_stride, fa_stream_t stream);
 
 /*
  * Bytes of device workspace fa_bwd needs: the per-row D_i = rowsum(dO * O)
  * and L*log2(e) vectors, (B, H, Sq rounded up to 128) fp32 each, and fp16
- * copies of q, dout (B, Sq, H, D) and k, v (B, Sk, H, D), each section
+ * copies of q, dout (B, Sq, H, D) and k, v (B, Sk, Hk, D), each section
  * rounded up to 256 bytes. Returns 0 for arguments fa_bwd would reject.
  */
-size_t fa_bwd_workspace_size(int B, int Sq, int Sk, int H, int D, int deterministic);
+size_t fa_bwd_workspace_size(int B, int Sq, int Sk, int H, int Hk, int D, int deterministic);
 
 /*
  * Backward (section "反向传播": recompute P from the saved logsumexp L, no
  * stored attention matrix). Inputs: dout, q, k, v, out (bf16) and lse (fp32)
  * from fa_fwd with the same arguments. Writes dq (B,Sq,H,D), dk, dv
- * (B,Sk,H,D) bf16; they are overwritten, not accumulated.
+ * (B,Sk,Hk,D) bf16; they are overwritten, not accumulated. With Hk < H the
+ * dk and dv of a key/value head are the sums over the query heads sharing
+ * it, formed inside one thread block.
  * deterministic: accepted for the page's interface (section "2.4"). Every
  * run is bitwise reproducible in either mode, because no output element is
  * accumulated across thread blocks: one kernel per 128-key tile produces dK
@@ -103,17 +111,17 @@ size_t fa_bwd_workspace_size(int B, int Sq, int Sk, int H, int D, int determinis
  */
 int fa_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,
            void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Sq, int Sk, int H,
-           int D, float scale, int causal, int window_left, int window_right, const float* alibi_slopes,
+           int Hk, int D, float scale, int causal, int window_left, int window_right, const float* alibi_slopes,
            int alibi_batch_stride, int deterministic, fa_stream_t stream);
 
 /*
  * Split count fa_decode_splitkv uses when num_splits == 0: chosen from the
  * SM count of the current device so the split kernel fills whole waves.
  */
-int fa_decode_num_splits(int B, int Sq, int Sk, int H, int D);
+int fa_decode_num_splits(int B, int Sq, int Sk, int H, int Hk, int D);
 
 /* Bytes of workspace fa_decode_splitkv needs for `num_splits` (0 = auto). */
-size_t fa_decode_workspace_size(int B, int Sq, int Sk, int H, int D, int num_splits);
+size_t fa_decode_workspace_size(int B, int Sq, int Sk, int H, int Hk, int D, int num_splits);
 
 /*
  * Split-KV decode for short queries (section "2.2：针对推理进行优化": the
@@ -127,8 +135,8 @@ size_t fa_decode_workspace_size(int B, int Sq, int Sk, int H, int D, int num_spl
  * workspace: >= fa_decode_workspace_size() bytes, 256-byte aligned.
  */
 int fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, void* out, float* lse,
-                      void* workspace, size_t workspace_bytes, int B, int Sq, int Sk, int H, int D, float scale,
-                      int causal, int window_left, int window_right, const float* alibi_slopes,
+                      void* workspace, size_t workspace_bytes, int B, int Sq, int Sk, int H, int Hk, int D,
+                      float scale, int causal, int window_left, int window_right, const float* alibi_slopes,
                       int alibi_batch_stride, int num_splits, fa_stream_t stream);
 
 /*
@@ -149,9 +157,9 @@ int fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, v
  *   array has to start at zero: each call writes every partial it reads.
  */
 int fa_decode_splitkv_noalloc(const void* q, const void* k_cache, const void* v_cache, void* out, float* lse,
-                              int B, int Sq, int Sk, int H, int D, float scale, int causal, int window_left,
-                              int window_right, const float* alibi_slopes, int alibi_batch_stride, int num_splits,
-                              fa_stream_t stream);
+                              int B, int Sq, int Sk, int H, int Hk, int D, float scale, int causal,
+                              int window_left, int window_right, const float* alibi_slopes, int alibi_batch_stride,
+                              int num_splits, fa_stream_t stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device status word of

@@ -24,4 +24,5 @@ from .attention import (  # noqa: F401
     attention_fwd,
     attention_bwd,
     decode_splitkv,
+    kv_head,
 )

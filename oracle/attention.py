@@ -29,6 +29,11 @@ Definitions used (the page's notation where it has one):
 * Split-KV decode (section "2.2：针对推理进行优化"): each split computes
   attention over its key range; a separate step merges them. Merge used here
   is the exact logsumexp merge: L = log sum_s exp(L_s), O = sum_s exp(L_s - L) O_s.
+* Key/value heads (section "代码解读博客：FlashCrossAttention", kv of shape
+  (B, Sk, 2, H_k, D)): k and v may have Hk heads with H a multiple of Hk.
+  Reading taken here (the page gives no mapping): query head h attends
+  key/value head h // (H // Hk), consecutive groups. The gradient of a shared
+  key/value head is the sum of the gradients its query heads contribute.
 """
 from __future__ import annotations
 
@@ -210,39 +215,54 @@ def _default_scale(D, scale):
     return 1.0 / math.sqrt(D) if (scale is None or scale <= 0) else float(scale)
 
 
+def kv_head(h: int, H: int, Hk: int) -> int:
+    """Key/value head read by query head h when k/v have Hk heads (H a multiple of Hk)."""
+    if Hk < 1 or H % Hk != 0:
+        raise ValueError(f"query heads {H} are not a multiple of key/value heads {Hk}")
+    return h // (H // Hk)
+
+
 def attention_fwd(q, k, v, scale=None, causal=False, window=(-1, -1), alibi_slopes=None):
-    """Batched forward: q (B,Sq,H,D), k/v (B,Sk,H,D) -> O (B,Sq,H,D), L (B,H,Sq), all fp64."""
+    """Batched forward: q (B,Sq,H,D), k/v (B,Sk,Hk,D) -> O (B,Sq,H,D), L (B,H,Sq), all fp64."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     B, Sq, H, D = q.shape
+    Hk = k.shape[2]
     sc = _default_scale(D, scale)
     o = np.zeros_like(q)
     lse = np.zeros((B, H, Sq))
     for b in range(B):
         for h in range(H):
+            g = kv_head(h, H, Hk)
             o[b, :, h, :], lse[b, h] = head_fwd(
-                q[b, :, h, :], k[b, :, h, :], v[b, :, h, :], sc, causal, window[0],
+                q[b, :, h, :], k[b, :, g, :], v[b, :, g, :], sc, causal, window[0],
                 window[1], _slope_for(alibi_slopes, b, h))
     return o, lse
 
 
 def attention_bwd(dout, q, k, v, scale=None, causal=False, window=(-1, -1), alibi_slopes=None):
-    """Batched backward: returns dQ, dK, dV in the layouts of q, k, v (fp64)."""
+    """Batched backward: returns dQ, dK, dV in the layouts of q, k, v (fp64). With k/v of
+    Hk < H heads, dK and dV of a key/value head sum the contributions of its query heads."""
     dout = np.asarray(dout, dtype=np.float64)
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     B, Sq, H, D = q.shape
+    Hk = k.shape[2]
     sc = _default_scale(D, scale)
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
     for b in range(B):
         for h in range(H):
-            dq[b, :, h, :], dk[b, :, h, :], dv[b, :, h, :] = head_bwd(
-                dout[b, :, h, :], q[b, :, h, :], k[b, :, h, :], v[b, :, h, :], sc, causal,
+            g = kv_head(h, H, Hk)
+            dqh, dkh, dvh = head_bwd(
+                dout[b, :, h, :], q[b, :, h, :], k[b, :, g, :], v[b, :, g, :], sc, causal,
                 window[0], window[1], _slope_for(alibi_slopes, b, h))
+            dq[b, :, h, :] = dqh
+            dk[b, :, g, :] += dkh
+            dv[b, :, g, :] += dvh
     return dq, dk, dv
 
 
@@ -257,15 +277,16 @@ def decode_splitkv(q, k, v, num_splits, scale=None, causal=False, window=(-1, -1
     """
     q = np.asarray(q, dtype=np.float64)
     B, Sq, H, D = q.shape
-    Sk = k.shape[1]
+    Sk, Hk = k.shape[1], k.shape[2]
     sc = _default_scale(D, scale)
     bounds = [(Sk * s) // num_splits for s in range(num_splits + 1)]
     o = np.zeros_like(q)
     lse = np.zeros((B, H, Sq))
     for b in range(B):
         for h in range(H):
-            kh = np.asarray(k[b, :, h, :], dtype=np.float64)
-            vh = np.asarray(v[b, :, h, :], dtype=np.float64)
+            g = kv_head(h, H, Hk)
+            kh = np.asarray(k[b, :, g, :], dtype=np.float64)
+            vh = np.asarray(v[b, :, g, :], dtype=np.float64)
             parts = [head_partial(q[b, :, h, :], kh, vh, bounds[s], bounds[s + 1], sc, causal,
                                   window[0], window[1], _slope_for(alibi_slopes, b, h))
                      for s in range(num_splits)]

@@ -43,12 +43,13 @@ def test_version_and_strings(lib):
 
 
 def _fwd(lib, **kw):
-    a = dict(q=16, k=16, v=16, out=16, lse=16, B=1, Sq=8, Sk=8, H=1, D=64, scale=0.0, causal=0, wl=-1, wr=-1,
-             alibi=None, ab=0)
+    a = dict(q=16, k=16, v=16, out=16, lse=16, B=1, Sq=8, Sk=8, H=1, Hk=None, D=64, scale=0.0, causal=0, wl=-1,
+             wr=-1, alibi=None, ab=0)
     a.update(kw)
+    Hk = a["H"] if a["Hk"] is None else a["Hk"]
     P = ctypes.c_void_p
     return lib.fa_fwd(P(a["q"]), P(a["k"]), P(a["v"]), P(a["out"]), P(a["lse"]), a["B"], a["Sq"], a["Sk"], a["H"],
-                      a["D"], ctypes.c_float(a["scale"]), a["causal"], a["wl"], a["wr"], P(a["alibi"]), a["ab"],
+                      Hk, a["D"], ctypes.c_float(a["scale"]), a["causal"], a["wl"], a["wr"], P(a["alibi"]), a["ab"],
                       P(None))
 
 
@@ -61,6 +62,10 @@ def test_argument_checks_without_gpu(lib):
     assert _fwd(lib, wl=-2) == fa.FA_ERR_INVALID
     assert _fwd(lib, alibi=16, ab=3, H=2) == fa.FA_ERR_INVALID
     assert _fwd(lib, D=96) == fa.FA_ERR_UNSUPPORTED
+    # key/value heads: H must be a positive multiple of Hk
+    assert _fwd(lib, H=4, Hk=0) == fa.FA_ERR_INVALID
+    assert _fwd(lib, H=4, Hk=3) == fa.FA_ERR_INVALID
+    assert _fwd(lib, H=4, Hk=8) == fa.FA_ERR_INVALID
 
 
 def test_workspace_sizes(lib):
@@ -69,8 +74,11 @@ def test_workspace_sizes(lib):
     # two fp32 per-row vectors (L in log2 units and rowsum(dO*O)), rows padded to 128,
     # and fp16 copies of q, dout (B, Sq, H, D) and k, v (B, Sk, H, D)
     B, Sq, Sk, H, D = 1, 100, 128, 2, 64
-    assert lib.fa_bwd_workspace_size(B, Sq, Sk, H, D, 0) >= 2 * B * H * 128 * 4 + 2 * B * Sq * H * D * 2 + \
-        2 * B * Sk * H * D * 2
-    assert lib.fa_bwd_workspace_size(1, 128, 128, 2, 96, 0) == 0
-    assert lib.fa_decode_workspace_size(2, 1, 1000, 4, 128, 3) >= 2 * 4 * 3 * (128 + 1) * 4
-    assert lib.fa_decode_workspace_size(2, 17, 1000, 4, 128, 3) == 0
+    for Hk in (2, 1):  # the k/v copies have Hk heads
+        assert lib.fa_bwd_workspace_size(B, Sq, Sk, H, Hk, D, 0) >= 2 * B * H * 128 * 4 + \
+            2 * B * Sq * H * D * 2 + 2 * B * Sk * Hk * D * 2
+    assert lib.fa_bwd_workspace_size(1, 128, 128, 2, 2, 96, 0) == 0
+    assert lib.fa_bwd_workspace_size(1, 128, 128, 4, 3, 64, 0) == 0
+    assert lib.fa_decode_workspace_size(2, 1, 1000, 4, 4, 128, 3) >= 2 * 4 * 3 * (128 + 1) * 4
+    assert lib.fa_decode_workspace_size(2, 1, 1000, 4, 1, 128, 3) >= 2 * 4 * 3 * (128 + 1) * 4
+    assert lib.fa_decode_workspace_size(2, 17, 1000, 4, 4, 128, 3) == 0

@@ -27,7 +27,7 @@ def _noalloc_fn():
     fn = fa.library().fa_decode_splitkv_noalloc
     P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     fn.restype = I
-    fn.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, I, P, I, I, P]
+    fn.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, I, I, P, I, I, P]
     return fa, fn
 
 
@@ -35,9 +35,9 @@ def _call(fn, q, k, v, out, lse, n, causal=1):
     import torch
 
     B, Sq, H, D = q.shape
-    Sk = k.shape[1]
+    Sk, Hk = k.shape[1], k.shape[2]
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    return fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, Sq, Sk, H, D, 0.0,
+    return fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, Sq, Sk, H, Hk, D, 0.0,
               causal, -1, -1, None, 0, n, stream)
 
 
@@ -72,6 +72,6 @@ def test_noalloc_rejects_requests_beyond_its_array():
     out = torch.empty_like(q)
     lse = torch.empty((B, H, Sq), dtype=torch.float32, device="cuda")
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    rc = fn(q.data_ptr(), k.data_ptr(), k.data_ptr(), out.data_ptr(), lse.data_ptr(), B, Sq, Sk, H, D, 0.0, 1,
+    rc = fn(q.data_ptr(), k.data_ptr(), k.data_ptr(), out.data_ptr(), lse.data_ptr(), B, Sq, Sk, H, H, D, 0.0, 1,
             -1, -1, None, 0, 64, stream)
     assert rc == FA_ERR_WORKSPACE
