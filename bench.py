@@ -351,7 +351,7 @@ def run_ours(args):
     total_ms = _max_over_ranks(total_ms, ws, dev)
 
     # roofline of the dominant kernel group
-    groups = {"fa_bwd_main (fa_bwd launch group)": (sum(t_bwd), 2.5 * f_fwd, "tensor"),
+    groups = {"fa_bwd (pre + dK/dV + dQ launch group)": (sum(t_bwd), 2.5 * f_fwd, "tensor"),
               "fa_fwd_kernel": (sum(t_fwd), f_fwd, "tensor"),
               "fa_decode_split (+combine)": (sum(t_dec), dec_bytes, "hbm")}
     dom = max(groups, key=lambda g: groups[g][0])
@@ -477,6 +477,8 @@ PROFILE_CASES = {
     "bwd128": dict(op="bwd", B=4, S=4096, H=16, D=128, causal=False),
     "bwd64": dict(op="bwd", B=4, S=4096, H=32, D=64, causal=False),
     "decode": dict(op="decode", B=16, S=32768, H=32, D=128, causal=True),
+    # decode with a 1.07 GB cache: small enough for multi-pass captures
+    "decode4k": dict(op="decode", B=16, S=4096, H=32, D=128, causal=True),
 }
 
 

@@ -28,6 +28,8 @@ from ._native import (  # noqa: F401
     fa_decode_workspace_size,
     fa_decode_num_splits,
     fa_device_status,
+    fa_selftest_wait_timeout,
+    FA_SELFTEST_SITE,
 )
 
 __all__ = [
@@ -43,4 +45,5 @@ __all__ = [
     "fa_decode_workspace_size",
     "fa_decode_num_splits",
     "fa_device_status",
+    "fa_selftest_wait_timeout",
 ]

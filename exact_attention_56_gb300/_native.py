@@ -47,6 +47,7 @@ _SIGS = {
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _I,
                                _I, _P]),
     "fa_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
+    "fa_selftest_wait_timeout": (_I, [_P]),
 }
 
 
@@ -234,6 +235,15 @@ def fa_decode_splitkv(q, k_cache, v_cache, *, softmax_scale=None, causal=False, 
                                      _stream_ptr(stream, dev))
     _check("fa_decode_splitkv", st)
     return out, lse
+
+
+FA_SELFTEST_SITE = 0x7E
+
+
+def fa_selftest_wait_timeout(stream=None):
+    """Launch the diagnostic warp whose bounded wait runs out (about one second)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    _check("fa_selftest_wait_timeout", library().fa_selftest_wait_timeout(_stream_ptr(stream, dev)))
 
 
 def fa_device_status(stream=None):

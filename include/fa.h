@@ -169,6 +169,21 @@ int fa_decode_splitkv_noalloc(const void* q, const void* k_cache, const void* v_
  */
 int fa_device_status(fa_stream_t stream, unsigned int* detail);
 
+/* Wait-site code the self-test below records in the device status word. */
+#define FA_SELFTEST_SITE 0x7E
+
+/*
+ * Diagnostic, outside the method: launches one warp that waits, through the
+ * same bounded wait the attention kernels use, on a barrier that nothing
+ * arrives at. After about one second the wait gives up and records
+ * FA_ERR_TIMEOUT with site FA_SELFTEST_SITE in the device status word, so a
+ * following fa_device_status(stream, &d) returns FA_ERR_TIMEOUT with
+ * (d & 0xFFFF) == FA_SELFTEST_SITE, and the context stays usable. This lets a
+ * caller exercise the failure path on a real GPU without faulting it.
+ * Returns FA_OK, or FA_ERR_CUDA if the launch fails.
+ */
+int fa_selftest_wait_timeout(fa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
