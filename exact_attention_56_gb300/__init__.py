@@ -24,6 +24,9 @@ from ._native import (  # noqa: F401
     fa_fwd,
     fa_bwd,
     fa_bwd_workspace_size,
+    fa_fwd_varlen,
+    fa_bwd_varlen,
+    fa_bwd_varlen_workspace_size,
     fa_decode_splitkv,
     fa_decode_workspace_size,
     fa_decode_num_splits,
@@ -41,6 +44,9 @@ __all__ = [
     "fa_fwd",
     "fa_bwd",
     "fa_bwd_workspace_size",
+    "fa_fwd_varlen",
+    "fa_bwd_varlen",
+    "fa_bwd_varlen_workspace_size",
     "fa_decode_splitkv",
     "fa_decode_workspace_size",
     "fa_decode_num_splits",

@@ -40,6 +40,11 @@ _SIGS = {
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _I, _P]),
     "fa_bwd_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "fa_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _I,
+                           _P]),
+    "fa_bwd_varlen_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "fa_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F,
+                           _I, _I, _I, _P, _I, _I, _P]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P,
                     _I, _I, _P]),
     "fa_decode_num_splits": (_I, [_I, _I, _I, _I, _I, _I]),
@@ -194,6 +199,90 @@ def fa_bwd(dout, q, k, v, out, lse, *, softmax_scale=None, causal=False, window_
                           _scale(softmax_scale, D), int(bool(causal)), int(window_size[0]), int(window_size[1]),
                           _ptr(al), al_stride, int(bool(deterministic)), _stream_ptr(stream, dev))
     _check("fa_bwd", st)
+    return dq, dk, dv
+
+
+def _cu(t, name, B, total, dev):
+    _need(t, name, torch.int32, (B + 1,), dev)
+    return t
+
+
+def fa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, *, softmax_scale=None,
+                  causal=False, window_size=(-1, -1), alibi_slopes=None, out=None, lse=None, stream=None):
+    """Packed sequences: q (total_q,H,D), k/v (total_k,Hk,D) bf16, cu_seqlens int32 (B+1,) on the device;
+    max_seqlen_* at least the longest sequence. -> out (total_q,H,D) bf16, lse (H,total_q) fp32."""
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 3:
+        raise ValueError("q must be (total_q, H, D)")
+    total_q, H, D = q.shape
+    total_k = k.shape[0]
+    if k.dim() != 3:
+        raise ValueError("k must be (total_k, Hk, D)")
+    Hk = int(k.shape[1])
+    if Hk < 1 or H % Hk != 0:
+        raise ValueError(f"the query heads ({H}) must be a multiple of the key/value heads ({Hk})")
+    dev = q.device
+    B = int(cu_seqlens_q.numel()) - 1
+    _cu(cu_seqlens_q, "cu_seqlens_q", B, total_q, dev)
+    _cu(cu_seqlens_k, "cu_seqlens_k", B, total_k, dev)
+    _need(k, "k", torch.bfloat16, (total_k, Hk, D), dev)
+    _need(v, "v", torch.bfloat16, (total_k, Hk, D), dev)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((H, total_q), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, (total_q, H, D), dev)
+    _need(lse, "lse", torch.float32, (H, total_q), dev)
+    al, al_stride = _alibi(alibi_slopes, B, H, dev)
+    st = library().fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q),
+                                 _ptr(cu_seqlens_k), B, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), H,
+                                 Hk, D, _scale(softmax_scale, D), int(bool(causal)), int(window_size[0]),
+                                 int(window_size[1]), _ptr(al), al_stride, _stream_ptr(stream, dev))
+    _check("fa_fwd_varlen", st)
+    return out, lse
+
+
+def fa_bwd_varlen_workspace_size(B, total_q, total_k, max_seqlen_q, H, D, Hk=None) -> int:
+    Hk = H if Hk is None else Hk
+    return int(library().fa_bwd_varlen_workspace_size(B, total_q, total_k, max_seqlen_q, H, Hk, D))
+
+
+def fa_bwd_varlen(dout, q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, *,
+                  softmax_scale=None, causal=False, window_size=(-1, -1), alibi_slopes=None, deterministic=False,
+                  dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward of fa_fwd_varlen: dq (total_q,H,D), dk/dv (total_k,Hk,D) bf16."""
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 3 or k.dim() != 3:
+        raise ValueError("q must be (total_q, H, D) and k (total_k, Hk, D)")
+    total_q, H, D = q.shape
+    total_k, Hk = k.shape[0], int(k.shape[1])
+    if Hk < 1 or H % Hk != 0:
+        raise ValueError(f"the query heads ({H}) must be a multiple of the key/value heads ({Hk})")
+    dev = q.device
+    B = int(cu_seqlens_q.numel()) - 1
+    _cu(cu_seqlens_q, "cu_seqlens_q", B, total_q, dev)
+    _cu(cu_seqlens_k, "cu_seqlens_k", B, total_k, dev)
+    for name, t, shp in (("k", k, (total_k, Hk, D)), ("v", v, (total_k, Hk, D)), ("dout", dout, (total_q, H, D)),
+                         ("out", out, (total_q, H, D))):
+        _need(t, name, torch.bfloat16, shp, dev)
+    _need(lse, "lse", torch.float32, (H, total_q), dev)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t, shp in (("dq", dq, (total_q, H, D)), ("dk", dk, (total_k, Hk, D)), ("dv", dv, (total_k, Hk, D))):
+        _need(t, name, torch.bfloat16, shp, dev)
+    need = fa_bwd_varlen_workspace_size(B, total_q, total_k, int(max_seqlen_q), H, D, Hk=Hk)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, device=dev)
+    al, al_stride = _alibi(alibi_slopes, B, H, dev)
+    st = library().fa_bwd_varlen(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), _ptr(workspace), workspace.numel(), _ptr(cu_seqlens_q),
+                                 _ptr(cu_seqlens_k), B, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), H,
+                                 Hk, D, _scale(softmax_scale, D), int(bool(causal)), int(window_size[0]),
+                                 int(window_size[1]), _ptr(al), al_stride, int(bool(deterministic)),
+                                 _stream_ptr(stream, dev))
+    _check("fa_bwd_varlen", st)
     return dq, dk, dv
 
 

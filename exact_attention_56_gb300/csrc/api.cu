@@ -140,7 +140,26 @@ int fa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, i
                         alibi_batch_stride, &s);
   if (st != FA_OK) return st;
   if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
-  return fa::fwd_launch(s, q, k, v, out, lse, reinterpret_cast<cudaStream_t>(stream));
+  return fa::fwd_launch(s, q, k, v, out, lse, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* out, float* lse, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, int B, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                  int H, int Hk, int D, float scale, int causal, int window_left, int window_right,
+                  const float* alibi_slopes, int alibi_batch_stride, fa_stream_t stream) {
+  if (!q || !k || !v || !out || !lse || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse)) return FA_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
+    return FA_ERR_INVALID;
+  if (total_q < 1 || total_k < 1) return FA_ERR_INVALID;
+  AttnShape s;
+  int st = check_common(B, max_seqlen_q, max_seqlen_k, H, Hk, D, scale, causal, window_left, window_right,
+                        alibi_slopes, alibi_batch_stride, &s);
+  if (st != FA_OK) return st;
+  if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
+  if (total_q > (1 << 30) || total_k > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  const fa::VarlenArgs vl{cu_seqlens_q, cu_seqlens_k, total_q, total_k};
+  return fa::fwd_launch(s, q, k, v, out, lse, &vl, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t fa_bwd_workspace_size(int B, int Sq, int Sk, int H, int Hk, int D, int deterministic) {
@@ -164,7 +183,40 @@ int fa_bwd(const void* dout, const void* q, const void* k, const void* v, const 
   const size_t need = fa::bwd_workspace_bytes(B, Sq, Sk, H, Hk, D, deterministic);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
     return FA_ERR_WORKSPACE;
-  return fa::bwd_launch(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, deterministic,
+  return fa::bwd_launch(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, deterministic, nullptr,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t fa_bwd_varlen_workspace_size(int B, int total_q, int total_k, int max_seqlen_q, int H, int Hk, int D) {
+  if (B < 1 || total_q < 1 || total_k < 1 || max_seqlen_q < 1 || H < 1 || Hk < 1 || H % Hk != 0) return 0;
+  if (D != 64 && D != 128) return 0;
+  return fa::bwd_varlen_workspace_bytes(B, total_q, total_k, max_seqlen_q, H, Hk, D);
+}
+
+int fa_bwd_varlen(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,
+                  void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, int B, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                  int H, int Hk, int D, float scale, int causal, int window_left, int window_right,
+                  const float* alibi_slopes, int alibi_batch_stride, int deterministic, fa_stream_t stream) {
+  if (!dout || !q || !k || !v || !out || !lse || !dq || !dk || !dv || !cu_seqlens_q || !cu_seqlens_k)
+    return FA_ERR_INVALID;
+  if (!aligned16(dout) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
+    return FA_ERR_INVALID;
+  if (total_q < 1 || total_k < 1) return FA_ERR_INVALID;
+  AttnShape s;
+  int st = check_common(B, max_seqlen_q, max_seqlen_k, H, Hk, D, scale, causal, window_left, window_right,
+                        alibi_slopes, alibi_batch_stride, &s);
+  if (st != FA_OK) return st;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (total_q > (1 << 30) || total_k > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  const size_t need = fa::bwd_varlen_workspace_bytes(B, total_q, total_k, max_seqlen_q, H, Hk, D);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return FA_ERR_WORKSPACE;
+  const fa::VarlenArgs vl{cu_seqlens_q, cu_seqlens_k, total_q, total_k};
+  return fa::bwd_launch(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, deterministic, &vl,
                         reinterpret_cast<cudaStream_t>(stream));
 }
 

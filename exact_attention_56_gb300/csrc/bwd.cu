@@ -72,8 +72,14 @@ struct BwdParams {
   __nv_bfloat16* dv;
   const float* alibi;
   int alibi_bstride;
-  int B, Sq, Sk, H, Sq_pad, n_qt;
+  int B, Sq, Sk, H, Sq_pad, n_qt;  // with cu_q: Sq, Sk the longest sequences
   int Hk, group;  // key/value heads; query heads per key/value head
+  // Packed sequences: NULL for the padded layout, else device int32 (B + 1,)
+  // prefix sums into (total_q, H, D) / (total_k, Hk, D) tensors, lse (H, total_q).
+  // The L2 / D vectors stay padded per (b, h) to Sq_pad rows.
+  const int* cu_q;
+  const int* cu_k;
+  int total_q, total_k;
   int wl, wr;
   float scale;
   float scale_log2;
@@ -120,13 +126,23 @@ __device__ __forceinline__ void drain_wait_b(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// One sequence's lengths, first rows and TMA batch coordinate.
+struct SeqInfo {
+  int Sq, Sk, q_off, k_off, tb;
+};
+__device__ __forceinline__ SeqInfo seq_info(const BwdParams& p, int b) {
+  if (!p.cu_q) return SeqInfo{p.Sq, p.Sk, 0, 0, b};
+  const int q0 = p.cu_q[b], k0 = p.cu_k[b];
+  return SeqInfo{p.cu_q[b + 1] - q0, p.cu_k[b + 1] - k0, q0, k0, 0};
+}
+
 // Does query tile qt meet key tile kt (does the bounding interval of its rows'
 // live keys intersect the key tile)?
-__device__ __forceinline__ bool qtile_meets(int qt, int kt, const BwdParams& p) {
+__device__ __forceinline__ bool qtile_meets(int qt, int kt, const BwdParams& p, int Sq, int Sk) {
   const int r0 = qt * 128;
-  const int r1 = min(p.Sq, r0 + 128) - 1;
-  const int lo = live_range(r0, p.Sq, p.Sk, p.wl, p.wr).lo;
-  const int hi = live_range(r1, p.Sq, p.Sk, p.wl, p.wr).hi;
+  const int r1 = min(Sq, r0 + 128) - 1;
+  const int lo = live_range(r0, Sq, Sk, p.wl, p.wr).lo;
+  const int hi = live_range(r1, Sq, Sk, p.wl, p.wr).hi;
   if (hi < lo) return false;
   return !(hi < kt * 128 || lo > kt * 128 + 127);
 }
@@ -146,18 +162,20 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 u) {
 //   query rows: D_i = rowsum(dO_i o O_i), L2_i = L_i*log2(e) (+inf where L_i = -inf),
 //               fp16 copies of Q_i and dO_i;
 //   key rows:   fp16 copies of K_j and V_j;
-//   padding:    D = 0 and L2 = +inf on the rows padding Sq to whole 128-row tiles.
+//   padding:    D = 0 and L2 = +inf on the vector rows of each (b, h) past its
+//               sequence, up to the whole 128-row tiles of Sq_pad.
 // The three item ranges start on multiples of 32, so each warp works inside one
 // of them and the D/8 lanes of a query row are consecutive lanes of one warp.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
   constexpr int CPR = D / 8;
-  const long long n_q = (long long)p.B * p.Sq * p.H * CPR;
+  const long long rows_q = p.cu_q ? (long long)p.total_q : (long long)p.B * p.Sq;  // query tokens
+  const long long rows_k = p.cu_q ? (long long)p.total_k : (long long)p.B * p.Sk;
+  const long long n_q = rows_q * p.H * CPR;
   const long long k0 = (n_q + 31) & ~31LL;
-  const long long n_k = (long long)p.B * p.Sk * p.Hk * CPR;
+  const long long n_k = rows_k * p.Hk * CPR;
   const long long p0 = (k0 + n_k + 31) & ~31LL;
-  const int pad_rows = p.Sq_pad - p.Sq;
-  const long long n_pad = (long long)p.B * p.H * pad_rows;
+  const long long n_pad = (long long)p.B * p.H * p.Sq_pad;
   const long long total = p0 + n_pad;
   const int lane = int(threadIdx.x & 31);
   const long long stride = (long long)gridDim.x * blockDim.x;
@@ -184,14 +202,28 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
 #pragma unroll
       for (int off = CPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
       if (live && (i % CPR) == 0) {
-        const long long row = i / CPR;  // (b * Sq + s) * H + h
+        const long long row = i / CPR;  // token * H + h
         const int h = int(row % p.H);
-        const long long bs = row / p.H;
-        const int s = int(bs % p.Sq);
-        const int b = int(bs / p.Sq);
+        const long long tok = row / p.H;
+        int b, s;
+        size_t li;
+        if (p.cu_q) {  // the sequence holding this token: last b with cu_q[b] <= tok
+          int lo = 0, hi = p.B - 1;
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.cu_q[mid] <= tok) lo = mid; else hi = mid - 1;
+          }
+          b = lo;
+          s = int(tok - p.cu_q[b]);
+          li = size_t(h) * p.total_q + size_t(tok);
+        } else {
+          b = int(tok / p.Sq);
+          s = int(tok % p.Sq);
+          li = (size_t(b) * p.H + h) * p.Sq + s;
+        }
         const size_t vi = (size_t(b) * p.H + h) * p.Sq_pad + s;
         p.dvec[vi] = acc;
-        const float L = p.lse[(size_t(b) * p.H + h) * p.Sq + s];
+        const float L = p.lse[li];
         p.l2[vi] = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
       }
     } else if (wb < p0) {
@@ -204,9 +236,13 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
     } else {
       const long long t = i - p0;
       if (t < n_pad) {
-        const size_t vi = size_t(t / pad_rows) * p.Sq_pad + p.Sq + size_t(t % pad_rows);
-        p.dvec[vi] = 0.0f;
-        p.l2[vi] = INFINITY;
+        const int bh = int(t / p.Sq_pad), s = int(t % p.Sq_pad);
+        const int b = bh / p.H;
+        const int sq = p.cu_q ? p.cu_q[b + 1] - p.cu_q[b] : p.Sq;
+        if (s >= sq) {
+          p.dvec[t] = 0.0f;
+          p.l2[t] = INFINITY;
+        }
       }
     }
   }
@@ -270,13 +306,17 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
   const int hk = blockIdx.y;  // key/value head; its query heads are hk*group .. hk*group + group - 1
   const int b = blockIdx.z;
   const int j0 = kt * 128;
+  const SeqInfo sq_ = seq_info(p, b);
+  const int Sq = sq_.Sq, Sk = sq_.Sk;
+  if (j0 >= Sk) return;  // shorter than the longest key sequence: no keys here
+  const int n_qt = (Sq + 127) / 128;
 
   // Live query tiles of this key tile: a contiguous range, the same for every
   // query head. Iteration ii covers query head hk*group + ii / n_qtl and query
   // tile qt_first + ii % n_qtl, so the group's dK, dV sums stay in this CTA.
-  int qt_first = p.n_qt, qt_last = -1;
-  for (int qt = 0; qt < p.n_qt; ++qt) {
-    if (qtile_meets(qt, kt, p)) {
+  int qt_first = n_qt, qt_last = -1;
+  for (int qt = 0; qt < n_qt; ++qt) {
+    if (qtile_meets(qt, kt, p, Sq, Sk)) {
       qt_first = min(qt_first, qt);
       qt_last = qt;
     }
@@ -322,8 +362,10 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
       tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(&bars->kv_full, 2 * C::TILE_BYTES);
       for (int pn = 0; pn < C::PANELS; ++pn) {
-        tma_load_4d(smem + C::K_OFF + pn * C::PANEL_BYTES, &tm_k, &bars->kv_full, pn * 64, hk, j0, b);
-        tma_load_4d(smem + C::V_OFF + pn * C::PANEL_BYTES, &tm_v, &bars->kv_full, pn * 64, hk, j0, b);
+        tma_load_4d(smem + C::K_OFF + pn * C::PANEL_BYTES, &tm_k, &bars->kv_full, pn * 64, hk, sq_.k_off + j0,
+                    sq_.tb);
+        tma_load_4d(smem + C::V_OFF + pn * C::PANEL_BYTES, &tm_v, &bars->kv_full, pn * 64, hk, sq_.k_off + j0,
+                    sq_.tb);
       }
       int q_issued = 0, do_issued = 0;
       for (int ii = 0; ii < n_iter; ++ii) {
@@ -335,14 +377,14 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(&bars->q_full[s], C::TILE_BYTES);
         for (int pn = 0; pn < C::PANELS; ++pn)
           tma_load_4d(smem + C::Q_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bars->q_full[s], pn * 64,
-                      hq, i0, b);
+                      hq, sq_.q_off + i0, sq_.tb);
         q_issued = ii + 1;
         const int d = ii % C::NDO;
         if (!fa_wait(&bars->do_empty[d], (uint32_t(ii / C::NDO) & 1u) ^ 1u, watch, SITE_KV_DOEMPTY)) break;
         mbar_arrive_expect_tx(&bars->do_full[d], C::DO_TX);
         for (int pn = 0; pn < C::PANELS; ++pn)
           tma_load_4d(smem + C::DO_OFF + d * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_do, &bars->do_full[d],
-                      pn * 64, hq, i0, b);
+                      pn * 64, hq, sq_.q_off + i0, sq_.tb);
         bulk_load(smem + C::VEC_OFF + d * 1024, p.l2 + vec_base + i0, 512, &bars->do_full[d]);
         bulk_load(smem + C::VEC_OFF + d * 1024 + 512, p.dvec + vec_base + i0, 512, &bars->do_full[d]);
         do_issued = ii + 1;
@@ -452,14 +494,14 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
     const int r = wq * 32 + lane;
     const int j = j0 + r;
     const uint32_t lane_addr = uint32_t(wq * 32) << 16;
-    const int off = p.Sk - p.Sq;
+    const int off = Sk - Sq;
     // live queries of key j: i in [qlo, qhi]
     auto qbounds = [&](int jj, int& lo, int& hi) {
       lo = (p.wr >= 0) ? jj - off - p.wr : 0;
-      hi = (p.wl >= 0) ? jj - off + p.wl : p.Sq - 1;
+      hi = (p.wl >= 0) ? jj - off + p.wl : Sq - 1;
       lo = max(lo, 0);
-      hi = min(hi, p.Sq - 1);
-      if (jj >= p.Sk) {
+      hi = min(hi, Sq - 1);
+      if (jj >= Sk) {
         lo = 1;
         hi = 0;
       }
@@ -467,9 +509,9 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
     int qlo, qhi;
     qbounds(j, qlo, qhi);
     int qlo_max, dummy, qhi_min;
-    qbounds(min(p.Sk - 1, j0 + 127), qlo_max, dummy);
+    qbounds(min(Sk - 1, j0 + 127), qlo_max, dummy);
     qbounds(j0, dummy, qhi_min);
-    const bool tile_keys_ok = j0 + 127 < p.Sk;
+    const bool tile_keys_ok = j0 + 127 < Sk;
     const bool has_alibi = p.alibi != nullptr;
     const float sl = p.scale_log2;
     bool ok = true;
@@ -548,8 +590,11 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
     constexpr int SLICE = D / (C::NCW / 2);
     const bool is_dv = w < C::NCW / 2;
     const int col0 = (w % (C::NCW / 2)) * SLICE;
-    const bool row_ok = j < p.Sk;
-    __nv_bfloat16* dst = (is_dv ? p.dv : p.dk) + ((size_t(b) * p.Sk + size_t(j)) * p.Hk + hk) * size_t(D) + col0;
+    // read again rather than kept live across the loop
+    const SeqInfo e_sq = seq_info(p, b);
+    const bool row_ok = j < e_sq.Sk;
+    const size_t krow = p.cu_q ? size_t(e_sq.k_off) + j : size_t(b) * e_sq.Sk + j;
+    __nv_bfloat16* dst = (is_dv ? p.dv : p.dk) + (krow * p.Hk + hk) * size_t(D) + col0;
     const float mul = is_dv ? 1.0f : p.scale;
     if (n_iter == 0) {
       if (row_ok)
@@ -628,16 +673,19 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
   DqBars* bars = reinterpret_cast<DqBars*>(smem + C::BAR_OFF);
   const int warp = int(warp_id());
   const int lane = int(lane_id());
-  const int n_qt = p.n_qt;
-  // Query tiles with more live keys first (causal / right-bounded windows).
-  const int qt = (p.wr >= 0) ? (n_qt - 1 - int(blockIdx.x)) : int(blockIdx.x);
   const int h = blockIdx.y;
   const int hkv = h / p.group;  // key/value head of this query head
   const int b = blockIdx.z;
+  const SeqInfo sq_ = seq_info(p, b);
+  const int Sq = sq_.Sq, Sk = sq_.Sk;
+  const int n_qt = (Sq + 127) / 128;
+  if (int(blockIdx.x) >= n_qt) return;  // shorter than the longest query sequence: no rows here
+  // Query tiles with more live keys first (causal / right-bounded windows).
+  const int qt = (p.wr >= 0) ? (n_qt - 1 - int(blockIdx.x)) : int(blockIdx.x);
   const int row0 = qt * 128;
-  const int last_row = min(p.Sq, row0 + 128) - 1;
-  const int kv_lo = live_range(row0, p.Sq, p.Sk, p.wl, p.wr).lo;
-  const int kv_hi = live_range(last_row, p.Sq, p.Sk, p.wl, p.wr).hi;
+  const int last_row = min(Sq, row0 + 128) - 1;
+  const int kv_lo = live_range(row0, Sq, Sk, p.wl, p.wr).lo;
+  const int kv_hi = live_range(last_row, Sq, Sk, p.wl, p.wr).hi;
   const int jb = kv_lo / 128;
   const int n_blocks = (kv_hi >= kv_lo) ? (kv_hi / 128 + 1 - jb) : 0;
 
@@ -675,8 +723,10 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(&bars->q_full, 2 * C::TILE_BYTES);
       for (int pn = 0; pn < C::PANELS; ++pn) {
-        tma_load_4d(smem + C::Q_OFF + pn * C::PANEL_BYTES, &tm_q, &bars->q_full, pn * 64, h, row0, b);
-        tma_load_4d(smem + C::DO_OFF + pn * C::PANEL_BYTES, &tm_do, &bars->q_full, pn * 64, h, row0, b);
+        tma_load_4d(smem + C::Q_OFF + pn * C::PANEL_BYTES, &tm_q, &bars->q_full, pn * 64, h, sq_.q_off + row0,
+                    sq_.tb);
+        tma_load_4d(smem + C::DO_OFF + pn * C::PANEL_BYTES, &tm_do, &bars->q_full, pn * 64, h, sq_.q_off + row0,
+                    sq_.tb);
       }
       int issued = 0;
       bool ok = true;
@@ -692,7 +742,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
           const CUtensorMap* m = kv ? &tm_v : &tm_k;
           for (int pn = 0; pn < C::PANELS; ++pn)
             tma_load_4d(smem + C::KV_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, m, &bars->kv_full[s],
-                        pn * 64, hkv, (jb + jj) * 128, b);
+                        pn * 64, hkv, sq_.k_off + (jb + jj) * 128, sq_.tb);
           issued = it + 1;
         }
       }
@@ -789,15 +839,15 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     const int r = wq * 32 + lane;
     const int i = row0 + r;
     const uint32_t lane_addr = uint32_t(wq * 32) << 16;
-    const RowRange rr = live_range(i, p.Sq, p.Sk, p.wl, p.wr);
-    const int tile_lo_max = live_range(last_row, p.Sq, p.Sk, p.wl, p.wr).lo;
-    const int tile_hi_min = live_range(row0, p.Sq, p.Sk, p.wl, p.wr).hi;
+    const RowRange rr = live_range(i, Sq, Sk, p.wl, p.wr);
+    const int tile_lo_max = live_range(last_row, Sq, Sk, p.wl, p.wr).lo;
+    const int tile_hi_min = live_range(row0, Sq, Sk, p.wl, p.wr).hi;
     const size_t vi = (size_t(b) * p.H + h) * p.Sq_pad + i;  // i < Sq_pad always
     const float l2 = p.l2[vi];
     const float dval = p.dvec[vi];
     const bool has_alibi = p.alibi != nullptr;
     const float slope_log2 = has_alibi ? p.alibi[b * p.alibi_bstride + h] * 1.4426950408889634f : 0.0f;
-    const int c_i = i + p.Sk - p.Sq;
+    const int c_i = i + Sk - Sq;
     const float sl = p.scale_log2;
     bool ok = true;
     for (int jj = 0; jj < n_blocks && ok; ++jj) {
@@ -854,8 +904,9 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     }
     // ------------------------------------------------------------ dQ epilogue (each group D/NCW columns)
     constexpr int SLICE = D / C::NCW;  // 16 or 32
-    const bool row_ok = i < p.Sq;
-    __nv_bfloat16* dst = p.dq + ((size_t(b) * p.Sq + size_t(i)) * p.H + h) * size_t(D) + w * SLICE;
+    const bool row_ok = i < Sq;
+    const size_t qrow = p.cu_q ? size_t(sq_.q_off) + i : size_t(b) * Sq + i;
+    __nv_bfloat16* dst = p.dq + (qrow * p.H + h) * size_t(D) + w * SLICE;
     if (n_blocks == 0) {
       if (row_ok)
         for (int e = 0; e < SLICE / 8; ++e) reinterpret_cast<uint4*>(dst)[e] = make_uint4(0, 0, 0, 0);
@@ -885,21 +936,32 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
 
 static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Workspace: L2 and D vectors (B, H, Sq_pad) fp32, then fp16 copies of Q, dO
-// (B, Sq, H, D) and K, V (B, Sk, Hk, D).
+// Workspace: L2 and D vectors (B, H, Sq_pad) fp32 (Sq_pad: the longest query
+// sequence rounded up to 128 rows), then fp16 copies of Q, dO (rows_q tokens,
+// H heads) and K, V (rows_k tokens, Hk heads), each region 256-byte aligned.
+struct BwdWs {
+  size_t vec, qside, kside;
+  size_t total() const { return 2 * vec + 2 * qside + 2 * kside; }
+};
+static BwdWs bwd_ws(int B, int max_sq, long long rows_q, long long rows_k, int H, int Hk, int D) {
+  const size_t sq_pad = size_t((max_sq + 127) / 128) * 128;
+  return BwdWs{al256(size_t(B) * H * sq_pad * 4), al256(size_t(rows_q) * H * D * 2),
+               al256(size_t(rows_k) * Hk * D * 2)};
+}
+
 size_t bwd_workspace_bytes(int B, int Sq, int Sk, int H, int Hk, int D, int deterministic) {
   (void)deterministic;  // every run is deterministic: no cross-CTA reductions
-  const size_t sq_pad = size_t((Sq + 127) / 128) * 128;
-  const size_t vec = al256(size_t(B) * H * sq_pad * 4);
-  const size_t qside = al256(size_t(B) * Sq * H * D * 2);
-  const size_t kside = al256(size_t(B) * Sk * Hk * D * 2);
-  return 2 * vec + 2 * qside + 2 * kside;
+  return bwd_ws(B, Sq, (long long)B * Sq, (long long)B * Sk, H, Hk, D).total();
+}
+
+size_t bwd_varlen_workspace_bytes(int B, int total_q, int total_k, int max_sq, int H, int Hk, int D) {
+  return bwd_ws(B, max_sq, total_q, total_k, H, Hk, D).total();
 }
 
 template <int D>
 static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, const void* k, const void* v,
                         const void* out, const float* lse, void* dq, void* dk, void* dv, void* ws,
-                        cudaStream_t stream) {
+                        const VarlenArgs* vl, cudaStream_t stream) {
   BwdParams p;
   p.B = s.B;
   p.Sq = s.Sq;
@@ -909,16 +971,20 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
   p.group = s.H / s.Hk;
   p.Sq_pad = ((s.Sq + 127) / 128) * 128;
   p.n_qt = p.Sq_pad / 128;
+  p.cu_q = vl ? vl->cu_q : nullptr;
+  p.cu_k = vl ? vl->cu_k : nullptr;
+  p.total_q = vl ? vl->total_q : 0;
+  p.total_k = vl ? vl->total_k : 0;
+  const long long rows_q = vl ? vl->total_q : (long long)s.B * s.Sq;
+  const long long rows_k = vl ? vl->total_k : (long long)s.B * s.Sk;
+  const BwdWs L = bwd_ws(s.B, s.Sq, rows_q, rows_k, s.H, s.Hk, D);
   uint8_t* w = static_cast<uint8_t*>(ws);
-  const size_t vec = al256(size_t(s.B) * s.H * p.Sq_pad * 4);
-  const size_t qside = al256(size_t(s.B) * s.Sq * s.H * D * 2);
-  const size_t kside = al256(size_t(s.B) * s.Sk * s.Hk * D * 2);
   p.l2 = reinterpret_cast<float*>(w);
-  p.dvec = reinterpret_cast<float*>(w + vec);
-  p.q16 = reinterpret_cast<uint16_t*>(w + 2 * vec);
-  p.do16 = reinterpret_cast<uint16_t*>(w + 2 * vec + qside);
-  p.k16 = reinterpret_cast<uint16_t*>(w + 2 * vec + 2 * qside);
-  p.v16 = reinterpret_cast<uint16_t*>(w + 2 * vec + 2 * qside + kside);
+  p.dvec = reinterpret_cast<float*>(w + L.vec);
+  p.q16 = reinterpret_cast<uint16_t*>(w + 2 * L.vec);
+  p.do16 = reinterpret_cast<uint16_t*>(w + 2 * L.vec + L.qside);
+  p.k16 = reinterpret_cast<uint16_t*>(w + 2 * L.vec + 2 * L.qside);
+  p.v16 = reinterpret_cast<uint16_t*>(w + 2 * L.vec + 2 * L.qside + L.kside);
   p.dout = static_cast<const __nv_bfloat16*>(dout);
   p.out = static_cast<const __nv_bfloat16*>(out);
   p.q = static_cast<const __nv_bfloat16*>(q);
@@ -937,18 +1003,21 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
   p.status = device_status_word();
   if (!p.status) return FA_ERR_CUDA;
   if (s.B > 65535 || s.H > 65535) return FA_ERR_UNSUPPORTED;
+  // Packed sequences are one (1, total, H, D) tensor.
+  const int mb = vl ? 1 : s.B;
+  const int mq_rows = vl ? vl->total_q : s.Sq, mk_rows = vl ? vl->total_k : s.Sk;
   CUtensorMap mq, mk, mv, mdo;
-  if (!make_bshd_map(&mq, p.q16, s.B, s.Sq, s.H, D, 128, true) ||
-      !make_bshd_map(&mk, p.k16, s.B, s.Sk, s.Hk, D, 128, true) ||
-      !make_bshd_map(&mv, p.v16, s.B, s.Sk, s.Hk, D, 128, true) ||
-      !make_bshd_map(&mdo, p.do16, s.B, s.Sq, s.H, D, 128, true))
+  if (!make_bshd_map(&mq, p.q16, mb, mq_rows, s.H, D, 128, true) ||
+      !make_bshd_map(&mk, p.k16, mb, mk_rows, s.Hk, D, 128, true) ||
+      !make_bshd_map(&mv, p.v16, mb, mk_rows, s.Hk, D, 128, true) ||
+      !make_bshd_map(&mdo, p.do16, mb, mq_rows, s.H, D, 128, true))
     return FA_ERR_CUDA;
 
   {
     const long long cpr = D / 8;
-    const long long n_q = ((long long)s.B * s.Sq * s.H * cpr + 31) & ~31LL;
-    const long long n_k = ((long long)s.B * s.Sk * s.Hk * cpr + 31) & ~31LL;
-    const long long total = n_q + n_k + (long long)s.B * s.H * (p.Sq_pad - s.Sq);
+    const long long n_q = (rows_q * s.H * cpr + 31) & ~31LL;
+    const long long n_k = (rows_k * s.Hk * cpr + 31) & ~31LL;
+    const long long total = n_q + n_k + (long long)s.B * s.H * p.Sq_pad;
     const long long cap = (long long)device_sm_count() * 8;  // 8 blocks of 256 threads per SM
     const int grid = int(std::max(1LL, std::min(cap, (total + 255) / 256)));
     fa_bwd_pre_kernel<D><<<grid, 256, 0, stream>>>(p);
@@ -968,13 +1037,13 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
 
 int bwd_launch(const AttnShape& s, const void* dout, const void* q, const void* k, const void* v, const void* out,
                const float* lse, void* dq, void* dk, void* dv, void* workspace, int deterministic,
-               cudaStream_t stream) {
+               const VarlenArgs* varlen, cudaStream_t stream) {
   (void)deterministic;
   switch (s.D) {
     case 64:
-      return launch_bwd_t<64>(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, stream);
+      return launch_bwd_t<64>(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, varlen, stream);
     case 128:
-      return launch_bwd_t<128>(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, stream);
+      return launch_bwd_t<128>(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, varlen, stream);
     default:
       return FA_ERR_UNSUPPORTED;
   }

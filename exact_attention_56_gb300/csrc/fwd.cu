@@ -34,8 +34,15 @@ struct FwdParams {
   float* lse;
   const float* alibi;
   int alibi_bstride;
-  int B, Sq, Sk, H;
-  int group;         // query heads per key/value head (H / Hk)
+  int B, Sq, Sk, H;   // Sq, Sk: padded layout; with cu_q the longest sequences
+  int group;          // query heads per key/value head (H / Hk)
+  // Packed sequences (page section "代码解读博客：FlashSelfAttention": cu_seqlens):
+  // NULL for the padded (B, S, H, D) layout; else device int32 (B + 1,) prefix
+  // sums, q/out rows cu_q[b] .. cu_q[b+1]-1 of a (total_q, H, D) tensor and lse
+  // (H, total_q).
+  const int* cu_q;
+  const int* cu_k;
+  int total_q;
   int wl, wr;
   float scale_log2;  // softmax scale * log2(e)
   unsigned int* status;
@@ -90,7 +97,9 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <int D, int NT>
+// VARLEN: packed sequences (cu_q, cu_k set); a separate instance, so the padded
+// layout keeps its lengths in kernel parameters rather than registers.
+template <int D, int NT, bool VARLEN>
 __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -103,17 +112,27 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
   const int warp = int(warp_id());
   const int lane = int(lane_id());
 
-  const int n_groups = (p.Sq + NT * 128 - 1) / (NT * 128);
-  // Groups with more live keys first (causal / right-bounded windows).
-  const int qg = (p.wr >= 0) ? (n_groups - 1 - int(blockIdx.x)) : int(blockIdx.x);
   const int h = blockIdx.y;
   const int hkv = h / p.group;  // key/value head of this query head
   const int b = blockIdx.z;
+  // This sequence's lengths and first rows; tb is the TMA batch coordinate.
+  int Sq = p.Sq, Sk = p.Sk, q_off = 0, k_off = 0, tb = b;
+  if (VARLEN) {
+    q_off = p.cu_q[b];
+    Sq = p.cu_q[b + 1] - q_off;
+    k_off = p.cu_k[b];
+    Sk = p.cu_k[b + 1] - k_off;
+    tb = 0;
+  }
+  const int n_groups = (Sq + NT * 128 - 1) / (NT * 128);
+  if (int(blockIdx.x) >= n_groups) return;  // shorter than the longest sequence: no rows here
+  // Groups with more live keys first (causal / right-bounded windows).
+  const int qg = (p.wr >= 0) ? (n_groups - 1 - int(blockIdx.x)) : int(blockIdx.x);
   const int row0 = qg * NT * 128;
-  const int last_row = min(p.Sq, row0 + NT * 128) - 1;
+  const int last_row = min(Sq, row0 + NT * 128) - 1;
 
-  const RowRange first_rr = live_range(row0, p.Sq, p.Sk, p.wl, p.wr);
-  const RowRange last_rr = live_range(last_row, p.Sq, p.Sk, p.wl, p.wr);
+  const RowRange first_rr = live_range(row0, Sq, Sk, p.wl, p.wr);
+  const RowRange last_rr = live_range(last_row, Sq, Sk, p.wl, p.wr);
   const int kv_lo = first_rr.lo;
   const int kv_hi = last_rr.hi;
   const int jb = kv_lo / 128;
@@ -154,7 +173,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
       for (int t = 0; t < NT; ++t)
         for (int pn = 0; pn < C::PANELS; ++pn)
           tma_load_4d(smem + C::Q_OFF + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bars->q_full, pn * 64,
-                      h, row0 + t * 128, b);
+                      h, q_off + row0 + t * 128, tb);
       int issued = 0;
       bool ok = true;
       for (int jj = 0; jj < n_blocks && ok; ++jj) {
@@ -170,7 +189,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
           const CUtensorMap* m = kv ? &tm_v : &tm_k;
           for (int pn = 0; pn < C::PANELS; ++pn)
             tma_load_4d(smem + C::KV_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, m, &bars->kv_full[s],
-                        pn * 64, hkv, (jb + jj) * 128, b);
+                        pn * 64, hkv, k_off + (jb + jj) * 128, tb);
           issued = it + 1;
         }
       }
@@ -282,15 +301,15 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
     const int r = wq * 32 + lane;
     const int i = row0 + t * 128 + r;
     const uint32_t lane_addr = uint32_t(wq * 32) << 16;
-    const RowRange rr = live_range(i, p.Sq, p.Sk, p.wl, p.wr);
+    const RowRange rr = live_range(i, Sq, Sk, p.wl, p.wr);
     const int tile_first = row0 + t * 128;
-    const int tile_last = min(p.Sq - 1, tile_first + 127);
-    const int tile_lo_max = live_range(tile_last, p.Sq, p.Sk, p.wl, p.wr).lo;
-    const int tile_hi_min = live_range(tile_first, p.Sq, p.Sk, p.wl, p.wr).hi;
+    const int tile_last = min(Sq - 1, tile_first + 127);
+    const int tile_lo_max = live_range(tile_last, Sq, Sk, p.wl, p.wr).lo;
+    const int tile_hi_min = live_range(tile_first, Sq, Sk, p.wl, p.wr).hi;
     const bool has_alibi = p.alibi != nullptr;
     const float slope_log2 =
         has_alibi ? p.alibi[b * p.alibi_bstride + h] * 1.4426950408889634f : 0.0f;
-    const int c_i = i + p.Sk - p.Sq;
+    const int c_i = i + Sk - Sq;
     const float sl = p.scale_log2;
 
     float m = -INFINITY;  // reference max (log2 units) the running O and l are relative to
@@ -381,14 +400,19 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
     }
 
     // ------------------------------------------------------------ epilogue
-    const bool row_ok = i < p.Sq;
-    const size_t orow = ((size_t(b) * p.Sq + size_t(i)) * p.H + h) * size_t(D);
+    // The sequence's length and first row are read again here rather than kept
+    // live across the loop, which would cost registers in the loop.
+    const int e_off = VARLEN ? p.cu_q[b] : 0;
+    const int e_sq = VARLEN ? p.cu_q[b + 1] - e_off : p.Sq;
+    const bool row_ok = i < e_sq;
+    const size_t orow = ((VARLEN ? size_t(e_off) + i : size_t(b) * e_sq + i) * p.H + h) * size_t(D);
+    const size_t lrow = VARLEN ? size_t(h) * p.total_q + e_off + i : (size_t(b) * p.H + h) * e_sq + i;
     if (n_blocks == 0) {
       if (row_ok) {
         uint4 z = make_uint4(0, 0, 0, 0);
         uint4* dst = reinterpret_cast<uint4*>(p.out + orow);
         for (int e = 0; e < D / 8; ++e) dst[e] = z;
-        p.lse[(size_t(b) * p.H + h) * p.Sq + i] = -INFINITY;
+        p.lse[lrow] = -INFINITY;
       }
     } else if (ok && fa_wait_warp(&bars->pv_done[t], uint32_t(n_blocks - 1) & 1u, watch, SITE_SM_EPI)) {
       tc_fence_after();
@@ -408,8 +432,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
         }
       }
       if (row_ok)
-        p.lse[(size_t(b) * p.H + h) * p.Sq + i] =
-            (l > 0.0f) ? (m + lg2_approx(l)) * 0.6931471805599453f : -INFINITY;
+        p.lse[lrow] = (l > 0.0f) ? (m + lg2_approx(l)) * 0.6931471805599453f : -INFINITY;
     }
   }
 
@@ -424,9 +447,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
 
 template <int D, int NT>
 static int launch_fwd_t(const AttnShape& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                        void* out, float* lse, cudaStream_t stream) {
+                        void* out, float* lse, const VarlenArgs* vl, cudaStream_t stream) {
   using C = FwdCfg<D, NT>;
-  auto kern = fa_fwd_kernel<D, NT>;
+  auto kern = vl ? fa_fwd_kernel<D, NT, true> : fa_fwd_kernel<D, NT, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
     return FA_ERR_CUDA;
   FwdParams p;
@@ -439,6 +462,9 @@ static int launch_fwd_t(const AttnShape& s, const CUtensorMap& mq, const CUtenso
   p.Sk = s.Sk;
   p.H = s.H;
   p.group = s.H / s.Hk;
+  p.cu_q = vl ? vl->cu_q : nullptr;
+  p.cu_k = vl ? vl->cu_k : nullptr;
+  p.total_q = vl ? vl->total_q : 0;
   p.wl = s.wl;
   p.wr = s.wr;
   p.scale_log2 = s.scale * 1.4426950408889634f;
@@ -450,19 +476,22 @@ static int launch_fwd_t(const AttnShape& s, const CUtensorMap& mq, const CUtenso
 }
 
 int fwd_launch(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,
-               cudaStream_t stream) {
+               const VarlenArgs* vl, cudaStream_t stream) {
   if (s.B > 65535 || s.H > 65535) return FA_ERR_UNSUPPORTED;
+  // Packed sequences are one (1, total, H, D) tensor; s.Sq, s.Sk are then the longest lengths.
+  const int mb = vl ? 1 : s.B;
+  const int rows_q = vl ? vl->total_q : s.Sq, rows_k = vl ? vl->total_k : s.Sk;
   CUtensorMap mq, mk, mv;
-  if (!make_bshd_map(&mq, q, s.B, s.Sq, s.H, s.D, 128) || !make_bshd_map(&mk, k, s.B, s.Sk, s.Hk, s.D, 128) ||
-      !make_bshd_map(&mv, v, s.B, s.Sk, s.Hk, s.D, 128))
+  if (!make_bshd_map(&mq, q, mb, rows_q, s.H, s.D, 128) || !make_bshd_map(&mk, k, mb, rows_k, s.Hk, s.D, 128) ||
+      !make_bshd_map(&mv, v, mb, rows_k, s.Hk, s.D, 128))
     return FA_ERR_CUDA;
   switch (s.D) {
     case 64:
-      return launch_fwd_t<64, 2>(s, mq, mk, mv, out, lse, stream);
+      return launch_fwd_t<64, 2>(s, mq, mk, mv, out, lse, vl, stream);
     case 128:
-      return launch_fwd_t<128, 2>(s, mq, mk, mv, out, lse, stream);
+      return launch_fwd_t<128, 2>(s, mq, mk, mv, out, lse, vl, stream);
     case 256:
-      return launch_fwd_t<256, 1>(s, mq, mk, mv, out, lse, stream);
+      return launch_fwd_t<256, 1>(s, mq, mk, mv, out, lse, vl, stream);
     default:
       return FA_ERR_UNSUPPORTED;
   }

@@ -17,6 +17,15 @@ struct AttnShape {
   int alibi_bstride;  // 0 (slopes (H,)) or H (slopes (B,H))
 };
 
+// Packed sequences: cumulative lengths cu_q, cu_k (device int32, B + 1 each,
+// starting at 0) and the packed row counts. With these the kernels take each
+// sequence's own lengths and rows; AttnShape's Sq, Sk are the longest ones.
+struct VarlenArgs {
+  const int* cu_q;
+  const int* cu_k;
+  int total_q, total_k;
+};
+
 // Status word of the current device (device pointer), or NULL on failure.
 unsigned int* device_status_word();
 
@@ -30,14 +39,15 @@ bool make_bshd_map(CUtensorMap* map, const void* base, int B, int S, int H, int 
 
 // Kernel launchers (return an fa_status value).
 int fwd_launch(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,
-               cudaStream_t stream);
+               const VarlenArgs* varlen, cudaStream_t stream);
 int decode_launch(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,
                   void* workspace, int num_splits, cudaStream_t stream);
 size_t decode_workspace_bytes(int B, int Sq, int H, int D, int num_splits);
 int decode_auto_splits(int B, int Sq, int Sk, int H, int Hk, int D);
 int bwd_launch(const AttnShape& s, const void* dout, const void* q, const void* k, const void* v,
                const void* out, const float* lse, void* dq, void* dk, void* dv, void* workspace,
-               int deterministic, cudaStream_t stream);
+               int deterministic, const VarlenArgs* varlen, cudaStream_t stream);
+size_t bwd_varlen_workspace_bytes(int B, int total_q, int total_k, int max_sq, int H, int Hk, int D);
 size_t bwd_workspace_bytes(int B, int Sq, int Sk, int H, int Hk, int D, int deterministic);
 
 }  // namespace fa

@@ -84,6 +84,26 @@ int fa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, i
            int alibi_batch_stride, fa_stream_t stream);
 
 /*
+ * Forward over packed sequences of different lengths (page section
+ * "代码解读博客：FlashSelfAttention": cu_seqlens, max_seqlen; the page's
+ * flash_attn_varlen_func, section "函数重命名"). Sequence b has query rows
+ * cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of q (total_q, H, D) and key rows
+ * cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1 of k, v (total_k, Hk, D); it is
+ * attended exactly as fa_fwd would attend it alone (the causal diagonal and
+ * the window are placed per sequence, ALiBi slopes are per b as in fa_fwd).
+ * Writes out (total_q, H, D) bf16 and lse (H, total_q) fp32.
+ * cu_seqlens_q, cu_seqlens_k: DEVICE int32 arrays of B + 1 non-decreasing
+ * entries starting at 0 and ending at total_q / total_k (a sequence may be
+ * empty). max_seqlen_q / max_seqlen_k must be at least the longest query /
+ * key sequence: the grid is sized from them and rows beyond are not
+ * computed. These arrays stay on the device and are not checked.
+ */
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* out, float* lse, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, int B, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                  int H, int Hk, int D, float scale, int causal, int window_left, int window_right,
+                  const float* alibi_slopes, int alibi_batch_stride, fa_stream_t stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: the per-row D_i = rowsum(dO * O)
  * and L*log2(e) vectors, (B, H, Sq rounded up to 128) fp32 each, and fp16
  * copies of q, dout (B, Sq, H, D) and k, v (B, Sk, Hk, D), each section
@@ -113,6 +133,22 @@ int fa_bwd(const void* dout, const void* q, const void* k, const void* v, const 
            void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Sq, int Sk, int H,
            int Hk, int D, float scale, int causal, int window_left, int window_right, const float* alibi_slopes,
            int alibi_batch_stride, int deterministic, fa_stream_t stream);
+
+/* Bytes of device workspace fa_bwd_varlen needs (see fa_bwd_workspace_size). */
+size_t fa_bwd_varlen_workspace_size(int B, int total_q, int total_k, int max_seqlen_q, int H, int Hk, int D);
+
+/*
+ * Backward over packed sequences: the layouts, cu_seqlens and max_seqlen
+ * arguments of fa_fwd_varlen, with dout, q, k, v, out and lse as fa_fwd_varlen
+ * takes and writes them. Writes dq (total_q, H, D), dk, dv (total_k, Hk, D)
+ * bf16, each sequence's gradients exactly as fa_bwd computes them for that
+ * sequence alone. Workspace and precision as fa_bwd.
+ */
+int fa_bwd_varlen(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,
+                  void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, int B, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                  int H, int Hk, int D, float scale, int causal, int window_left, int window_right,
+                  const float* alibi_slopes, int alibi_batch_stride, int deterministic, fa_stream_t stream);
 
 /*
  * Split count fa_decode_splitkv uses when num_splits == 0: chosen from the

@@ -25,4 +25,6 @@ from .attention import (  # noqa: F401
     attention_bwd,
     decode_splitkv,
     kv_head,
+    attention_fwd_varlen,
+    attention_bwd_varlen,
 )

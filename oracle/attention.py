@@ -29,6 +29,11 @@ Definitions used (the page's notation where it has one):
 * Split-KV decode (section "2.2：针对推理进行优化"): each split computes
   attention over its key range; a separate step merges them. Merge used here
   is the exact logsumexp merge: L = log sum_s exp(L_s), O = sum_s exp(L_s - L) O_s.
+* Packed sequences (section "代码解读博客：FlashSelfAttention": cu_seqlens,
+  "cumulative lengths of the sequences in the batch, used to index into qkv";
+  section "函数重命名": flash_attn_varlen_func): sequence b is rows
+  cu[b] .. cu[b+1]-1 of a (total, H, D) tensor and is attended exactly as it
+  would be alone, masks placed per sequence. lse is laid out (H, total_q).
 * Key/value heads (section "代码解读博客：FlashCrossAttention", kv of shape
   (B, Sk, 2, H_k, D)): k and v may have Hk heads with H a multiple of Hk.
   Reading taken here (the page gives no mapping): query head h attends
@@ -293,3 +298,59 @@ def decode_splitkv(q, k, v, num_splits, scale=None, causal=False, window=(-1, -1
             o[b, :, h, :], lse[b, h] = combine_partials([p[0] for p in parts],
                                                         [p[1] for p in parts])
     return o, lse
+
+
+def _sequences(cu_seqlens_q, cu_seqlens_k):
+    cq = [int(x) for x in np.asarray(cu_seqlens_q).ravel()]
+    ck = [int(x) for x in np.asarray(cu_seqlens_k).ravel()]
+    if len(cq) != len(ck) or cq[0] != 0 or ck[0] != 0 or any(b < a for a, b in zip(cq, cq[1:])) or \
+            any(b < a for a, b in zip(ck, ck[1:])):
+        raise ValueError("cu_seqlens must be non-decreasing (B + 1,) arrays starting at 0")
+    return [(cq[b], cq[b + 1], ck[b], ck[b + 1]) for b in range(len(cq) - 1)]
+
+
+def attention_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale=None, causal=False, window=(-1, -1),
+                         alibi_slopes=None):
+    """Packed forward: q (total_q,H,D), k/v (total_k,Hk,D) -> O (total_q,H,D), L (H,total_q), fp64.
+    Each sequence is the one-batch attention_fwd of its own rows (slopes of its index b)."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    total_q, H, D = q.shape
+    o = np.zeros_like(q)
+    lse = np.full((H, total_q), -np.inf)
+    for b, (q0, q1, k0, k1) in enumerate(_sequences(cu_seqlens_q, cu_seqlens_k)):
+        if q1 == q0:
+            continue
+        slopes = None if alibi_slopes is None else _batch_slopes(alibi_slopes, b)
+        if k1 == k0:  # no key at all: every row has no live key
+            continue
+        ob, lb = attention_fwd(q[None, q0:q1], k[None, k0:k1], v[None, k0:k1], scale, causal, window, slopes)
+        o[q0:q1] = ob[0]
+        lse[:, q0:q1] = lb[0]
+    return o, lse
+
+
+def attention_bwd_varlen(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, scale=None, causal=False, window=(-1, -1),
+                         alibi_slopes=None):
+    """Packed backward: dQ (total_q,H,D), dK, dV (total_k,Hk,D), fp64, sequence by sequence."""
+    dout = np.asarray(dout, dtype=np.float64)
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b, (q0, q1, k0, k1) in enumerate(_sequences(cu_seqlens_q, cu_seqlens_k)):
+        if q1 == q0 or k1 == k0:
+            continue
+        slopes = None if alibi_slopes is None else _batch_slopes(alibi_slopes, b)
+        g = attention_bwd(dout[None, q0:q1], q[None, q0:q1], k[None, k0:k1], v[None, k0:k1], scale, causal,
+                          window, slopes)
+        dq[q0:q1], dk[k0:k1], dv[k0:k1] = g[0][0], g[1][0], g[2][0]
+    return dq, dk, dv
+
+
+def _batch_slopes(alibi_slopes, b):
+    a = np.asarray(alibi_slopes, dtype=np.float64)
+    return a if a.ndim == 1 else a[b]
