@@ -52,6 +52,8 @@ _SIGS = {
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _I,
                                _I, _P]),
     "fa_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
+    "fa_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
+                             _I, _P, _I, _I, _P]),
     "fa_selftest_wait_timeout": (_I, [_P]),
 }
 
@@ -323,6 +325,47 @@ def fa_decode_splitkv(q, k_cache, v_cache, *, softmax_scale=None, causal=False, 
                                      int(window_size[1]), _ptr(al), al_stride, int(num_splits),
                                      _stream_ptr(stream, dev))
     _check("fa_decode_splitkv", st)
+    return out, lse
+
+
+def fa_decode_paged(q, k_pages, v_pages, block_table, seqlens_k, max_seqlen_k, *, softmax_scale=None,
+                    causal=False, window_size=(-1, -1), alibi_slopes=None, num_splits=0, workspace=None, out=None,
+                    lse=None, stream=None):
+    """Split-KV decode over a paged cache: q (B,Sq<=16,H,D); k/v pages (num_pages,page_size,Hk,D) bf16;
+    block_table (B,max_pages) and seqlens_k (B,) int32 on the device; max_seqlen_k >= every seqlens_k[b].
+    -> out (B,Sq,H,D) bf16, lse (B,H,Sq) fp32."""
+    _need(q, "q", torch.bfloat16)
+    B, Sq, H, D = q.shape
+    if k_pages.dim() != 4:
+        raise ValueError("k_pages must be (num_pages, page_size, Hk, D)")
+    num_pages, page_size, Hk = int(k_pages.shape[0]), int(k_pages.shape[1]), int(k_pages.shape[2])
+    if Hk < 1 or H % Hk != 0:
+        raise ValueError(f"the query heads ({H}) must be a multiple of the key/value heads ({Hk})")
+    dev = q.device
+    _need(k_pages, "k_pages", torch.bfloat16, (num_pages, page_size, Hk, D), dev)
+    _need(v_pages, "v_pages", torch.bfloat16, (num_pages, page_size, Hk, D), dev)
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be (B, max_pages_per_seq)")
+    max_pages = int(block_table.shape[1])
+    _need(block_table, "block_table", torch.int32, (B, max_pages), dev)
+    _need(seqlens_k, "seqlens_k", torch.int32, (B,), dev)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, (B, Sq, H, D), dev)
+    _need(lse, "lse", torch.float32, (B, H, Sq), dev)
+    need = fa_decode_workspace_size(B, Sq, int(max_seqlen_k), H, D, num_splits, Hk=Hk)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, device=dev)
+    al, al_stride = _alibi(alibi_slopes, B, H, dev)
+    st = library().fa_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seqlens_k),
+                                   _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), B, Sq, int(max_seqlen_k),
+                                   num_pages, page_size, max_pages, H, Hk, D, _scale(softmax_scale, D),
+                                   int(bool(causal)), int(window_size[0]), int(window_size[1]), _ptr(al), al_stride,
+                                   int(num_splits), _stream_ptr(stream, dev))
+    _check("fa_decode_paged", st)
     return out, lse
 
 

@@ -251,7 +251,35 @@ int fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, v
   const size_t need = fa::decode_workspace_bytes(B, Sq, H, D, n);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
     return FA_ERR_WORKSPACE;
-  return fa::decode_launch(s, q, k_cache, v_cache, out, lse, workspace, n, reinterpret_cast<cudaStream_t>(stream));
+  return fa::decode_launch(s, q, k_cache, v_cache, out, lse, workspace, n, nullptr,
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                    const int* seqlens_k, void* out, float* lse, void* workspace, size_t workspace_bytes, int B,
+                    int Sq, int max_seqlen_k, int num_pages, int page_size, int max_pages_per_seq, int H, int Hk,
+                    int D, float scale, int causal, int window_left, int window_right, const float* alibi_slopes,
+                    int alibi_batch_stride, int num_splits, fa_stream_t stream) {
+  if (!q || !k_pages || !v_pages || !block_table || !seqlens_k || !out || !lse) return FA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out) || !aligned16(lse))
+    return FA_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seqlens_k) & 3u))
+    return FA_ERR_INVALID;
+  if (num_pages < 1 || page_size < 1 || max_pages_per_seq < 1) return FA_ERR_INVALID;
+  AttnShape s;
+  int st = check_common(B, Sq, max_seqlen_k, H, Hk, D, scale, causal, window_left, window_right, alibi_slopes,
+                        alibi_batch_stride, &s);
+  if (st != FA_OK) return st;
+  if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
+  if (Sq > 16 || page_size % 128 != 0 || (long long)max_pages_per_seq * page_size > (1 << 30))
+    return FA_ERR_UNSUPPORTED;
+  if (num_splits < 0 || num_splits > 256) return FA_ERR_INVALID;
+  const int n = num_splits == 0 ? fa::decode_auto_splits(B, Sq, max_seqlen_k, H, Hk, D) : num_splits;
+  const size_t need = fa::decode_workspace_bytes(B, Sq, H, D, n);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return FA_ERR_WORKSPACE;
+  const fa::PagedArgs pg{block_table, seqlens_k, num_pages, page_size, max_pages_per_seq};
+  return fa::decode_launch(s, q, k_pages, v_pages, out, lse, workspace, n, &pg, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fa_device_status(fa_stream_t stream, unsigned int* detail) {

@@ -5,7 +5,8 @@
 // cache; the key range is cut into splits handled by separate thread blocks,
 // and a separate kernel merges the per-split results.
 //
-// Split kernel (one CTA per (split, head, batch x query row)):
+// Split kernel (one CTA per (split, head, batch x query row)); the caches are
+// dense (B, Sk, Hk, D) or pages addressed through a block table:
 //   warp 4      TMA producer: streams 32 KB stages (TK keys of K and of V,
 //               128-byte swizzled) through an mbarrier ring.
 //   warps 0..3  consumers: thread (g, c) owns 16-byte chunk c of the head dim
@@ -53,8 +54,15 @@ struct DecParams {
   float* part_l;  // [B][Sq][H][n]
   const float* alibi;
   int alibi_bstride;
-  int B, Sq, Sk, H, n_splits;
+  int B, Sq, Sk, H, n_splits;  // Sk: with a page table, the longest sequence
   int group;  // query heads per key/value head (H / Hk)
+  // Paged KV cache (page section "2.5：分页KV缓存"): NULL for the dense
+  // (B, Sk, Hk, D) caches; else logical key block p of sequence b lives in page
+  // block_table[b * max_pages + p] of (num_pages, page_size, Hk, D) caches and
+  // the sequence has seqlens_k[b] keys. page_size is a multiple of TK.
+  const int* block_table;
+  const int* seqlens_k;
+  int page_size, max_pages;
   int wl, wr;
   float scale_log2;
   unsigned int* status;
@@ -98,12 +106,18 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS)
   const int h = blockIdx.y;
   const int b = blockIdx.z / p.Sq;
   const int i = blockIdx.z % p.Sq;
-  const RowRange rr = live_range(i, p.Sq, p.Sk, p.wl, p.wr);
-  int ks = int((long long)p.Sk * split / p.n_splits);
-  int ke = int((long long)p.Sk * (split + 1) / p.n_splits);  // exclusive
+  // this sequence's keys; a page-table length is clamped to the table's reach
+  const int Sk = p.block_table ? max(0, min(p.seqlens_k[b], p.max_pages * p.page_size)) : p.Sk;
+  const RowRange rr = live_range(i, p.Sq, Sk, p.wl, p.wr);
+  // Splits cut the key range at whole tiles, so a tile never straddles a page;
+  // keys outside [ks, ke) (the live range clipped to this split) are masked.
+  const int n_all = (Sk + C::TK - 1) / C::TK;
+  int ks = int((long long)n_all * split / p.n_splits) * C::TK;
+  int ke = min(Sk, int((long long)n_all * (split + 1) / p.n_splits) * C::TK);  // exclusive
   ks = max(ks, rr.lo);
   ke = min(ke, rr.hi + 1);
-  const int n_tiles = ke > ks ? (ke - ks + C::TK - 1) / C::TK : 0;
+  const int t0 = (ks / C::TK) * C::TK;  // first tile, aligned
+  const int n_tiles = ke > ks ? (ke - t0 + C::TK - 1) / C::TK : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::NSTAGE; ++s) {
@@ -130,11 +144,15 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS)
         if (!fa_wait(&bars->empty[s], ph ^ 1u, watch, SITE_DEC_EMPTY)) break;
         uint8_t* st = smem + s * C::STAGE_BYTES;
         mbar_arrive_expect_tx(&bars->full[s], C::STAGE_BYTES);
-        const int row = ks + t * C::TK;
+        int row = t0 + t * C::TK, tb = b;
+        if (p.block_table) {  // (row in page, page) coordinates of this tile
+          tb = p.block_table[size_t(b) * p.max_pages + row / p.page_size];
+          row %= p.page_size;
+        }
 #pragma unroll
         for (int pn = 0; pn < C::PANELS; ++pn) {
-          tma_load_4d(st + pn * C::PANEL_BYTES, &tm_k, &bars->full[s], pn * 64, h / p.group, row, b);
-          tma_load_4d(st + C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_v, &bars->full[s], pn * 64, h / p.group, row, b);
+          tma_load_4d(st + pn * C::PANEL_BYTES, &tm_k, &bars->full[s], pn * 64, h / p.group, row, tb);
+          tma_load_4d(st + C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_v, &bars->full[s], pn * 64, h / p.group, row, tb);
         }
         issued = t + 1;
       }
@@ -165,7 +183,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS)
   }
   const bool has_alibi = p.alibi != nullptr;
   const float slope_log2 = has_alibi ? p.alibi[b * p.alibi_bstride + h] * 1.4426950408889634f : 0.0f;
-  const int c_i = i + p.Sk - p.Sq;
+  const int c_i = i + Sk - p.Sq;
   const int pn = c / 8;
   const int cc = c % 8;
 
@@ -179,7 +197,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS)
     if (!fa_wait_warp(&bars->full[s], uint32_t(t / C::NSTAGE) & 1u, watch, SITE_DEC_FULL)) break;
     const uint8_t* kt = smem + s * C::STAGE_BYTES + pn * C::PANEL_BYTES;
     const uint8_t* vt = kt + C::TILE_BYTES;
-    const int row0 = ks + t * C::TK;
+    const int row0 = t0 + t * C::TK;
     float sc[C::KPL];
 #pragma unroll
     for (int u = 0; u < C::KPL; ++u) {
@@ -194,7 +212,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS)
       for (int off = C::CH / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
       const int kj = row0 + kr;
       if (has_alibi) d -= slope_log2 * fabsf(float(c_i - kj));
-      sc[u] = (kj < ke) ? d : -INFINITY;
+      sc[u] = (kj >= ks && kj < ke) ? d : -INFINITY;
     }
     float mt = sc[0];
 #pragma unroll
@@ -342,10 +360,13 @@ int decode_auto_splits(int B, int Sq, int Sk, int H, int Hk, int D) {
 
 template <int D>
 static int launch_decode_t(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,
-                           void* ws, int n, cudaStream_t stream) {
+                           void* ws, int n, const PagedArgs* pg, cudaStream_t stream) {
   using C = DecCfg<D>;
+  if (pg && pg->page_size % C::TK != 0) return FA_ERR_UNSUPPORTED;
+  // Dense caches are (B, Sk, Hk, D); pages are (num_pages, page_size, Hk, D).
+  const int mb = pg ? pg->num_pages : s.B, mrows = pg ? pg->page_size : s.Sk;
   CUtensorMap mk, mv;
-  if (!make_bshd_map(&mk, k, s.B, s.Sk, s.Hk, D, C::TK) || !make_bshd_map(&mv, v, s.B, s.Sk, s.Hk, D, C::TK))
+  if (!make_bshd_map(&mk, k, mb, mrows, s.Hk, D, C::TK) || !make_bshd_map(&mv, v, mb, mrows, s.Hk, D, C::TK))
     return FA_ERR_CUDA;
   auto kern = fa_decode_split_kernel<D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
@@ -362,6 +383,10 @@ static int launch_decode_t(const AttnShape& s, const void* q, const void* k, con
   p.Sk = s.Sk;
   p.H = s.H;
   p.group = s.H / s.Hk;
+  p.block_table = pg ? pg->block_table : nullptr;
+  p.seqlens_k = pg ? pg->seqlens_k : nullptr;
+  p.page_size = pg ? pg->page_size : 0;
+  p.max_pages = pg ? pg->max_pages : 0;
   p.n_splits = n;
   p.wl = s.wl;
   p.wr = s.wr;
@@ -379,14 +404,14 @@ static int launch_decode_t(const AttnShape& s, const void* q, const void* k, con
 }
 
 int decode_launch(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,
-                  void* workspace, int n, cudaStream_t stream) {
+                  void* workspace, int n, const PagedArgs* paged, cudaStream_t stream) {
   switch (s.D) {
     case 64:
-      return launch_decode_t<64>(s, q, k, v, out, lse, workspace, n, stream);
+      return launch_decode_t<64>(s, q, k, v, out, lse, workspace, n, paged, stream);
     case 128:
-      return launch_decode_t<128>(s, q, k, v, out, lse, workspace, n, stream);
+      return launch_decode_t<128>(s, q, k, v, out, lse, workspace, n, paged, stream);
     case 256:
-      return launch_decode_t<256>(s, q, k, v, out, lse, workspace, n, stream);
+      return launch_decode_t<256>(s, q, k, v, out, lse, workspace, n, paged, stream);
     default:
       return FA_ERR_UNSUPPORTED;
   }

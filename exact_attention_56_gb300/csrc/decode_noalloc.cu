@@ -90,5 +90,5 @@ extern "C" int fa_decode_splitkv_noalloc(const void* q, const void* k_cache, con
   s.wr = causal ? 0 : window_right;
   s.alibi = alibi_slopes;
   s.alibi_bstride = alibi_slopes ? alibi_batch_stride : 0;
-  return fa::decode_launch(s, q, k_cache, v_cache, out, lse, ws, n, reinterpret_cast<cudaStream_t>(stream));
+  return fa::decode_launch(s, q, k_cache, v_cache, out, lse, ws, n, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }

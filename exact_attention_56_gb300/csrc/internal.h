@@ -26,6 +26,14 @@ struct VarlenArgs {
   int total_q, total_k;
 };
 
+// Paged KV cache for decode: caches (num_pages, page_size, Hk, D); key block p
+// of sequence b is page block_table[b * max_pages + p]; seqlens_k[b] keys.
+struct PagedArgs {
+  const int* block_table;
+  const int* seqlens_k;
+  int num_pages, page_size, max_pages;
+};
+
 // Status word of the current device (device pointer), or NULL on failure.
 unsigned int* device_status_word();
 
@@ -41,7 +49,7 @@ bool make_bshd_map(CUtensorMap* map, const void* base, int B, int S, int H, int 
 int fwd_launch(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,
                const VarlenArgs* varlen, cudaStream_t stream);
 int decode_launch(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,
-                  void* workspace, int num_splits, cudaStream_t stream);
+                  void* workspace, int num_splits, const PagedArgs* paged, cudaStream_t stream);
 size_t decode_workspace_bytes(int B, int Sq, int H, int D, int num_splits);
 int decode_auto_splits(int B, int Sq, int Sk, int H, int Hk, int D);
 int bwd_launch(const AttnShape& s, const void* dout, const void* q, const void* k, const void* v,

@@ -176,6 +176,26 @@ int fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, v
                       int alibi_batch_stride, int num_splits, fa_stream_t stream);
 
 /*
+ * Split-KV decode over a paged KV cache (section "2.5：分页KV缓存", which only
+ * names the feature; the layout here is the reading taken): k_pages, v_pages
+ * are (num_pages, page_size, Hk, D) bf16; logical key block p (keys
+ * p*page_size .. p*page_size + page_size - 1) of sequence b is page
+ * block_table[b * max_pages_per_seq + p]; sequence b has seqlens_k[b] keys.
+ * block_table (B, max_pages_per_seq) and seqlens_k (B,) are DEVICE int32
+ * arrays, not read back: a length beyond max_pages_per_seq * page_size is
+ * clamped to it, and a page index outside [0, num_pages) reads zeros.
+ * max_seqlen_k bounds every seqlens_k[b] (it sizes the splits). q, out, lse,
+ * masks (anchored at each sequence's own length), ALiBi, num_splits and the
+ * workspace (fa_decode_workspace_size with Sk = max_seqlen_k) are those of
+ * fa_decode_splitkv. Supported: page_size a multiple of 128, Sq <= 16.
+ */
+int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                    const int* seqlens_k, void* out, float* lse, void* workspace, size_t workspace_bytes, int B,
+                    int Sq, int max_seqlen_k, int num_pages, int page_size, int max_pages_per_seq, int H, int Hk,
+                    int D, float scale, int causal, int window_left, int window_right, const float* alibi_slopes,
+                    int alibi_batch_stride, int num_splits, fa_stream_t stream);
+
+/*
  * Split-KV decode that allocates nothing and takes no workspace. The pages
  * have no counterpart to this entry point; it exists for callers that cannot
  * allocate device memory where they run decode (an allocation-free serving

@@ -27,4 +27,5 @@ from .attention import (  # noqa: F401
     kv_head,
     attention_fwd_varlen,
     attention_bwd_varlen,
+    decode_paged,
 )

@@ -34,6 +34,10 @@ Definitions used (the page's notation where it has one):
   section "函数重命名": flash_attn_varlen_func): sequence b is rows
   cu[b] .. cu[b+1]-1 of a (total, H, D) tensor and is attended exactly as it
   would be alone, masks placed per sequence. lse is laid out (H, total_q).
+* Paged KV cache (section "2.5：分页KV缓存" names the feature only). Reading
+  taken here: caches of pages (num_pages, page_size, Hk, D); key block p of
+  sequence b (keys p*page_size ..) is page block_table[b, p]; the sequence has
+  seqlens_k[b] keys, and decode attends them as the dense forward would.
 * Key/value heads (section "代码解读博客：FlashCrossAttention", kv of shape
   (B, Sk, 2, H_k, D)): k and v may have Hk heads with H a multiple of Hk.
   Reading taken here (the page gives no mapping): query head h attends
@@ -354,3 +358,27 @@ def attention_bwd_varlen(dout, q, k, v, cu_seqlens_q, cu_seqlens_k, scale=None, 
 def _batch_slopes(alibi_slopes, b):
     a = np.asarray(alibi_slopes, dtype=np.float64)
     return a if a.ndim == 1 else a[b]
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seqlens_k, scale=None, causal=False, window=(-1, -1),
+                 alibi_slopes=None):
+    """Decode over a paged cache: q (B,Sq,H,D), pages (num_pages,page_size,Hk,D), block_table (B,max_pages),
+    seqlens_k (B,) -> O (B,Sq,H,D), L (B,H,Sq) fp64. Each sequence's keys are gathered page by page and
+    attended as attention_fwd does; a sequence without keys gives O = 0, L = -inf."""
+    q = np.asarray(q, dtype=np.float64)
+    B, Sq, H, D = q.shape
+    page_size = k_pages.shape[1]
+    table = np.asarray(block_table)
+    o = np.zeros_like(q)
+    lse = np.full((B, H, Sq), -np.inf)
+    for b in range(B):
+        n = int(seqlens_k[b])
+        if n == 0:
+            continue
+        pages = [int(table[b, p]) for p in range((n + page_size - 1) // page_size)]
+        kb = np.concatenate([np.asarray(k_pages[pg], dtype=np.float64) for pg in pages])[:n]
+        vb = np.concatenate([np.asarray(v_pages[pg], dtype=np.float64) for pg in pages])[:n]
+        slopes = None if alibi_slopes is None else _batch_slopes(alibi_slopes, b)
+        ob, lb = attention_fwd(q[b:b + 1], kb[None], vb[None], scale, causal, window, slopes)
+        o[b], lse[b] = ob[0], lb[0]
+    return o, lse
