@@ -29,6 +29,7 @@ from ._native import (  # noqa: F401
     fa_bwd_varlen_workspace_size,
     fa_decode_splitkv,
     fa_decode_paged,
+    fa_decode_kvcache,
     fa_decode_workspace_size,
     fa_decode_num_splits,
     fa_device_status,
@@ -50,6 +51,7 @@ __all__ = [
     "fa_bwd_varlen_workspace_size",
     "fa_decode_splitkv",
     "fa_decode_paged",
+    "fa_decode_kvcache",
     "fa_decode_workspace_size",
     "fa_decode_num_splits",
     "fa_device_status",

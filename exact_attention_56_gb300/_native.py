@@ -54,6 +54,8 @@ _SIGS = {
     "fa_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "fa_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
                              _I, _P, _I, _I, _P]),
+    "fa_decode_kvcache": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _SZ,
+                               _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _I, _I, _P]),
     "fa_selftest_wait_timeout": (_I, [_P]),
 }
 
@@ -366,6 +368,67 @@ def fa_decode_paged(q, k_pages, v_pages, block_table, seqlens_k, max_seqlen_k, *
                                    int(bool(causal)), int(window_size[0]), int(window_size[1]), _ptr(al), al_stride,
                                    int(num_splits), _stream_ptr(stream, dev))
     _check("fa_decode_paged", st)
+    return out, lse
+
+
+def fa_decode_kvcache(q, k_cache, v_cache, cache_seqlens, k_new=None, v_new=None, *, rotary_cos=None,
+                      rotary_sin=None, rotary_interleaved=False, block_table=None, softmax_scale=None, causal=False,
+                      window_size=(-1, -1), alibi_slopes=None, num_splits=0, workspace=None, out=None, lse=None,
+                      stream=None):
+    """Decode step on a KV cache: appends k_new, v_new (B,S_new,Hk,D) behind cache_seqlens (B,) int32 in
+    place (keys rotated), rotates q, and attends. Caches dense (B,rows,Hk,D) or, with block_table
+    (B,max_pages) int32, pages (num_pages,page_size,Hk,D). rotary_cos/sin: (len, rotary_dim/2) fp32."""
+    _need(q, "q", torch.bfloat16)
+    B, Sq, H, D = q.shape
+    dev = q.device
+    if k_cache.dim() != 4:
+        raise ValueError("k_cache must be 4-D")
+    Hk = int(k_cache.shape[2])
+    if Hk < 1 or H % Hk != 0:
+        raise ValueError(f"the query heads ({H}) must be a multiple of the key/value heads ({Hk})")
+    _need(k_cache, "k_cache", torch.bfloat16, tuple(k_cache.shape), dev)
+    _need(v_cache, "v_cache", torch.bfloat16, tuple(k_cache.shape), dev)
+    _need(cache_seqlens, "cache_seqlens", torch.int32, (B,), dev)
+    if block_table is not None:
+        num_pages, page_size = int(k_cache.shape[0]), int(k_cache.shape[1])
+        max_pages = int(block_table.shape[1]) if block_table.dim() == 2 else -1
+        _need(block_table, "block_table", torch.int32, (B, max_pages), dev)
+        cache_rows = 0
+        cap = max_pages * page_size
+    else:
+        if k_cache.shape[0] != B:
+            raise ValueError("a dense cache must be (B, rows, Hk, D)")
+        num_pages, page_size, max_pages = 0, 0, 0
+        cache_rows = cap = int(k_cache.shape[1])
+    S_new = 0
+    if k_new is not None:
+        S_new = int(k_new.shape[1])
+        _need(k_new, "k_new", torch.bfloat16, (B, S_new, Hk, D), dev)
+        _need(v_new, "v_new", torch.bfloat16, (B, S_new, Hk, D), dev)
+    rot_dim = rot_len = 0
+    if rotary_cos is not None:
+        _need(rotary_cos, "rotary_cos", torch.float32, device=dev)
+        rot_len, half = int(rotary_cos.shape[0]), int(rotary_cos.shape[1])
+        _need(rotary_sin, "rotary_sin", torch.float32, (rot_len, half), dev)
+        rot_dim = 2 * half
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, (B, Sq, H, D), dev)
+    _need(lse, "lse", torch.float32, (B, H, Sq), dev)
+    need = fa_decode_workspace_size(B, Sq, cap, H, D, num_splits, Hk=Hk)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, device=dev)
+    al, al_stride = _alibi(alibi_slopes, B, H, dev)
+    st = library().fa_decode_kvcache(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_seqlens), _ptr(k_new), _ptr(v_new), S_new,
+        _ptr(rotary_cos), _ptr(rotary_sin), rot_dim, rot_len, int(bool(rotary_interleaved)), _ptr(block_table),
+        num_pages, page_size, max_pages, _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), B, Sq,
+        cache_rows, H, Hk, D, _scale(softmax_scale, D), int(bool(causal)), int(window_size[0]), int(window_size[1]),
+        _ptr(al), al_stride, int(num_splits), _stream_ptr(stream, dev))
+    _check("fa_decode_kvcache", st)
     return out, lse
 
 

@@ -278,8 +278,56 @@ int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, con
   const size_t need = fa::decode_workspace_bytes(B, Sq, H, D, n);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
     return FA_ERR_WORKSPACE;
-  const fa::PagedArgs pg{block_table, seqlens_k, num_pages, page_size, max_pages_per_seq};
-  return fa::decode_launch(s, q, k_pages, v_pages, out, lse, workspace, n, &pg, reinterpret_cast<cudaStream_t>(stream));
+  const fa::CacheArgs cg{block_table, seqlens_k, num_pages, page_size, max_pages_per_seq,
+                         0, max_pages_per_seq * page_size, fa::Rotary{nullptr, nullptr, 0, 0, 0}};
+  return fa::decode_launch(s, q, k_pages, v_pages, out, lse, workspace, n, &cg, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fa_decode_kvcache(const void* q, void* k_cache, void* v_cache, const int* cache_seqlens, const void* k_new,
+                      const void* v_new, int S_new, const float* rotary_cos, const float* rotary_sin, int rotary_dim,
+                      int rotary_len, int rotary_interleaved, const int* block_table, int num_pages, int page_size,
+                      int max_pages_per_seq, void* out, float* lse, void* workspace, size_t workspace_bytes, int B,
+                      int Sq, int cache_rows, int H, int Hk, int D, float scale, int causal, int window_left,
+                      int window_right, const float* alibi_slopes, int alibi_batch_stride, int num_splits,
+                      fa_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !cache_seqlens || !out || !lse) return FA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(lse))
+    return FA_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(cache_seqlens) & 3u) return FA_ERR_INVALID;
+  if (S_new < 0 || (S_new > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))))
+    return FA_ERR_INVALID;
+  if (rotary_cos || rotary_sin) {
+    if (!rotary_cos || !rotary_sin || (reinterpret_cast<uintptr_t>(rotary_cos) & 3u) ||
+        (reinterpret_cast<uintptr_t>(rotary_sin) & 3u) || rotary_len < 1)
+      return FA_ERR_INVALID;
+    if (rotary_dim < 16 || rotary_dim > D || rotary_dim % 16 != 0) return FA_ERR_UNSUPPORTED;
+  }
+  const bool paged = block_table != nullptr;
+  if (paged) {
+    if (reinterpret_cast<uintptr_t>(block_table) & 3u) return FA_ERR_INVALID;
+    if (num_pages < 1 || page_size < 1 || max_pages_per_seq < 1) return FA_ERR_INVALID;
+    if (page_size % 128 != 0 || (long long)max_pages_per_seq * page_size > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  } else if (cache_rows < 1) {
+    return FA_ERR_INVALID;
+  }
+  const int cap = paged ? max_pages_per_seq * page_size : cache_rows;
+  AttnShape s;
+  int st = check_common(B, Sq, cap, H, Hk, D, scale, causal, window_left, window_right, alibi_slopes,
+                        alibi_batch_stride, &s);
+  if (st != FA_OK) return st;
+  if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
+  if (Sq > 16) return FA_ERR_UNSUPPORTED;
+  if (num_splits < 0 || num_splits > 256) return FA_ERR_INVALID;
+  const int n = num_splits == 0 ? fa::decode_auto_splits(B, Sq, cap, H, Hk, D) : num_splits;
+  const size_t need = fa::decode_workspace_bytes(B, Sq, H, D, n);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return FA_ERR_WORKSPACE;
+  const fa::CacheArgs cg{block_table, cache_seqlens, num_pages, page_size, max_pages_per_seq, S_new, cap,
+                         fa::Rotary{rotary_cos, rotary_sin, rotary_dim, rotary_len, rotary_interleaved ? 1 : 0}};
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  st = fa::kv_append_launch(s, k_new, v_new, k_cache, v_cache, cg, cs);
+  if (st != FA_OK) return st;
+  return fa::decode_launch(s, q, k_cache, v_cache, out, lse, workspace, n, &cg, cs);
 }
 
 int fa_device_status(fa_stream_t stream, unsigned int* detail) {

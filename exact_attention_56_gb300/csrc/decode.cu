@@ -26,6 +26,7 @@
 #include "../../include/fa.h"
 #include "internal.h"
 #include "ptx.cuh"
+#include "rotary.cuh"
 
 namespace fa {
 
@@ -63,6 +64,11 @@ struct DecParams {
   const int* block_table;
   const int* seqlens_k;
   int page_size, max_pages;
+  // With seqlens_k, sequence b has min(seqlens_k[b] + s_new, cap) keys: s_new
+  // rows appended in this call behind seqlens_k[b] cached ones, cap the rows the
+  // cache holds per sequence.
+  int s_new, cap;
+  Rotary rot;  // rotation of q, row i at position i + Sk_b - Sq (rot.cos NULL: none)
   int wl, wr;
   float scale_log2;
   unsigned int* status;
@@ -106,8 +112,8 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS)
   const int h = blockIdx.y;
   const int b = blockIdx.z / p.Sq;
   const int i = blockIdx.z % p.Sq;
-  // this sequence's keys; a page-table length is clamped to the table's reach
-  const int Sk = p.block_table ? max(0, min(p.seqlens_k[b], p.max_pages * p.page_size)) : p.Sk;
+  // this sequence's keys, clamped to what the cache (or its page table) holds
+  const int Sk = p.seqlens_k ? max(0, min(p.seqlens_k[b] + p.s_new, p.cap)) : p.Sk;
   const RowRange rr = live_range(i, p.Sq, Sk, p.wl, p.wr);
   // Splits cut the key range at whole tiles, so a tile never straddles a page;
   // keys outside [ks, ke) (the live range clipped to this split) are masked.
@@ -176,8 +182,14 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS)
   const int g = tid / C::CH;
   float qf[8];
   {
-    const uint4 qv = *reinterpret_cast<const uint4*>(p.q + ((size_t(b) * p.Sq + i) * p.H + h) * D + c * 8);
-    bf16x8_to_f32(qv, qf);
+    const __nv_bfloat16* qrow = p.q + ((size_t(b) * p.Sq + i) * p.H + h) * D;
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(qrow + c * 8), qf);
+    if (p.rot.cos != nullptr && c * 8 < p.rot.dim) {  // rotary at the row's diagonal position
+      float pq[8];
+      if (!p.rot.interleaved)
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(qrow + rotary_partner(c * 8, p.rot)), pq);
+      rotary8(qf, pq, c * 8, i + Sk - p.Sq, p.rot);
+    }
 #pragma unroll
     for (int e = 0; e < 8; ++e) qf[e] *= p.scale_log2;
   }
@@ -271,6 +283,53 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS)
   if (tid == 0) p.part_l[pidx] = L > 0.0f ? (M + lg2_approx(L)) * 0.6931471805599453f : -INFINITY;
 }
 
+// Appends s_new rows of k_new, v_new (B, s_new, Hk, D) to the cache at
+// positions seqlens[b] + s, the keys rotated at their positions (page section
+// "2.2": flash_attn_with_kvcache updates the KV cache in place and applies
+// rotary embeddings). One thread per 16-byte chunk; rows past the cache's
+// capacity, and rows whose page index lies outside the cache, are not written.
+template <int D>
+__global__ void __launch_bounds__(256) fa_kv_append_kernel(const __nv_bfloat16* __restrict__ k_new,
+                                                           const __nv_bfloat16* __restrict__ v_new,
+                                                           __nv_bfloat16* k_cache, __nv_bfloat16* v_cache,
+                                                           const int* seqlens, const int* block_table, int B,
+                                                           int s_new, int Hk, int cap, int num_pages, int page_size,
+                                                           int max_pages, Rotary rot) {
+  constexpr int CPR = D / 8;
+  const long long n = (long long)B * s_new * Hk * CPR;
+  for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < n;
+       it += (long long)gridDim.x * blockDim.x) {
+    const int c = int(it % CPR);
+    const long long row = it / CPR;  // (b * s_new + s) * Hk + hk
+    const int hk = int(row % Hk);
+    const int s = int((row / Hk) % s_new);
+    const int b = int(row / (Hk * (long long)s_new));
+    const int pos = seqlens[b] + s;
+    if (pos < 0 || pos >= cap) continue;
+    size_t dst_row;
+    if (block_table) {
+      const int page = block_table[size_t(b) * max_pages + pos / page_size];
+      if (page < 0 || page >= num_pages) continue;
+      dst_row = size_t(page) * page_size + pos % page_size;
+    } else {
+      dst_row = size_t(b) * cap + pos;
+    }
+    const size_t src = size_t(row) * D;
+    const size_t dst = (dst_row * Hk + hk) * D + c * 8;
+    *reinterpret_cast<uint4*>(v_cache + dst) = *reinterpret_cast<const uint4*>(v_new + src + c * 8);
+    uint4 kv = *reinterpret_cast<const uint4*>(k_new + src + c * 8);
+    if (rot.cos != nullptr && c * 8 < rot.dim) {
+      float x[8], px[8];
+      bf16x8_to_f32(kv, x);
+      if (!rot.interleaved) bf16x8_to_f32(*reinterpret_cast<const uint4*>(k_new + src + rotary_partner(c * 8, rot)), px);
+      rotary8(x, px, c * 8, pos, rot);
+      kv = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                      pack_bf16x2(x[6], x[7]));
+    }
+    *reinterpret_cast<uint4*>(k_cache + dst) = kv;
+  }
+}
+
 // One warp per (b, query row, head).
 template <int D>
 __global__ void __launch_bounds__(256) fa_decode_combine_kernel(const float* __restrict__ part_o,
@@ -330,6 +389,35 @@ __global__ void __launch_bounds__(256) fa_decode_combine_kernel(const float* __r
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+int kv_append_launch(const AttnShape& s, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                     const CacheArgs& c, cudaStream_t stream) {
+  if (c.s_new < 1) return FA_OK;
+  const long long items = (long long)s.B * c.s_new * s.Hk * (s.D / 8);
+  const long long cap_blocks = (long long)device_sm_count() * 8;
+  const int grid = int(std::max(1LL, std::min(cap_blocks, (items + 255) / 256)));
+  const auto* kn = static_cast<const __nv_bfloat16*>(k_new);
+  const auto* vn = static_cast<const __nv_bfloat16*>(v_new);
+  auto* kc = static_cast<__nv_bfloat16*>(k_cache);
+  auto* vc = static_cast<__nv_bfloat16*>(v_cache);
+  switch (s.D) {
+    case 64:
+      fa_kv_append_kernel<64><<<grid, 256, 0, stream>>>(kn, vn, kc, vc, c.seqlens, c.block_table, s.B, c.s_new, s.Hk,
+                                                          c.cap, c.num_pages, c.page_size, c.max_pages, c.rot);
+      break;
+    case 128:
+      fa_kv_append_kernel<128><<<grid, 256, 0, stream>>>(kn, vn, kc, vc, c.seqlens, c.block_table, s.B, c.s_new, s.Hk,
+                                                           c.cap, c.num_pages, c.page_size, c.max_pages, c.rot);
+      break;
+    case 256:
+      fa_kv_append_kernel<256><<<grid, 256, 0, stream>>>(kn, vn, kc, vc, c.seqlens, c.block_table, s.B, c.s_new, s.Hk,
+                                                           c.cap, c.num_pages, c.page_size, c.max_pages, c.rot);
+      break;
+    default:
+      return FA_ERR_UNSUPPORTED;
+  }
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 size_t decode_workspace_bytes(int B, int Sq, int H, int D, int n) {
   const size_t units = size_t(B) * Sq * H * n;
   return align256(units * D * 4) + align256(units * 4);
@@ -360,11 +448,12 @@ int decode_auto_splits(int B, int Sq, int Sk, int H, int Hk, int D) {
 
 template <int D>
 static int launch_decode_t(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,
-                           void* ws, int n, const PagedArgs* pg, cudaStream_t stream) {
+                           void* ws, int n, const CacheArgs* cg, cudaStream_t stream) {
   using C = DecCfg<D>;
-  if (pg && pg->page_size % C::TK != 0) return FA_ERR_UNSUPPORTED;
-  // Dense caches are (B, Sk, Hk, D); pages are (num_pages, page_size, Hk, D).
-  const int mb = pg ? pg->num_pages : s.B, mrows = pg ? pg->page_size : s.Sk;
+  const bool paged = cg && cg->block_table;
+  if (paged && cg->page_size % C::TK != 0) return FA_ERR_UNSUPPORTED;
+  // Dense caches are (B, rows, Hk, D); pages are (num_pages, page_size, Hk, D).
+  const int mb = paged ? cg->num_pages : s.B, mrows = paged ? cg->page_size : (cg ? cg->cap : s.Sk);
   CUtensorMap mk, mv;
   if (!make_bshd_map(&mk, k, mb, mrows, s.Hk, D, C::TK) || !make_bshd_map(&mv, v, mb, mrows, s.Hk, D, C::TK))
     return FA_ERR_CUDA;
@@ -383,10 +472,13 @@ static int launch_decode_t(const AttnShape& s, const void* q, const void* k, con
   p.Sk = s.Sk;
   p.H = s.H;
   p.group = s.H / s.Hk;
-  p.block_table = pg ? pg->block_table : nullptr;
-  p.seqlens_k = pg ? pg->seqlens_k : nullptr;
-  p.page_size = pg ? pg->page_size : 0;
-  p.max_pages = pg ? pg->max_pages : 0;
+  p.block_table = cg ? cg->block_table : nullptr;
+  p.seqlens_k = cg ? cg->seqlens : nullptr;
+  p.page_size = cg ? cg->page_size : 0;
+  p.max_pages = cg ? cg->max_pages : 0;
+  p.s_new = cg ? cg->s_new : 0;
+  p.cap = cg ? cg->cap : s.Sk;
+  p.rot = cg ? cg->rot : Rotary{nullptr, nullptr, 0, 0, 0};
   p.n_splits = n;
   p.wl = s.wl;
   p.wr = s.wr;
@@ -404,7 +496,7 @@ static int launch_decode_t(const AttnShape& s, const void* q, const void* k, con
 }
 
 int decode_launch(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,
-                  void* workspace, int n, const PagedArgs* paged, cudaStream_t stream) {
+                  void* workspace, int n, const CacheArgs* paged, cudaStream_t stream) {
   switch (s.D) {
     case 64:
       return launch_decode_t<64>(s, q, k, v, out, lse, workspace, n, paged, stream);

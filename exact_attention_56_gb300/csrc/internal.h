@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "rotary.cuh"
+
 namespace fa {
 
 // Arguments common to every attention entry point, after validation.
@@ -26,12 +28,17 @@ struct VarlenArgs {
   int total_q, total_k;
 };
 
-// Paged KV cache for decode: caches (num_pages, page_size, Hk, D); key block p
-// of sequence b is page block_table[b * max_pages + p]; seqlens_k[b] keys.
-struct PagedArgs {
+// Decode over a cache with per-sequence lengths: dense (B, cap, Hk, D) caches
+// (block_table NULL) or pages (num_pages, page_size, Hk, D), key block p of
+// sequence b in page block_table[b * max_pages + p]. Sequence b has
+// min(seqlens[b] + s_new, cap) keys, the last s_new appended in this call.
+// rot: rotary embedding of q (and of the appended keys); rot.cos NULL for none.
+struct CacheArgs {
   const int* block_table;
-  const int* seqlens_k;
+  const int* seqlens;
   int num_pages, page_size, max_pages;
+  int s_new, cap;
+  Rotary rot;
 };
 
 // Status word of the current device (device pointer), or NULL on failure.
@@ -49,7 +56,11 @@ bool make_bshd_map(CUtensorMap* map, const void* base, int B, int S, int H, int 
 int fwd_launch(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,
                const VarlenArgs* varlen, cudaStream_t stream);
 int decode_launch(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,
-                  void* workspace, int num_splits, const PagedArgs* paged, cudaStream_t stream);
+                  void* workspace, int num_splits, const CacheArgs* cache, cudaStream_t stream);
+// Writes the s_new rows of k_new, v_new (B, s_new, Hk, D) into the cache behind
+// seqlens[b], the keys rotated (cache.rot); run before decode_launch.
+int kv_append_launch(const AttnShape& s, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                     const CacheArgs& cache, cudaStream_t stream);
 size_t decode_workspace_bytes(int B, int Sq, int H, int D, int num_splits);
 int decode_auto_splits(int B, int Sq, int Sk, int H, int Hk, int D);
 int bwd_launch(const AttnShape& s, const void* dout, const void* q, const void* k, const void* v,

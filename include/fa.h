@@ -196,6 +196,39 @@ int fa_decode_paged(const void* q, const void* k_pages, const void* v_pages, con
                     int alibi_batch_stride, int num_splits, fa_stream_t stream);
 
 /*
+ * Decode step on a KV cache, appending new keys/values in place and applying
+ * rotary embeddings first (section "2.2：针对推理进行优化": flash_attn_with_kvcache
+ * "performs rotary embedding and updates the KV cache in place"; the pages give
+ * no formula, the standard rotary embedding is the reading taken).
+ * Cache: dense k_cache, v_cache (B, cache_rows, Hk, D) when block_table is
+ * NULL, else pages (num_pages, page_size, Hk, D) addressed as in
+ * fa_decode_paged. cache_seqlens (B,) DEVICE int32: keys already cached.
+ * 1. If S_new > 0, rows s of k_new, v_new (B, S_new, Hk, D) are written to
+ *    cache position cache_seqlens[b] + s, the keys rotated at that position.
+ *    Rows past the cache's capacity (cache_rows, or max_pages_per_seq *
+ *    page_size) or on a page index outside [0, num_pages) are not written.
+ *    cache_seqlens itself is not updated.
+ * 2. Query row i of sequence b is rotated at its diagonal position
+ *    i + Sk_b - Sq, Sk_b = min(cache_seqlens[b] + S_new, capacity), and
+ *    attends the sequence's Sk_b keys as fa_decode_splitkv does.
+ * Rotary (rotary_cos == NULL: none): rotary_cos, rotary_sin (rotary_len,
+ * rotary_dim / 2) fp32 on the device; the pair (x1, x2) at frequency f and
+ * position t becomes (x1 cos - x2 sin, x1 sin + x2 cos), cos = cos[t][f],
+ * pairs (2f, 2f+1) if rotary_interleaved else (f, f + rotary_dim/2); elements
+ * at or beyond rotary_dim are unchanged; positions are clamped to
+ * [0, rotary_len - 1]. rotary_dim: a multiple of 16, at most D.
+ * q, out, lse, masks, ALiBi, num_splits and the workspace
+ * (fa_decode_workspace_size with Sk = the capacity) as fa_decode_splitkv.
+ */
+int fa_decode_kvcache(const void* q, void* k_cache, void* v_cache, const int* cache_seqlens, const void* k_new,
+                      const void* v_new, int S_new, const float* rotary_cos, const float* rotary_sin, int rotary_dim,
+                      int rotary_len, int rotary_interleaved, const int* block_table, int num_pages, int page_size,
+                      int max_pages_per_seq, void* out, float* lse, void* workspace, size_t workspace_bytes, int B,
+                      int Sq, int cache_rows, int H, int Hk, int D, float scale, int causal, int window_left,
+                      int window_right, const float* alibi_slopes, int alibi_batch_stride, int num_splits,
+                      fa_stream_t stream);
+
+/*
  * Split-KV decode that allocates nothing and takes no workspace. The pages
  * have no counterpart to this entry point; it exists for callers that cannot
  * allocate device memory where they run decode (an allocation-free serving

@@ -28,4 +28,7 @@ from .attention import (  # noqa: F401
     attention_fwd_varlen,
     attention_bwd_varlen,
     decode_paged,
+    rotary,
+    round_bf16,
+    decode_kvcache,
 )

@@ -38,6 +38,16 @@ Definitions used (the page's notation where it has one):
   taken here: caches of pages (num_pages, page_size, Hk, D); key block p of
   sequence b (keys p*page_size ..) is page block_table[b, p]; the sequence has
   seqlens_k[b] keys, and decode attends them as the dense forward would.
+* KV-cache decode with in-place append and rotary embedding (section "2.2",
+  flash_attn_with_kvcache "performs rotary embedding and updates the KV cache
+  in place"; no formula is given). Readings taken here: new rows go to
+  positions cache_seqlens[b] + s; the rotary embedding is the standard one,
+  each pair (x1, x2) at frequency f and position t rotated by the caller's
+  table angle, (x1 cos - x2 sin, x1 sin + x2 cos), pairs (2f, 2f+1) when
+  interleaved else (f, f + r/2); new keys rotate at their cache positions and
+  query row i at its diagonal position i + Sk - Sq. The cache holds bf16, so a
+  key written into it is the rotated key rounded to bf16 (nearest, ties to
+  even); values are copied unchanged.
 * Key/value heads (section "代码解读博客：FlashCrossAttention", kv of shape
   (B, Sk, 2, H_k, D)): k and v may have Hk heads with H a multiple of Hk.
   Reading taken here (the page gives no mapping): query head h attends
@@ -382,3 +392,86 @@ def decode_paged(q, k_pages, v_pages, block_table, seqlens_k, scale=None, causal
         ob, lb = attention_fwd(q[b:b + 1], kb[None], vb[None], scale, causal, window, slopes)
         o[b], lse[b] = ob[0], lb[0]
     return o, lse
+
+
+def round_bf16(x):
+    """Round to the nearest bfloat16 (ties to even), returned as float64: x goes through
+    fp32, whose upper 16 bits are kept after adding half of the dropped range."""
+    f = np.ascontiguousarray(np.asarray(x, dtype=np.float64).astype(np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def rotary(x, positions, cos_tab, sin_tab, interleaved=False):
+    """Rotate rows x (n, ..., D) at positions (n,) with tables (len, r/2); dims >= r unchanged.
+    Positions are clamped into the tables."""
+    x = np.array(x, dtype=np.float64, copy=True)
+    cos_tab = np.asarray(cos_tab, dtype=np.float64)
+    sin_tab = np.asarray(sin_tab, dtype=np.float64)
+    half = cos_tab.shape[1]
+    for n, t in enumerate(positions):
+        t = min(max(int(t), 0), cos_tab.shape[0] - 1)
+        for f in range(half):
+            i1, i2 = (2 * f, 2 * f + 1) if interleaved else (f, f + half)
+            c, s_ = cos_tab[t, f], sin_tab[t, f]
+            x1, x2 = x[n, ..., i1].copy(), x[n, ..., i2].copy()
+            x[n, ..., i1] = x1 * c - x2 * s_
+            x[n, ..., i2] = x1 * s_ + x2 * c
+    return x
+
+
+def decode_kvcache(q, k_cache, v_cache, cache_seqlens, k_new=None, v_new=None, rotary_cos=None, rotary_sin=None,
+                   interleaved=False, block_table=None, scale=None, causal=False, window=(-1, -1),
+                   alibi_slopes=None):
+    """Decode step on a cache: returns O (B,Sq,H,D), L (B,H,Sq) and the caches after the append (fp64).
+    Dense caches are (B, rows, Hk, D); with block_table (B, max_pages) they are pages
+    (num_pages, page_size, Hk, D). Rows past the capacity or on a page outside the cache are not written."""
+    q = np.asarray(q, dtype=np.float64)
+    kc = np.array(k_cache, dtype=np.float64, copy=True)
+    vc = np.array(v_cache, dtype=np.float64, copy=True)
+    B, Sq, H, D = q.shape
+    seq = [int(x) for x in np.asarray(cache_seqlens)]
+    rot = rotary_cos is not None
+    if block_table is not None:
+        table = np.asarray(block_table)
+        page_size = kc.shape[1]
+        cap = table.shape[1] * page_size
+
+        def slot(b, pos):
+            page = int(table[b, pos // page_size])
+            return None if not 0 <= page < kc.shape[0] else (page, pos % page_size)
+    else:
+        cap = kc.shape[1]
+
+        def slot(b, pos):
+            return (b, pos)
+    S_new = 0 if k_new is None else k_new.shape[1]
+    for b in range(B):
+        for s_ in range(S_new):
+            pos = seq[b] + s_
+            if not 0 <= pos < cap:
+                continue
+            where = slot(b, pos)
+            if where is None:
+                continue
+            kr = np.asarray(k_new[b, s_:s_ + 1], dtype=np.float64)
+            if rot:
+                kr = round_bf16(rotary(kr, [pos], rotary_cos, rotary_sin, interleaved))
+            kc[where] = kr[0]
+            vc[where] = np.asarray(v_new[b, s_], dtype=np.float64)
+    o = np.zeros_like(q)
+    lse = np.full((B, H, Sq), -np.inf)
+    for b in range(B):
+        n = max(0, min(seq[b] + S_new, cap))
+        if n == 0:
+            continue
+        kb = np.stack([kc[slot(b, j)] if slot(b, j) is not None else np.zeros(kc.shape[2:]) for j in range(n)])
+        vb = np.stack([vc[slot(b, j)] if slot(b, j) is not None else np.zeros(vc.shape[2:]) for j in range(n)])
+        qb = q[b]
+        if rot:
+            qb = rotary(qb, [i + n - Sq for i in range(Sq)], rotary_cos, rotary_sin, interleaved)
+        slopes = None if alibi_slopes is None else _batch_slopes(alibi_slopes, b)
+        ob, lb = attention_fwd(qb[None], kb[None], vb[None], scale, causal, window, slopes)
+        o[b], lse[b] = ob[0], lb[0]
+    return o, lse, kc, vc
