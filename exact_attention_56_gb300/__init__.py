@@ -26,6 +26,8 @@ from ._native import (  # noqa: F401
     fa_bwd_workspace_size,
     fa_fwd_varlen,
     fa_bwd_varlen,
+    fa_fwd_dropout,
+    fa_bwd_dropout,
     fa_bwd_varlen_workspace_size,
     fa_decode_splitkv,
     fa_decode_paged,
@@ -47,6 +49,8 @@ __all__ = [
     "fa_bwd",
     "fa_bwd_workspace_size",
     "fa_fwd_varlen",
+    "fa_fwd_dropout",
+    "fa_bwd_dropout",
     "fa_bwd_varlen",
     "fa_bwd_varlen_workspace_size",
     "fa_decode_splitkv",

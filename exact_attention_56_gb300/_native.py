@@ -52,6 +52,10 @@ _SIGS = {
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _I,
                                _I, _P]),
     "fa_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
+    "fa_fwd_dropout": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _I, _F, ctypes.c_uint64,
+                            ctypes.c_uint32, _P]),
+    "fa_bwd_dropout": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P,
+                            _I, _I, _F, ctypes.c_uint64, ctypes.c_uint32, _P]),
     "fa_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
                              _I, _P, _I, _I, _P]),
     "fa_decode_kvcache": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _SZ,
@@ -430,6 +434,61 @@ def fa_decode_kvcache(q, k_cache, v_cache, cache_seqlens, k_new=None, v_new=None
         _ptr(al), al_stride, int(num_splits), _stream_ptr(stream, dev))
     _check("fa_decode_kvcache", st)
     return out, lse
+
+
+def fa_fwd_dropout(q, k, v, dropout_p, seed, offset=0, *, softmax_scale=None, causal=False, window_size=(-1, -1),
+                   alibi_slopes=None, out=None, lse=None, stream=None):
+    """fa_fwd with dropout on the probabilities (Philox4x32-10 mask from seed, offset; see include/fa.h)."""
+    _need(q, "q", torch.bfloat16)
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    Hk = _kv_heads(k, H)
+    dev = q.device
+    _need(k, "k", torch.bfloat16, (B, Sk, Hk, D), dev)
+    _need(v, "v", torch.bfloat16, (B, Sk, Hk, D), dev)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, (B, Sq, H, D), dev)
+    _need(lse, "lse", torch.float32, (B, H, Sq), dev)
+    al, al_stride = _alibi(alibi_slopes, B, H, dev)
+    st = library().fa_fwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Sq, Sk, H, Hk, D,
+                                  _scale(softmax_scale, D), int(bool(causal)), int(window_size[0]),
+                                  int(window_size[1]), _ptr(al), al_stride, float(dropout_p), int(seed), int(offset),
+                                  _stream_ptr(stream, dev))
+    _check("fa_fwd_dropout", st)
+    return out, lse
+
+
+def fa_bwd_dropout(dout, q, k, v, out, lse, dropout_p, seed, offset=0, *, softmax_scale=None, causal=False,
+                   window_size=(-1, -1), alibi_slopes=None, deterministic=False, dq=None, dk=None, dv=None,
+                   workspace=None, stream=None):
+    """Backward of fa_fwd_dropout with the same dropout_p, seed and offset."""
+    _need(q, "q", torch.bfloat16)
+    B, Sq, H, D = q.shape
+    Sk = k.shape[1]
+    Hk = _kv_heads(k, H)
+    dev = q.device
+    for name, t, shp in (("k", k, (B, Sk, Hk, D)), ("v", v, (B, Sk, Hk, D)), ("dout", dout, (B, Sq, H, D)),
+                         ("out", out, (B, Sq, H, D))):
+        _need(t, name, torch.bfloat16, shp, dev)
+    _need(lse, "lse", torch.float32, (B, H, Sq), dev)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = fa_bwd_workspace_size(B, Sq, Sk, H, D, deterministic, Hk=Hk)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, device=dev)
+    al, al_stride = _alibi(alibi_slopes, B, H, dev)
+    st = library().fa_bwd_dropout(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dq), _ptr(dk),
+                                  _ptr(dv), _ptr(workspace), workspace.numel(), B, Sq, Sk, H, Hk, D,
+                                  _scale(softmax_scale, D), int(bool(causal)), int(window_size[0]),
+                                  int(window_size[1]), _ptr(al), al_stride, int(bool(deterministic)),
+                                  float(dropout_p), int(seed), int(offset), _stream_ptr(stream, dev))
+    _check("fa_bwd_dropout", st)
+    return dq, dk, dv
 
 
 FA_SELFTEST_SITE = 0x7E

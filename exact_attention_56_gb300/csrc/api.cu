@@ -140,7 +140,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, i
                         alibi_batch_stride, &s);
   if (st != FA_OK) return st;
   if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
-  return fa::fwd_launch(s, q, k, v, out, lse, nullptr, reinterpret_cast<cudaStream_t>(stream));
+  return fa::fwd_launch(s, q, k, v, out, lse, nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fa_fwd_varlen(const void* q, const void* k, const void* v, void* out, float* lse, const int* cu_seqlens_q,
@@ -159,7 +159,57 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* out, float*
   if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
   if (total_q > (1 << 30) || total_k > (1 << 30)) return FA_ERR_UNSUPPORTED;
   const fa::VarlenArgs vl{cu_seqlens_q, cu_seqlens_k, total_q, total_k};
-  return fa::fwd_launch(s, q, k, v, out, lse, &vl, reinterpret_cast<cudaStream_t>(stream));
+  return fa::fwd_launch(s, q, k, v, out, lse, &vl, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Dropout rule shared by fa_fwd_dropout and fa_bwd_dropout; p in [0, 1).
+static bool make_dropout(float p, uint64_t seed, uint32_t offset, fa::Dropout* d) {
+  if (!(p >= 0.0f && p < 1.0f)) return false;
+  const double t = double(p) * 4294967296.0;
+  d->thr = t >= 4294967295.0 ? 4294967295u : uint32_t(t);
+  d->keep_scale = 1.0f / (1.0f - p);
+  d->seed_lo = uint32_t(seed);
+  d->seed_hi = uint32_t(seed >> 32);
+  d->offset = offset;
+  return true;
+}
+
+int fa_fwd_dropout(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Sq, int Sk, int H,
+                   int Hk, int D, float scale, int causal, int window_left, int window_right, const float* alibi_slopes,
+                   int alibi_batch_stride, float dropout_p, uint64_t seed, uint32_t offset, fa_stream_t stream) {
+  if (!q || !k || !v || !out || !lse) return FA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse)) return FA_ERR_INVALID;
+  AttnShape s;
+  int st = check_common(B, Sq, Sk, H, Hk, D, scale, causal, window_left, window_right, alibi_slopes,
+                        alibi_batch_stride, &s);
+  if (st != FA_OK) return st;
+  if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
+  fa::Dropout dr;
+  if (!make_dropout(dropout_p, seed, offset, &dr)) return FA_ERR_INVALID;
+  return fa::fwd_launch(s, q, k, v, out, lse, nullptr, &dr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fa_bwd_dropout(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,
+                   void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Sq, int Sk,
+                   int H, int Hk, int D, float scale, int causal, int window_left, int window_right,
+                   const float* alibi_slopes, int alibi_batch_stride, int deterministic, float dropout_p,
+                   uint64_t seed, uint32_t offset, fa_stream_t stream) {
+  if (!dout || !q || !k || !v || !out || !lse || !dq || !dk || !dv) return FA_ERR_INVALID;
+  if (!aligned16(dout) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_INVALID;
+  AttnShape s;
+  int st = check_common(B, Sq, Sk, H, Hk, D, scale, causal, window_left, window_right, alibi_slopes,
+                        alibi_batch_stride, &s);
+  if (st != FA_OK) return st;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  fa::Dropout dr;
+  if (!make_dropout(dropout_p, seed, offset, &dr)) return FA_ERR_INVALID;
+  const size_t need = fa::bwd_workspace_bytes(B, Sq, Sk, H, Hk, D, deterministic);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return FA_ERR_WORKSPACE;
+  return fa::bwd_launch(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, deterministic, nullptr, &dr,
+                        reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t fa_bwd_workspace_size(int B, int Sq, int Sk, int H, int Hk, int D, int deterministic) {
@@ -183,7 +233,7 @@ int fa_bwd(const void* dout, const void* q, const void* k, const void* v, const 
   const size_t need = fa::bwd_workspace_bytes(B, Sq, Sk, H, Hk, D, deterministic);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
     return FA_ERR_WORKSPACE;
-  return fa::bwd_launch(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, deterministic, nullptr,
+  return fa::bwd_launch(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, deterministic, nullptr, nullptr,
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -216,7 +266,7 @@ int fa_bwd_varlen(const void* dout, const void* q, const void* k, const void* v,
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
     return FA_ERR_WORKSPACE;
   const fa::VarlenArgs vl{cu_seqlens_q, cu_seqlens_k, total_q, total_k};
-  return fa::bwd_launch(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, deterministic, &vl,
+  return fa::bwd_launch(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, deterministic, &vl, nullptr,
                         reinterpret_cast<cudaStream_t>(stream));
 }
 

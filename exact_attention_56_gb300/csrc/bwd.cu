@@ -50,6 +50,7 @@
 
 #include "../../include/fa.h"
 #include "internal.h"
+#include "philox.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -80,6 +81,9 @@ struct BwdParams {
   const int* cu_q;
   const int* cu_k;
   int total_q, total_k;
+  // Dropout (DROP instances): the forward's keep flags; dV takes P o Z and
+  // dS = P o (Z o dP - D), Z the kept entries' 1 / (1 - p) (0 where dropped).
+  Dropout drop;
   int wl, wr;
   float scale;
   float scale_log2;
@@ -288,7 +292,7 @@ struct KvBars {
   int abort;
 };
 
-template <int D>
+template <int D, bool DROP>
 __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -573,9 +577,15 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
           const float4 d4 = dvv[c / 4];
           const float dv0 = (c % 4 == 0) ? d4.x : d4.z;
           const float dv1 = (c % 4 == 0) ? d4.y : d4.w;
+          float z0 = 1.0f, z1 = 1.0f;
+          if (DROP) {  // this key's flags for query rows ib + c and ib + c + 1
+            const int bh = b * p.H + hq;
+            z0 = (dropout_keep4(p.drop, bh, ib + c, j >> 2) >> (j & 3)) & 1u ? p.drop.keep_scale : 0.0f;
+            z1 = (dropout_keep4(p.drop, bh, ib + c + 1, j >> 2) >> (j & 3)) & 1u ? p.drop.keep_scale : 0.0f;
+          }
           float s0, s1;
-          ds_pair(pv[c], pv[c + 1], dp[2 * e], dp[2 * e + 1], dv0, dv1, s0, s1);
-          pp[e] = pack_f16x2(pv[c], pv[c + 1]);
+          ds_pair(pv[c], pv[c + 1], dp[2 * e] * z0, dp[2 * e + 1] * z1, dv0, dv1, s0, s1);
+          pp[e] = pack_f16x2(pv[c] * z0, pv[c + 1] * z1);
           ps[e] = pack_f16x2(s0, s1);
         }
         tmem_st_x8(col, pp);
@@ -659,7 +669,7 @@ struct DqBars {
   int abort;
 };
 
-template <int D>
+template <int D, bool DROP>
 __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -890,10 +900,19 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         const uint32_t col = tmem + lane_addr + C::T_DP + w * C::COLS + 16 * ch;
         tmem_ld_cols(col, dp);
         uint32_t pk[8];
+        uint32_t keep = 0;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
+          float z0 = 1.0f, z1 = 1.0f;
+          if (DROP) {  // keys kb + c .. : one generator call per four keys
+            const int c = 16 * ch + 2 * e;
+            if ((e & 1) == 0) keep = dropout_keep4(p.drop, b * p.H + h, i, (kb + c) >> 2);
+            z0 = (keep >> (c & 3)) & 1u ? p.drop.keep_scale : 0.0f;
+            z1 = (keep >> ((c & 3) + 1)) & 1u ? p.drop.keep_scale : 0.0f;
+          }
           float s0, s1;
-          ds_pair(pv[16 * ch + 2 * e], pv[16 * ch + 2 * e + 1], dp[2 * e], dp[2 * e + 1], dval, dval, s0, s1);
+          ds_pair(pv[16 * ch + 2 * e], pv[16 * ch + 2 * e + 1], dp[2 * e] * z0, dp[2 * e + 1] * z1, dval, dval, s0,
+                  s1);
           pk[e] = pack_f16x2(s0, s1);
         }
         tmem_st_x8(col, pk);
@@ -961,7 +980,7 @@ size_t bwd_varlen_workspace_bytes(int B, int total_q, int total_k, int max_sq, i
 template <int D>
 static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, const void* k, const void* v,
                         const void* out, const float* lse, void* dq, void* dk, void* dv, void* ws,
-                        const VarlenArgs* vl, cudaStream_t stream) {
+                        const VarlenArgs* vl, const Dropout* dr, cudaStream_t stream) {
   BwdParams p;
   p.B = s.B;
   p.Sq = s.Sq;
@@ -975,6 +994,8 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
   p.cu_k = vl ? vl->cu_k : nullptr;
   p.total_q = vl ? vl->total_q : 0;
   p.total_k = vl ? vl->total_k : 0;
+  p.drop = dr ? *dr : Dropout{0, 1.0f, 0, 0, 0};
+  const bool drop = p.drop.thr != 0;
   const long long rows_q = vl ? vl->total_q : (long long)s.B * s.Sq;
   const long long rows_k = vl ? vl->total_k : (long long)s.B * s.Sk;
   const BwdWs L = bwd_ws(s.B, s.Sq, rows_q, rows_k, s.H, s.Hk, D);
@@ -1023,12 +1044,12 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
     fa_bwd_pre_kernel<D><<<grid, 256, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   }
-  auto kv = fa_bwd_dkdv_kernel<D>;
+  auto kv = drop ? fa_bwd_dkdv_kernel<D, true> : fa_bwd_dkdv_kernel<D, false>;
   if (cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, KvCfg<D>::SMEM_BYTES) != cudaSuccess)
     return FA_ERR_CUDA;
   kv<<<dim3((s.Sk + 127) / 128, s.Hk, s.B), KvCfg<D>::THREADS, KvCfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  auto dqk = fa_bwd_dq_kernel<D>;
+  auto dqk = drop ? fa_bwd_dq_kernel<D, true> : fa_bwd_dq_kernel<D, false>;
   if (cudaFuncSetAttribute(dqk, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::SMEM_BYTES) != cudaSuccess)
     return FA_ERR_CUDA;
   dqk<<<dim3(p.n_qt, s.H, s.B), DqCfg<D>::THREADS, DqCfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
@@ -1037,13 +1058,13 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
 
 int bwd_launch(const AttnShape& s, const void* dout, const void* q, const void* k, const void* v, const void* out,
                const float* lse, void* dq, void* dk, void* dv, void* workspace, int deterministic,
-               const VarlenArgs* varlen, cudaStream_t stream) {
+               const VarlenArgs* varlen, const Dropout* dropout, cudaStream_t stream) {
   (void)deterministic;
   switch (s.D) {
     case 64:
-      return launch_bwd_t<64>(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, varlen, stream);
+      return launch_bwd_t<64>(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, varlen, dropout, stream);
     case 128:
-      return launch_bwd_t<128>(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, varlen, stream);
+      return launch_bwd_t<128>(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, varlen, dropout, stream);
     default:
       return FA_ERR_UNSUPPORTED;
   }

@@ -25,6 +25,7 @@
 
 #include "../../include/fa.h"
 #include "internal.h"
+#include "philox.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -43,6 +44,7 @@ struct FwdParams {
   const int* cu_q;
   const int* cu_k;
   int total_q;
+  Dropout drop;  // used by the DROP instances only
   int wl, wr;
   float scale_log2;  // softmax scale * log2(e)
   unsigned int* status;
@@ -99,7 +101,9 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 
 // VARLEN: packed sequences (cu_q, cu_k set); a separate instance, so the padded
 // layout keeps its lengths in kernel parameters rather than registers.
-template <int D, int NT, bool VARLEN>
+// DROP: dropout on the probabilities that multiply V (the row sums use the
+// undropped ones, so L is unchanged).
+template <int D, int NT, bool VARLEN, bool DROP>
 __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -367,13 +371,20 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t pk[16];
+        uint32_t keep = 0;
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int c = q4 * 32 + 2 * e;
-          const float p0 = ex2_approx(fmaf(x[c], mul, -m_use));
-          const float p1 = ex2_approx(fmaf(x[c + 1], mul, -m_use));
+          float p0 = ex2_approx(fmaf(x[c], mul, -m_use));
+          float p1 = ex2_approx(fmaf(x[c + 1], mul, -m_use));
           rs[(e & 1) * 2] += p0;
           rs[(e & 1) * 2 + 1] += p1;
+          if (DROP) {
+            if ((e & 1) == 0) keep = dropout_keep4(p.drop, b * p.H + h, i, (kbase + c) >> 2);
+            const int sh = (c & 3);
+            p0 = (keep >> sh) & 1u ? p0 * p.drop.keep_scale : 0.0f;
+            p1 = (keep >> (sh + 1)) & 1u ? p1 * p.drop.keep_scale : 0.0f;
+          }
           pk[e] = pack_bf16x2(p0, p1);
         }
         tmem_st_x16(tmem + lane_addr + sb * 128 + q4 * 16, pk);
@@ -447,9 +458,12 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
 
 template <int D, int NT>
 static int launch_fwd_t(const AttnShape& s, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                        void* out, float* lse, const VarlenArgs* vl, cudaStream_t stream) {
+                        void* out, float* lse, const VarlenArgs* vl, const Dropout* dr, cudaStream_t stream) {
   using C = FwdCfg<D, NT>;
-  auto kern = vl ? fa_fwd_kernel<D, NT, true> : fa_fwd_kernel<D, NT, false>;
+  const bool drop = dr && dr->thr != 0;
+  if (vl && drop) return FA_ERR_UNSUPPORTED;  // dropout is built for the padded layout
+  auto kern = vl ? fa_fwd_kernel<D, NT, true, false>
+                 : (drop ? fa_fwd_kernel<D, NT, false, true> : fa_fwd_kernel<D, NT, false, false>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
     return FA_ERR_CUDA;
   FwdParams p;
@@ -465,6 +479,7 @@ static int launch_fwd_t(const AttnShape& s, const CUtensorMap& mq, const CUtenso
   p.cu_q = vl ? vl->cu_q : nullptr;
   p.cu_k = vl ? vl->cu_k : nullptr;
   p.total_q = vl ? vl->total_q : 0;
+  p.drop = dr ? *dr : Dropout{0, 1.0f, 0, 0, 0};
   p.wl = s.wl;
   p.wr = s.wr;
   p.scale_log2 = s.scale * 1.4426950408889634f;
@@ -476,7 +491,7 @@ static int launch_fwd_t(const AttnShape& s, const CUtensorMap& mq, const CUtenso
 }
 
 int fwd_launch(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,
-               const VarlenArgs* vl, cudaStream_t stream) {
+               const VarlenArgs* vl, const Dropout* dr, cudaStream_t stream) {
   if (s.B > 65535 || s.H > 65535) return FA_ERR_UNSUPPORTED;
   // Packed sequences are one (1, total, H, D) tensor; s.Sq, s.Sk are then the longest lengths.
   const int mb = vl ? 1 : s.B;
@@ -487,11 +502,11 @@ int fwd_launch(const AttnShape& s, const void* q, const void* k, const void* v, 
     return FA_ERR_CUDA;
   switch (s.D) {
     case 64:
-      return launch_fwd_t<64, 2>(s, mq, mk, mv, out, lse, vl, stream);
+      return launch_fwd_t<64, 2>(s, mq, mk, mv, out, lse, vl, dr, stream);
     case 128:
-      return launch_fwd_t<128, 2>(s, mq, mk, mv, out, lse, vl, stream);
+      return launch_fwd_t<128, 2>(s, mq, mk, mv, out, lse, vl, dr, stream);
     case 256:
-      return launch_fwd_t<256, 1>(s, mq, mk, mv, out, lse, vl, stream);
+      return launch_fwd_t<256, 1>(s, mq, mk, mv, out, lse, vl, dr, stream);
     default:
       return FA_ERR_UNSUPPORTED;
   }

@@ -5,6 +5,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "philox.cuh"
 #include "rotary.cuh"
 
 namespace fa {
@@ -54,7 +55,7 @@ bool make_bshd_map(CUtensorMap* map, const void* base, int B, int S, int H, int 
 
 // Kernel launchers (return an fa_status value).
 int fwd_launch(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,
-               const VarlenArgs* varlen, cudaStream_t stream);
+               const VarlenArgs* varlen, const Dropout* dropout, cudaStream_t stream);
 int decode_launch(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,
                   void* workspace, int num_splits, const CacheArgs* cache, cudaStream_t stream);
 // Writes the s_new rows of k_new, v_new (B, s_new, Hk, D) into the cache behind
@@ -65,7 +66,7 @@ size_t decode_workspace_bytes(int B, int Sq, int H, int D, int num_splits);
 int decode_auto_splits(int B, int Sq, int Sk, int H, int Hk, int D);
 int bwd_launch(const AttnShape& s, const void* dout, const void* q, const void* k, const void* v,
                const void* out, const float* lse, void* dq, void* dk, void* dv, void* workspace,
-               int deterministic, const VarlenArgs* varlen, cudaStream_t stream);
+               int deterministic, const VarlenArgs* varlen, const Dropout* dropout, cudaStream_t stream);
 size_t bwd_varlen_workspace_bytes(int B, int total_q, int total_k, int max_sq, int H, int Hk, int D);
 size_t bwd_workspace_bytes(int B, int Sq, int Sk, int H, int Hk, int D, int deterministic);
 

@@ -84,6 +84,32 @@ int fa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, i
            int alibi_batch_stride, fa_stream_t stream);
 
 /*
+ * Forward with dropout on the attention probabilities (section "参数说明":
+ * dropout_p). The pages give no random generator; the one used here is
+ * Philox4x32-10 (Salmon et al., "Parallel random numbers: as easy as 1, 2, 3",
+ * SC 2011). Entry (b, h, i, j) of the probability matrix P uses word j % 4 of
+ * Philox4x32-10(counter = (j / 4, i, b * H + h, offset), key = (seed & 0xffffffff,
+ * seed >> 32)); it is dropped when that word is below floor(dropout_p * 2^32)
+ * and otherwise scaled by 1 / (1 - dropout_p). out = (P o Z) V; lse is that of
+ * the undropped scores, as in fa_fwd. Same seed and offset give the same
+ * mask in fa_bwd_dropout. Arguments otherwise as fa_fwd; 0 <= dropout_p < 1.
+ */
+int fa_fwd_dropout(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Sq, int Sk, int H,
+                   int Hk, int D, float scale, int causal, int window_left, int window_right, const float* alibi_slopes,
+                   int alibi_batch_stride, float dropout_p, uint64_t seed, uint32_t offset, fa_stream_t stream);
+
+/*
+ * Backward of fa_fwd_dropout with the same dropout_p, seed and offset:
+ * dV = (P o Z)^T dO, dS = P o (Z o dO V^T - D), D_i = rowsum(dO o O),
+ * dQ = scale dS K, dK = scale dS^T Q. Arguments otherwise as fa_bwd.
+ */
+int fa_bwd_dropout(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,
+                   void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int Sq, int Sk,
+                   int H, int Hk, int D, float scale, int causal, int window_left, int window_right,
+                   const float* alibi_slopes, int alibi_batch_stride, int deterministic, float dropout_p,
+                   uint64_t seed, uint32_t offset, fa_stream_t stream);
+
+/*
  * Forward over packed sequences of different lengths (page section
  * "代码解读博客：FlashSelfAttention": cu_seqlens, max_seqlen; the page's
  * flash_attn_varlen_func, section "函数重命名"). Sequence b has query rows

@@ -13,6 +13,10 @@ section names below refer to that page.
 Parity status: every function here is pinned by tests under
 ``tests/test_oracle_*.py`` (worked mask examples, closed forms,
 invariants, an independent library routine and finite differences).
+One partial exception: the dropout generator ``philox4x32_10`` is pinned in
+structure (independently inverted rounds) and statistics, but not against
+published known-answer vectors, so its constants rest on the published
+definition as written here (parity partially pinned).
 """
 from .attention import (  # noqa: F401
     live_mask,
@@ -31,4 +35,9 @@ from .attention import (  # noqa: F401
     rotary,
     round_bf16,
     decode_kvcache,
+    philox4x32_10,
+    dropout_threshold,
+    dropout_scale_matrix,
+    attention_fwd_dropout,
+    attention_bwd_dropout,
 )

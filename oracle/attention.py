@@ -48,6 +48,11 @@ Definitions used (the page's notation where it has one):
   query row i at its diagonal position i + Sk - Sq. The cache holds bf16, so a
   key written into it is the rotated key rounded to bf16 (nearest, ties to
   even); values are copied unchanged.
+* Dropout (section "参数说明": dropout_p; no generator is given). Reading taken
+  here: Philox4x32-10 (Salmon et al., SC 2011) draws entry (b, h, i, j) of P as
+  word j % 4 of the block at counter (j // 4, i, b * H + h, offset), key = the
+  two 32-bit halves of the seed; the entry is dropped when the word is below
+  floor(p * 2^32), else scaled by 1 / (1 - p). O = (P o Z) V with L unchanged.
 * Key/value heads (section "代码解读博客：FlashCrossAttention", kv of shape
   (B, Sk, 2, H_k, D)): k and v may have Hk heads with H a multiple of Hk.
   Reading taken here (the page gives no mapping): query head h attends
@@ -475,3 +480,95 @@ def decode_kvcache(q, k_cache, v_cache, cache_seqlens, k_new=None, v_new=None, r
         ob, lb = attention_fwd(qb[None], kb[None], vb[None], scale, causal, window, slopes)
         o[b], lse[b] = ob[0], lb[0]
     return o, lse, kc, vc
+
+
+PHILOX_M0, PHILOX_M1 = 0xD2511F53, 0xCD9E8D57   # Philox4x32 multipliers (Salmon et al., SC 2011)
+PHILOX_W0, PHILOX_W1 = 0x9E3779B9, 0xBB67AE85   # key increments between rounds
+
+
+def philox4x32_10(x0, x1, x2, x3, k0, k1):
+    """Philox4x32 with 10 rounds on arrays of 32-bit counters; returns the four output words (uint64 arrays
+    holding 32-bit values). One round: hi0:lo0 = M0*x0, hi1:lo1 = M1*x2, then
+    (x0, x1, x2, x3) <- (hi1 ^ x1 ^ k0, lo1, hi0 ^ x3 ^ k1, lo0), then the key is bumped."""
+    mask = np.uint64(0xFFFFFFFF)
+    x = [np.asarray(t, dtype=np.uint64) & mask for t in (x0, x1, x2, x3)]
+    k0 = np.uint64(int(k0) & 0xFFFFFFFF)
+    k1 = np.uint64(int(k1) & 0xFFFFFFFF)
+    for _ in range(10):
+        p0 = np.uint64(PHILOX_M0) * x[0]
+        p1 = np.uint64(PHILOX_M1) * x[2]
+        hi0, lo0 = p0 >> np.uint64(32), p0 & mask
+        hi1, lo1 = p1 >> np.uint64(32), p1 & mask
+        x = [hi1 ^ x[1] ^ k0, lo1, hi0 ^ x[3] ^ k1, lo0]
+        k0 = (k0 + np.uint64(PHILOX_W0)) & mask
+        k1 = (k1 + np.uint64(PHILOX_W1)) & mask
+    return x
+
+
+def dropout_threshold(p):
+    """Words below this are dropped: floor(p * 2^32) with p taken as fp32, at most 2^32 - 1."""
+    t = int(math.floor(float(np.float32(p)) * 4294967296.0))
+    return min(t, 0xFFFFFFFF)
+
+
+def dropout_scale_matrix(Sq, Sk, bh, p, seed, offset):
+    """Z (Sq, Sk): 1 / (1 - p) where entry (i, j) of head bh = b * H + h is kept, else 0."""
+    nj4 = (Sk + 3) // 4
+    j4, i = np.meshgrid(np.arange(nj4), np.arange(Sq))
+    words = philox4x32_10(j4.ravel(), i.ravel(), np.full(j4.size, bh), np.full(j4.size, offset),
+                          int(seed) & 0xFFFFFFFF, int(seed) >> 32)
+    w = np.stack(words, axis=-1).reshape(Sq, nj4 * 4)[:, :Sk]
+    keep = w >= np.uint64(dropout_threshold(p))
+    return np.where(keep, 1.0 / (1.0 - float(np.float32(p))), 0.0)
+
+
+def attention_fwd_dropout(q, k, v, p, seed, offset=0, scale=None, causal=False, window=(-1, -1), alibi_slopes=None):
+    """Forward with dropout: O = (P o Z) V per (b, h), L as attention_fwd. Layouts as attention_fwd."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, Sq, H, D = q.shape
+    Sk, Hk = k.shape[1], k.shape[2]
+    sc = _default_scale(D, scale)
+    o = np.zeros_like(q)
+    lse = np.zeros((B, H, Sq))
+    for b in range(B):
+        for h in range(H):
+            g = kv_head(h, H, Hk)
+            s_, _ = _scores(q[b, :, h, :], k[b, :, g, :], sc, causal, window[0], window[1],
+                            _slope_for(alibi_slopes, b, h))
+            prob, lse[b, h] = _softmax_rows(s_)
+            z = dropout_scale_matrix(Sq, Sk, b * H + h, p, seed, offset)
+            o[b, :, h, :] = (prob * z) @ v[b, :, g, :]
+    return o, lse
+
+
+def attention_bwd_dropout(dout, q, k, v, p, seed, offset=0, scale=None, causal=False, window=(-1, -1),
+                          alibi_slopes=None):
+    """Backward with dropout: dV = (P o Z)^T dO, dP = Z o (dO V^T), D_i = sum_j P_ij dP_ij,
+    dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q (summed over a key/value head's query heads)."""
+    dout = np.asarray(dout, dtype=np.float64)
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, Sq, H, D = q.shape
+    Sk, Hk = k.shape[1], k.shape[2]
+    sc = _default_scale(D, scale)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            g = kv_head(h, H, Hk)
+            s_, _ = _scores(q[b, :, h, :], k[b, :, g, :], sc, causal, window[0], window[1],
+                            _slope_for(alibi_slopes, b, h))
+            prob, _ = _softmax_rows(s_)
+            z = dropout_scale_matrix(Sq, Sk, b * H + h, p, seed, offset)
+            do_h = dout[b, :, h, :]
+            dv[b, :, g, :] += (prob * z).T @ do_h
+            dp = z * (do_h @ v[b, :, g, :].T)
+            dvec = np.sum(prob * dp, axis=1, keepdims=True)
+            ds = prob * (dp - dvec)
+            dq[b, :, h, :] = sc * ds @ k[b, :, g, :]
+            dk[b, :, g, :] += sc * ds.T @ q[b, :, h, :]
+    return dq, dk, dv
