@@ -12,6 +12,9 @@ constexpr unsigned int FA_DEV_SITE_MASK = 0x0000FFFFu;
 // A legitimate wait inside these kernels lasts microseconds; one second
 // means a lost arrival, after which the kernel leaves instead of hanging.
 constexpr uint64_t FA_WAIT_TIMEOUT_NS = 1000000000ull;
+// Longest single sleep of a waiting thread before it re-checks the abort flag
+// and the watchdog; the thread wakes earlier when the awaited phase completes.
+constexpr uint32_t FA_WAIT_SLEEP_NS = 2000u;
 
 // Live key interval of query row i (page "FlashAttention：快速且内存高效的准确注意力机制",
 // sections "2.1" and "2.3"): the diagonal key is c(i) = i + Sk - Sq (bottom-right

@@ -56,6 +56,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread is suspended until the phase
+// completes or about `ns` nanoseconds pass, whichever comes first.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar_addr, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Per-CTA watchdog state: a shared abort flag plus the global status word.
 struct Watch {
   volatile int* abort;   // shared memory, 0 = running
@@ -69,15 +83,16 @@ __device__ __forceinline__ bool fa_wait(uint64_t* bar, uint32_t parity, const Wa
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(a, parity)) return true;
-    if ((it & 15u) == 0) {
-      if (*w.abort) return false;
-      if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) {
-        *w.abort = 1;
-        atomicOr(w.status, FA_DEV_TIMEOUT | (where & FA_DEV_SITE_MASK));
-        return false;
-      }
+  for (;;) {
+    // Sleeps until the phase completes (or FA_WAIT_SLEEP_NS pass) instead of
+    // polling, so waiting warps leave their scheduler's issue slots to the
+    // warps sharing it (the MMA issuer shares one with compute warps).
+    if (mbar_try_wait_sleep(a, parity, FA_WAIT_SLEEP_NS)) return true;
+    if (*w.abort) return false;
+    if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) {
+      *w.abort = 1;
+      atomicOr(w.status, FA_DEV_TIMEOUT | (where & FA_DEV_SITE_MASK));
+      return false;
     }
   }
 }
