@@ -404,7 +404,8 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     // Descriptors are built once; each k-step and stage is a constant added to
     // the start-address field, so issuing keeps pace with the tensor pipe.
-    if (lane == 0 && n_iter > 0) {
+    // The whole warp runs the loop; one elected lane issues each MMA and commit.
+    if (n_iter > 0) {
       constexpr uint32_t ID_SS = idesc_f16_f32(128, 128, 0, 0);  // S^T, dP^T: both operands K-major
       constexpr uint32_t ID_TN = idesc_f16_f32(128, D, 0, 1);    // dV, dK: A from TMEM, B (dO / Q) MN-major
       const uint64_t k_desc = sdesc_sw128(smem_u32(smem + C::K_OFF), 16, 1024);
@@ -414,24 +415,24 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
       const uint64_t q_mdesc = sdesc_sw128(smem_u32(smem + C::Q_OFF), C::PANEL_BYTES, 1024);    // MN-major (dK)
       const uint64_t do_mdesc = sdesc_sw128(smem_u32(smem + C::DO_OFF), C::PANEL_BYTES, 1024);  // MN-major (dV)
       const uint32_t t_s = tmem + C::T_S, t_dp = tmem + C::T_DP, t_dv = tmem + C::T_DV, t_dk = tmem + C::T_DK;
-      bool ok = fa_wait(&bars->kv_full, 0, watch, SITE_KV_KV) && fa_wait(&bars->q_full[0], 0, watch, SITE_KV_QFULL);
+      bool ok = fa_wait_warp(&bars->kv_full, 0, watch, SITE_KV_KV) && fa_wait_warp(&bars->q_full[0], 0, watch, SITE_KV_QFULL);
       if (ok) {  // S^T(0) = K Q^T
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
-          mma_ss(t_s, sdesc_adv(k_desc, off), sdesc_adv(q_kdesc, off), ID_SS, kk > 0 ? 1u : 0u);
+          mma_ss_w(t_s, sdesc_adv(k_desc, off), sdesc_adv(q_kdesc, off), ID_SS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bars->s_full);
+        mma_commit_w(&bars->s_full);
       }
-      if (ok && (ok = fa_wait(&bars->do_full[0], 0, watch, SITE_KV_DOFULL))) {  // dP^T(0) = V dO^T
+      if (ok && (ok = fa_wait_warp(&bars->do_full[0], 0, watch, SITE_KV_DOFULL))) {  // dP^T(0) = V dO^T
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
-          mma_ss(t_dp, sdesc_adv(v_desc, off), sdesc_adv(do_kdesc, off), ID_SS, kk > 0 ? 1u : 0u);
+          mma_ss_w(t_dp, sdesc_adv(v_desc, off), sdesc_adv(do_kdesc, off), ID_SS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bars->dp_full);
+        mma_commit_w(&bars->dp_full);
       }
       for (int ii = 0; ii < n_iter && ok; ++ii) {
         const bool more = ii + 1 < n_iter;
@@ -441,8 +442,8 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
         const uint32_t do_nxt = uint32_t((ii + 1) % C::NDO) * C::TILE_BYTES;
         // S^T of the next tile as soon as every compute group holds this one in registers
         if (more) {
-          if (!(ok = fa_wait(&bars->s_free, uint32_t(ii) & 1u, watch, SITE_KV_SFREE))) break;
-          if (!(ok = fa_wait(&bars->q_full[(ii + 1) % C::NQ], uint32_t((ii + 1) / C::NQ) & 1u, watch,
+          if (!(ok = fa_wait_warp(&bars->s_free, uint32_t(ii) & 1u, watch, SITE_KV_SFREE))) break;
+          if (!(ok = fa_wait_warp(&bars->q_full[(ii + 1) % C::NQ], uint32_t((ii + 1) / C::NQ) & 1u, watch,
                              SITE_KV_QFULL)))
             break;
           tc_fence_after();
@@ -450,28 +451,28 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
-            mma_ss(t_s, sdesc_adv(k_desc, off), sdesc_adv(qd, off), ID_SS, kk > 0 ? 1u : 0u);
+            mma_ss_w(t_s, sdesc_adv(k_desc, off), sdesc_adv(qd, off), ID_SS, kk > 0 ? 1u : 0u);
           }
-          mma_commit(&bars->s_full);
+          mma_commit_w(&bars->s_full);
         }
         // dV += P^T dO and dK += dS^T Q, two independent chains; the 16-query chunk kk
         // of P^T sits at dP^T column 16kk, that of dS^T at 16kk+8 (two fp16 per column)
-        if (!(ok = fa_wait(&bars->pd_ready, uint32_t(ii) & 1u, watch, SITE_KV_PD))) break;
+        if (!(ok = fa_wait_warp(&bars->pd_ready, uint32_t(ii) & 1u, watch, SITE_KV_PD))) break;
         tc_fence_after();
         {
           const uint64_t dod = sdesc_adv(do_mdesc, do_cur), qd = sdesc_adv(q_mdesc, q_cur);
           const uint32_t acc0 = ii > 0 ? 1u : 0u;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            mma_ts(t_dv, t_dp + kk * 16, sdesc_adv(dod, kk * 2048), ID_TN, kk > 0 ? 1u : acc0);
-            mma_ts(t_dk, t_dp + kk * 16 + 8, sdesc_adv(qd, kk * 2048), ID_TN, kk > 0 ? 1u : acc0);
+            mma_ts_w(t_dv, t_dp + kk * 16, sdesc_adv(dod, kk * 2048), ID_TN, kk > 0 ? 1u : acc0);
+            mma_ts_w(t_dk, t_dp + kk * 16 + 8, sdesc_adv(qd, kk * 2048), ID_TN, kk > 0 ? 1u : acc0);
           }
         }
-        mma_commit(&bars->do_empty[ii % C::NDO]);
-        mma_commit(&bars->q_empty[ii % C::NQ]);
+        mma_commit_w(&bars->do_empty[ii % C::NDO]);
+        mma_commit_w(&bars->q_empty[ii % C::NQ]);
         // dP^T of the next tile overwrites P^T and dS^T of this one (read above, in order)
         if (more) {
-          if (!(ok = fa_wait(&bars->do_full[(ii + 1) % C::NDO], uint32_t((ii + 1) / C::NDO) & 1u, watch,
+          if (!(ok = fa_wait_warp(&bars->do_full[(ii + 1) % C::NDO], uint32_t((ii + 1) / C::NDO) & 1u, watch,
                              SITE_KV_DOFULL)))
             break;
           tc_fence_after();
@@ -479,15 +480,15 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
-            mma_ss(t_dp, sdesc_adv(v_desc, off), sdesc_adv(dod, off), ID_SS, kk > 0 ? 1u : 0u);
+            mma_ss_w(t_dp, sdesc_adv(v_desc, off), sdesc_adv(dod, off), ID_SS, kk > 0 ? 1u : 0u);
           }
-          mma_commit(&bars->dp_full);
+          mma_commit_w(&bars->dp_full);
         }
       }
       if (ok) {
-        mma_commit(&bars->acc_done);
+        mma_commit_w(&bars->acc_done);
       } else {
-        mma_commit(&bars->drain);
+        mma_commit_w(&bars->drain);
         drain_wait_b(&bars->drain, 0);
       }
     }
@@ -767,7 +768,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     // formed, dQ(jj) and then dP(jj+1), which overwrites dS(jj) (read in
     // order). Descriptors are built once per tile; each k-step is a constant
     // added to the start-address field.
-    if (lane == 0 && n_blocks > 0) {
+    // The whole warp runs the loop; one elected lane issues each MMA and commit.
+    if (n_blocks > 0) {
       constexpr uint32_t ID_SS = idesc_f16_f32(128, 128, 0, 0);  // S = Q K^T, dP = dO V^T
       constexpr uint32_t ID_DQ = idesc_f16_f32(128, D, 0, 1);    // dQ: dS from TMEM, K MN-major
       const uint64_t q_desc = sdesc_sw128(smem_u32(smem + C::Q_OFF), 16, 1024);
@@ -777,14 +779,14 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       const uint32_t t_s = tmem + C::T_S, t_dp = tmem + C::T_DP, t_dq = tmem + C::T_DQ;
       auto slot_bytes = [](int it) { return uint32_t(it % C::NSLOT) * C::TILE_BYTES; };
       auto wait_full = [&](int it, uint32_t site) {
-        return fa_wait(&bars->kv_full[it % C::NSLOT], uint32_t(it / C::NSLOT) & 1u, watch, site);
+        return fa_wait_warp(&bars->kv_full[it % C::NSLOT], uint32_t(it / C::NSLOT) & 1u, watch, site);
       };
       auto issue_s = [=](int jj) {  // S(jj) = Q K_jj^T
         const uint64_t kd = sdesc_adv(kv_kdesc, slot_bytes(2 * jj));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
-          mma_ss(t_s, sdesc_adv(q_desc, off), sdesc_adv(kd, off), ID_SS, kk > 0 ? 1u : 0u);
+          mma_ss_w(t_s, sdesc_adv(q_desc, off), sdesc_adv(kd, off), ID_SS, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_dp = [=](int jj) {  // dP(jj) = dO V_jj^T
@@ -792,53 +794,53 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
-          mma_ss(t_dp, sdesc_adv(do_desc, off), sdesc_adv(vd, off), ID_SS, kk > 0 ? 1u : 0u);
+          mma_ss_w(t_dp, sdesc_adv(do_desc, off), sdesc_adv(vd, off), ID_SS, kk > 0 ? 1u : 0u);
         }
       };
-      bool ok = fa_wait(&bars->q_full, 0, watch, SITE_DQ_Q) && wait_full(0, SITE_DQ_K);
+      bool ok = fa_wait_warp(&bars->q_full, 0, watch, SITE_DQ_Q) && wait_full(0, SITE_DQ_K);
       if (ok) {
         tc_fence_after();
         issue_s(0);
-        mma_commit(&bars->s_full);
+        mma_commit_w(&bars->s_full);
       }
       if (ok && (ok = wait_full(1, SITE_DQ_V))) {
         tc_fence_after();
         issue_dp(0);
-        mma_commit(&bars->dp_full);
-        mma_commit(&bars->kv_empty[1 % C::NSLOT]);  // V_0: only dP reads it
+        mma_commit_w(&bars->dp_full);
+        mma_commit_w(&bars->kv_empty[1 % C::NSLOT]);  // V_0: only dP reads it
       }
       for (int jj = 0; jj < n_blocks && ok; ++jj) {
         const bool more = jj + 1 < n_blocks;
         if (more) {
-          if (!(ok = fa_wait(&bars->s_free, uint32_t(jj) & 1u, watch, SITE_DQ_S))) break;
+          if (!(ok = fa_wait_warp(&bars->s_free, uint32_t(jj) & 1u, watch, SITE_DQ_S))) break;
           if (!(ok = wait_full(2 * (jj + 1), SITE_DQ_K))) break;
           tc_fence_after();
           issue_s(jj + 1);
-          mma_commit(&bars->s_full);
+          mma_commit_w(&bars->s_full);
         }
         // dQ += dS K ; keys 16kk..16kk+15 of dS sit at dP columns 16kk+0..7
-        if (!(ok = fa_wait(&bars->ds_ready, uint32_t(jj) & 1u, watch, SITE_DQ_DS))) break;
+        if (!(ok = fa_wait_warp(&bars->ds_ready, uint32_t(jj) & 1u, watch, SITE_DQ_DS))) break;
         tc_fence_after();
         {
           const uint64_t kd = sdesc_adv(kv_mdesc, slot_bytes(2 * jj));
           const uint32_t acc0 = jj > 0 ? 1u : 0u;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ts(t_dq, t_dp + kk * 16, sdesc_adv(kd, kk * 2048), ID_DQ, kk > 0 ? 1u : acc0);
+            mma_ts_w(t_dq, t_dp + kk * 16, sdesc_adv(kd, kk * 2048), ID_DQ, kk > 0 ? 1u : acc0);
         }
-        mma_commit(&bars->kv_empty[(2 * jj) % C::NSLOT]);  // K_jj: read by S_jj and this dQ
+        mma_commit_w(&bars->kv_empty[(2 * jj) % C::NSLOT]);  // K_jj: read by S_jj and this dQ
         if (more) {
           if (!(ok = wait_full(2 * (jj + 1) + 1, SITE_DQ_V))) break;
           tc_fence_after();
           issue_dp(jj + 1);
-          mma_commit(&bars->dp_full);
-          mma_commit(&bars->kv_empty[(2 * (jj + 1) + 1) % C::NSLOT]);  // V_{jj+1}
+          mma_commit_w(&bars->dp_full);
+          mma_commit_w(&bars->kv_empty[(2 * (jj + 1) + 1) % C::NSLOT]);  // V_{jj+1}
         }
       }
       if (ok) {
-        mma_commit(&bars->acc_done);
+        mma_commit_w(&bars->acc_done);
       } else {
-        mma_commit(&bars->drain);
+        mma_commit_w(&bars->drain);
         drain_wait_b(&bars->drain, 0);
       }
     }

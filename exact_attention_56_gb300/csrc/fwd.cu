@@ -205,7 +205,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_blocks > 0) {
+    // The whole warp runs the loop; one elected lane issues each MMA and commit.
+    if (n_blocks > 0) {
       constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
       constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);    // P from TMEM, V MN-major
       // Descriptors are built once; each k-step, Q tile and ring slot is a
@@ -217,7 +218,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
 
       auto slot_of = [](int it) { return it % C::NSLOT; };
       auto wait_full = [&](int it, uint32_t site) {
-        return fa_wait(&bars->kv_full[slot_of(it)], uint32_t(it / C::NSLOT) & 1u, watch, site);
+        return fa_wait_warp(&bars->kv_full[slot_of(it)], uint32_t(it / C::NSLOT) & 1u, watch, site);
       };
       auto issue_s = [=](int jj, int t, int sbuf) {
         const uint64_t qd = sdesc_adv(q_desc, uint32_t(t) * C::TILE_BYTES);
@@ -226,7 +227,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
-          mma_ss(ts, sdesc_adv(qd, off), sdesc_adv(kd, off), IDESC_S, kk > 0 ? 1u : 0u);
+          mma_ss_w(ts, sdesc_adv(qd, off), sdesc_adv(kd, off), IDESC_S, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [=](int jj, int t, int sbuf) {
@@ -234,67 +235,67 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
         const uint32_t to = tmem + C::O_COL0 + uint32_t(t) * D, tp = tmem + uint32_t(sbuf) * 128;
         const uint32_t acc0 = jj > 0 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ts(to, tp + kk * 8, sdesc_adv(vd, kk * 2048), IDESC_O, kk > 0 ? 1u : acc0);
+        for (int kk = 0; kk < 8; ++kk) mma_ts_w(to, tp + kk * 8, sdesc_adv(vd, kk * 2048), IDESC_O, kk > 0 ? 1u : acc0);
       };
 
-      bool ok = fa_wait(&bars->q_full, 0, watch, SITE_MMA_Q);
+      bool ok = fa_wait_warp(&bars->q_full, 0, watch, SITE_MMA_Q);
       tc_fence_after();
       if (NT == 2) {
         for (int jj = 0; jj < n_blocks && ok; ++jj) {
           if (!(ok = wait_full(2 * jj, SITE_MMA_K))) break;
           tc_fence_after();
           issue_s(jj, 0, 0);
-          mma_commit(&bars->s_full[0]);
+          mma_commit_w(&bars->s_full[0]);
           if (jj > 0) {
-            if (!(ok = fa_wait(&bars->p_full[1], uint32_t(jj - 1) & 1u, watch, SITE_MMA_P))) break;
+            if (!(ok = fa_wait_warp(&bars->p_full[1], uint32_t(jj - 1) & 1u, watch, SITE_MMA_P))) break;
             tc_fence_after();
             issue_pv(jj - 1, 1, 1);
-            mma_commit(&bars->pv_done[1]);
-            mma_commit(&bars->kv_empty[slot_of(2 * (jj - 1) + 1)]);
+            mma_commit_w(&bars->pv_done[1]);
+            mma_commit_w(&bars->kv_empty[slot_of(2 * (jj - 1) + 1)]);
           }
           issue_s(jj, 1, 1);
-          mma_commit(&bars->s_full[1]);
-          mma_commit(&bars->kv_empty[slot_of(2 * jj)]);
+          mma_commit_w(&bars->s_full[1]);
+          mma_commit_w(&bars->kv_empty[slot_of(2 * jj)]);
           if (!(ok = wait_full(2 * jj + 1, SITE_MMA_V))) break;
-          if (!(ok = fa_wait(&bars->p_full[0], uint32_t(jj) & 1u, watch, SITE_MMA_P))) break;
+          if (!(ok = fa_wait_warp(&bars->p_full[0], uint32_t(jj) & 1u, watch, SITE_MMA_P))) break;
           tc_fence_after();
           issue_pv(jj, 0, 0);
-          mma_commit(&bars->pv_done[0]);
+          mma_commit_w(&bars->pv_done[0]);
         }
         if (ok) {
           const int jj = n_blocks - 1;
-          if ((ok = fa_wait(&bars->p_full[1], uint32_t(jj) & 1u, watch, SITE_MMA_P))) {
+          if ((ok = fa_wait_warp(&bars->p_full[1], uint32_t(jj) & 1u, watch, SITE_MMA_P))) {
             tc_fence_after();
             issue_pv(jj, 1, 1);
-            mma_commit(&bars->pv_done[1]);
-            mma_commit(&bars->kv_empty[slot_of(2 * jj + 1)]);
+            mma_commit_w(&bars->pv_done[1]);
+            mma_commit_w(&bars->kv_empty[slot_of(2 * jj + 1)]);
           }
         }
       } else {
         if (ok && (ok = wait_full(0, SITE_MMA_K))) {
           tc_fence_after();
           issue_s(0, 0, 0);
-          mma_commit(&bars->s_full[0]);
-          mma_commit(&bars->kv_empty[slot_of(0)]);
+          mma_commit_w(&bars->s_full[0]);
+          mma_commit_w(&bars->kv_empty[slot_of(0)]);
         }
         for (int jj = 0; jj < n_blocks && ok; ++jj) {
           if (jj + 1 < n_blocks) {
             if (!(ok = wait_full(2 * (jj + 1), SITE_MMA_K))) break;
             tc_fence_after();
             issue_s(jj + 1, 0, (jj + 1) & 1);
-            mma_commit(&bars->s_full[(jj + 1) & 1]);
-            mma_commit(&bars->kv_empty[slot_of(2 * (jj + 1))]);
+            mma_commit_w(&bars->s_full[(jj + 1) & 1]);
+            mma_commit_w(&bars->kv_empty[slot_of(2 * (jj + 1))]);
           }
           if (!(ok = wait_full(2 * jj + 1, SITE_MMA_V))) break;
-          if (!(ok = fa_wait(&bars->p_full[0], uint32_t(jj) & 1u, watch, SITE_MMA_P))) break;
+          if (!(ok = fa_wait_warp(&bars->p_full[0], uint32_t(jj) & 1u, watch, SITE_MMA_P))) break;
           tc_fence_after();
           issue_pv(jj, 0, jj & 1);
-          mma_commit(&bars->pv_done[0]);
-          mma_commit(&bars->kv_empty[slot_of(2 * jj + 1)]);
+          mma_commit_w(&bars->pv_done[0]);
+          mma_commit_w(&bars->kv_empty[slot_of(2 * jj + 1)]);
         }
       }
       if (!ok) {  // let issued MMAs finish before TMEM is released
-        mma_commit(&bars->drain);
+        mma_commit_w(&bars->drain);
         drain_wait(&bars->drain, 0);
       }
     }
