@@ -121,6 +121,15 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+__device__ __forceinline__ void bulk_load_w(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Timeout-only wait used while draining after an abort.
 __device__ __forceinline__ void drain_wait_b(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
@@ -359,16 +368,17 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_iter > 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(&bars->kv_full, 2 * C::TILE_BYTES);
+    // The whole warp runs the loop; one elected lane issues each copy.
+    if (n_iter > 0) {
+      tma_prefetch_desc_w(&tm_q);
+      tma_prefetch_desc_w(&tm_k);
+      tma_prefetch_desc_w(&tm_v);
+      tma_prefetch_desc_w(&tm_do);
+      mbar_arrive_expect_tx_w(&bars->kv_full, 2 * C::TILE_BYTES);
       for (int pn = 0; pn < C::PANELS; ++pn) {
-        tma_load_4d(smem + C::K_OFF + pn * C::PANEL_BYTES, &tm_k, &bars->kv_full, pn * 64, hk, sq_.k_off + j0,
+        tma_load_4d_w(smem + C::K_OFF + pn * C::PANEL_BYTES, &tm_k, &bars->kv_full, pn * 64, hk, sq_.k_off + j0,
                     sq_.tb);
-        tma_load_4d(smem + C::V_OFF + pn * C::PANEL_BYTES, &tm_v, &bars->kv_full, pn * 64, hk, sq_.k_off + j0,
+        tma_load_4d_w(smem + C::V_OFF + pn * C::PANEL_BYTES, &tm_v, &bars->kv_full, pn * 64, hk, sq_.k_off + j0,
                     sq_.tb);
       }
       int q_issued = 0, do_issued = 0;
@@ -377,20 +387,20 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
         const int hq = hk * p.group + ii / n_qtl;
         const int i0 = (qt_first + ii % n_qtl) * 128;
         const size_t vec_base = (size_t(b) * p.H + hq) * p.Sq_pad;
-        if (!fa_wait(&bars->q_empty[s], (uint32_t(ii / C::NQ) & 1u) ^ 1u, watch, SITE_KV_EMPTY)) break;
-        mbar_arrive_expect_tx(&bars->q_full[s], C::TILE_BYTES);
+        if (!fa_wait_warp(&bars->q_empty[s], (uint32_t(ii / C::NQ) & 1u) ^ 1u, watch, SITE_KV_EMPTY)) break;
+        mbar_arrive_expect_tx_w(&bars->q_full[s], C::TILE_BYTES);
         for (int pn = 0; pn < C::PANELS; ++pn)
-          tma_load_4d(smem + C::Q_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bars->q_full[s], pn * 64,
+          tma_load_4d_w(smem + C::Q_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bars->q_full[s], pn * 64,
                       hq, sq_.q_off + i0, sq_.tb);
         q_issued = ii + 1;
         const int d = ii % C::NDO;
-        if (!fa_wait(&bars->do_empty[d], (uint32_t(ii / C::NDO) & 1u) ^ 1u, watch, SITE_KV_DOEMPTY)) break;
-        mbar_arrive_expect_tx(&bars->do_full[d], C::DO_TX);
+        if (!fa_wait_warp(&bars->do_empty[d], (uint32_t(ii / C::NDO) & 1u) ^ 1u, watch, SITE_KV_DOEMPTY)) break;
+        mbar_arrive_expect_tx_w(&bars->do_full[d], C::DO_TX);
         for (int pn = 0; pn < C::PANELS; ++pn)
-          tma_load_4d(smem + C::DO_OFF + d * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_do, &bars->do_full[d],
+          tma_load_4d_w(smem + C::DO_OFF + d * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_do, &bars->do_full[d],
                       pn * 64, hq, sq_.q_off + i0, sq_.tb);
-        bulk_load(smem + C::VEC_OFF + d * 1024, p.l2 + vec_base + i0, 512, &bars->do_full[d]);
-        bulk_load(smem + C::VEC_OFF + d * 1024 + 512, p.dvec + vec_base + i0, 512, &bars->do_full[d]);
+        bulk_load_w(smem + C::VEC_OFF + d * 1024, p.l2 + vec_base + i0, 512, &bars->do_full[d]);
+        bulk_load_w(smem + C::VEC_OFF + d * 1024 + 512, p.dvec + vec_base + i0, 512, &bars->do_full[d]);
         do_issued = ii + 1;
       }
       // every copy must land before the CTA may exit
@@ -727,16 +737,17 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_blocks > 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(&bars->q_full, 2 * C::TILE_BYTES);
+    // The whole warp runs the loop; one elected lane issues each copy.
+    if (n_blocks > 0) {
+      tma_prefetch_desc_w(&tm_q);
+      tma_prefetch_desc_w(&tm_k);
+      tma_prefetch_desc_w(&tm_v);
+      tma_prefetch_desc_w(&tm_do);
+      mbar_arrive_expect_tx_w(&bars->q_full, 2 * C::TILE_BYTES);
       for (int pn = 0; pn < C::PANELS; ++pn) {
-        tma_load_4d(smem + C::Q_OFF + pn * C::PANEL_BYTES, &tm_q, &bars->q_full, pn * 64, h, sq_.q_off + row0,
+        tma_load_4d_w(smem + C::Q_OFF + pn * C::PANEL_BYTES, &tm_q, &bars->q_full, pn * 64, h, sq_.q_off + row0,
                     sq_.tb);
-        tma_load_4d(smem + C::DO_OFF + pn * C::PANEL_BYTES, &tm_do, &bars->q_full, pn * 64, h, sq_.q_off + row0,
+        tma_load_4d_w(smem + C::DO_OFF + pn * C::PANEL_BYTES, &tm_do, &bars->q_full, pn * 64, h, sq_.q_off + row0,
                     sq_.tb);
       }
       int issued = 0;
@@ -745,14 +756,14 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         for (int kv = 0; kv < 2; ++kv) {
           const int it = 2 * jj + kv;
           const int s = it % C::NSLOT;
-          if (!fa_wait(&bars->kv_empty[s], (uint32_t(it / C::NSLOT) & 1u) ^ 1u, watch, SITE_DQ_EMPTY)) {
+          if (!fa_wait_warp(&bars->kv_empty[s], (uint32_t(it / C::NSLOT) & 1u) ^ 1u, watch, SITE_DQ_EMPTY)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&bars->kv_full[s], C::TILE_BYTES);
+          mbar_arrive_expect_tx_w(&bars->kv_full[s], C::TILE_BYTES);
           const CUtensorMap* m = kv ? &tm_v : &tm_k;
           for (int pn = 0; pn < C::PANELS; ++pn)
-            tma_load_4d(smem + C::KV_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, m, &bars->kv_full[s],
+            tma_load_4d_w(smem + C::KV_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, m, &bars->kv_full[s],
                         pn * 64, hkv, sq_.k_off + (jb + jj) * 128, sq_.tb);
           issued = it + 1;
         }

@@ -169,14 +169,15 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_blocks > 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(&bars->q_full, NT * C::TILE_BYTES);
+    // The whole warp runs the loop; one elected lane issues each copy.
+    if (n_blocks > 0) {
+      tma_prefetch_desc_w(&tm_q);
+      tma_prefetch_desc_w(&tm_k);
+      tma_prefetch_desc_w(&tm_v);
+      mbar_arrive_expect_tx_w(&bars->q_full, NT * C::TILE_BYTES);
       for (int t = 0; t < NT; ++t)
         for (int pn = 0; pn < C::PANELS; ++pn)
-          tma_load_4d(smem + C::Q_OFF + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bars->q_full, pn * 64,
+          tma_load_4d_w(smem + C::Q_OFF + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q, &bars->q_full, pn * 64,
                       h, q_off + row0 + t * 128, tb);
       int issued = 0;
       bool ok = true;
@@ -185,14 +186,14 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
           const int it = 2 * jj + kv;
           const int s = it % C::NSLOT;
           const uint32_t ph = uint32_t(it / C::NSLOT) & 1u;
-          if (!fa_wait(&bars->kv_empty[s], ph ^ 1u, watch, SITE_PROD_EMPTY)) {
+          if (!fa_wait_warp(&bars->kv_empty[s], ph ^ 1u, watch, SITE_PROD_EMPTY)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&bars->kv_full[s], C::TILE_BYTES);
+          mbar_arrive_expect_tx_w(&bars->kv_full[s], C::TILE_BYTES);
           const CUtensorMap* m = kv ? &tm_v : &tm_k;
           for (int pn = 0; pn < C::PANELS; ++pn)
-            tma_load_4d(smem + C::KV_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, m, &bars->kv_full[s],
+            tma_load_4d_w(smem + C::KV_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, m, &bars->kv_full[s],
                         pn * 64, hkv, k_off + (jb + jj) * 128, tb);
           issued = it + 1;
         }
