@@ -268,9 +268,12 @@ struct KvCfg {
   static constexpr int PANEL_BYTES = 128 * 128;
   static constexpr int TILE_BYTES = PANELS * PANEL_BYTES;
   // Q of the next tile is read early (S^T of tile ii+1 is issued while tile ii
-  // is still being processed), so Q gets a third stage; dO is read last.
-  static constexpr int NQ = 3;   // Q stages
-  static constexpr int NDO = 2;  // dO (+ L2, D) stages
+  // is still being processed), so Q gets a third stage; dO is read last. At
+  // D = 64, dP^T of tile ii+1 also runs early (two dP^T buffers), and the
+  // smaller tiles leave room for four stages of each.
+  static constexpr int NQ = D == 64 ? 4 : 3;   // Q stages
+  static constexpr int NDO = D == 64 ? 4 : 2;  // dO (+ L2, D) stages
+  static constexpr int NDP = D == 64 ? 2 : 1;  // dP^T buffers in TMEM
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = TILE_BYTES;
   static constexpr int Q_OFF = 2 * TILE_BYTES;
@@ -283,23 +286,28 @@ struct KvCfg {
   static constexpr int NCT = 128 * NCW;  // compute threads
   static constexpr int THREADS = 128 + NCT;
   static constexpr int DO_TX = TILE_BYTES + 1024;
-  // TMEM: S^T [0,128) fp32; dP^T [128,256) fp32, over which, once consumed, the
-  // 16-query chunk kk of P^T (fp16 pairs) sits at columns 16kk+0..7 and that of
-  // dS^T at 16kk+8..15, so every compute group writes only inside the dP^T
-  // columns it has read itself; dV and dK accumulators after it.
-  static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
+  // TMEM: S^T [0,128) fp32; dP^T of tile ii in buffer ii % NDP at
+  // [128 + 128 b, 256 + 128 b) fp32, over which, once consumed, the 16-query
+  // chunk kk of P^T (fp16 pairs) sits at columns 16kk+0..7 and that of dS^T at
+  // 16kk+8..15, so every compute group writes only inside the dP^T columns it
+  // has read itself; dV and dK accumulators after the buffers. With two
+  // buffers, S^T and dP^T of tile ii+1 run on the tensor pipe while the
+  // compute groups form P^T and dS^T of tile ii.
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 128 + 128 * NDP, T_DK = T_DV + D;
   static_assert(T_DK + D <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
 struct KvBars {
   uint64_t kv_full;
-  uint64_t q_full[3], q_empty[3];
-  uint64_t do_full[2], do_empty[2];
-  uint64_t s_full, s_free, dp_full, pd_ready, acc_done, drain;
+  uint64_t q_full[4], q_empty[4];
+  uint64_t do_full[4], do_empty[4];
+  uint64_t s_full, s_free, acc_done, drain;
+  uint64_t dp_full[2], pd_ready[2];  // per dP^T buffer
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(KvBars) <= 256, "barrier block");
 
 template <int D, bool DROP>
 __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
@@ -348,9 +356,11 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
       mbar_init(&bars->do_empty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, C::NCT);
-    mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->pd_ready, C::NCT);
+    mbar_init(&bars->s_free, C::NCT / 32);  // one arrive per compute warp
+    for (int s = 0; s < C::NDP; ++s) {
+      mbar_init(&bars->dp_full[s], 1);
+      mbar_init(&bars->pd_ready[s], C::NCT / 32);
+    }
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
@@ -425,6 +435,21 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
       const uint64_t q_mdesc = sdesc_sw128(smem_u32(smem + C::Q_OFF), C::PANEL_BYTES, 1024);    // MN-major (dK)
       const uint64_t do_mdesc = sdesc_sw128(smem_u32(smem + C::DO_OFF), C::PANEL_BYTES, 1024);  // MN-major (dV)
       const uint32_t t_s = tmem + C::T_S, t_dp = tmem + C::T_DP, t_dv = tmem + C::T_DV, t_dk = tmem + C::T_DK;
+      // dP^T(ii) = V dO^T into buffer ii % NDP
+      auto issue_dp = [&](int ii) {
+        if (!fa_wait_warp(&bars->do_full[ii % C::NDO], uint32_t(ii / C::NDO) & 1u, watch, SITE_KV_DOFULL))
+          return false;
+        tc_fence_after();
+        const uint64_t dod = sdesc_adv(do_kdesc, uint32_t(ii % C::NDO) * C::TILE_BYTES);
+        const uint32_t dst = t_dp + uint32_t(ii % C::NDP) * 128;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
+          mma_ss_w(dst, sdesc_adv(v_desc, off), sdesc_adv(dod, off), ID_SS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit_w(&bars->dp_full[ii % C::NDP]);
+        return true;
+      };
       bool ok = fa_wait_warp(&bars->kv_full, 0, watch, SITE_KV_KV) && fa_wait_warp(&bars->q_full[0], 0, watch, SITE_KV_QFULL);
       if (ok) {  // S^T(0) = K Q^T
         tc_fence_after();
@@ -435,21 +460,12 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
         }
         mma_commit_w(&bars->s_full);
       }
-      if (ok && (ok = fa_wait_warp(&bars->do_full[0], 0, watch, SITE_KV_DOFULL))) {  // dP^T(0) = V dO^T
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
-          mma_ss_w(t_dp, sdesc_adv(v_desc, off), sdesc_adv(do_kdesc, off), ID_SS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit_w(&bars->dp_full);
-      }
+      ok = ok && issue_dp(0);
       for (int ii = 0; ii < n_iter && ok; ++ii) {
         const bool more = ii + 1 < n_iter;
         const uint32_t q_cur = uint32_t(ii % C::NQ) * C::TILE_BYTES;        // Q stage of tile ii
         const uint32_t q_nxt = uint32_t((ii + 1) % C::NQ) * C::TILE_BYTES;  // Q stage of tile ii + 1
         const uint32_t do_cur = uint32_t(ii % C::NDO) * C::TILE_BYTES;
-        const uint32_t do_nxt = uint32_t((ii + 1) % C::NDO) * C::TILE_BYTES;
         // S^T of the next tile as soon as every compute group holds this one in registers
         if (more) {
           if (!(ok = fa_wait_warp(&bars->s_free, uint32_t(ii) & 1u, watch, SITE_KV_SFREE))) break;
@@ -464,36 +480,30 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
             mma_ss_w(t_s, sdesc_adv(k_desc, off), sdesc_adv(qd, off), ID_SS, kk > 0 ? 1u : 0u);
           }
           mma_commit_w(&bars->s_full);
+          // with a second buffer, dP^T of the next tile too; it overwrites the
+          // buffer of tile ii-1, whose dV, dK were issued before (read in order)
+          if (C::NDP == 2 && !(ok = issue_dp(ii + 1))) break;
         }
         // dV += P^T dO and dK += dS^T Q, two independent chains; the 16-query chunk kk
-        // of P^T sits at dP^T column 16kk, that of dS^T at 16kk+8 (two fp16 per column)
-        if (!(ok = fa_wait_warp(&bars->pd_ready, uint32_t(ii) & 1u, watch, SITE_KV_PD))) break;
+        // of P^T sits at dP^T column 16kk of its buffer, that of dS^T at 16kk+8
+        const int pb = ii % C::NDP;
+        if (!(ok = fa_wait_warp(&bars->pd_ready[pb], uint32_t(ii / C::NDP) & 1u, watch, SITE_KV_PD))) break;
         tc_fence_after();
         {
           const uint64_t dod = sdesc_adv(do_mdesc, do_cur), qd = sdesc_adv(q_mdesc, q_cur);
+          const uint32_t src = t_dp + uint32_t(pb) * 128;
           const uint32_t acc0 = ii > 0 ? 1u : 0u;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            mma_ts_w(t_dv, t_dp + kk * 16, sdesc_adv(dod, kk * 2048), ID_TN, kk > 0 ? 1u : acc0);
-            mma_ts_w(t_dk, t_dp + kk * 16 + 8, sdesc_adv(qd, kk * 2048), ID_TN, kk > 0 ? 1u : acc0);
+            mma_ts_w(t_dv, src + kk * 16, sdesc_adv(dod, kk * 2048), ID_TN, kk > 0 ? 1u : acc0);
+            mma_ts_w(t_dk, src + kk * 16 + 8, sdesc_adv(qd, kk * 2048), ID_TN, kk > 0 ? 1u : acc0);
           }
         }
         mma_commit_w(&bars->do_empty[ii % C::NDO]);
         mma_commit_w(&bars->q_empty[ii % C::NQ]);
-        // dP^T of the next tile overwrites P^T and dS^T of this one (read above, in order)
-        if (more) {
-          if (!(ok = fa_wait_warp(&bars->do_full[(ii + 1) % C::NDO], uint32_t((ii + 1) / C::NDO) & 1u, watch,
-                             SITE_KV_DOFULL)))
-            break;
-          tc_fence_after();
-          const uint64_t dod = sdesc_adv(do_kdesc, do_nxt);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
-            mma_ss_w(t_dp, sdesc_adv(v_desc, off), sdesc_adv(dod, off), ID_SS, kk > 0 ? 1u : 0u);
-          }
-          mma_commit_w(&bars->dp_full);
-        }
+        // with one buffer, dP^T of the next tile overwrites P^T and dS^T of this
+        // one, read above (in order)
+        if (C::NDP == 1 && more && !(ok = issue_dp(ii + 1))) break;
       }
       if (ok) {
         mma_commit_w(&bars->acc_done);
@@ -545,7 +555,7 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
       float pv[C::COLS];
       tmem_ld_cols(tmem + lane_addr + C::T_S + w * C::COLS, pv);
       tc_fence_before();
-      mbar_arrive(&bars->s_free);
+      mbar_arrive_warp(&bars->s_free);
       const bool need_mask = !(tile_keys_ok && i0 >= qlo_max && i0 + 127 <= qhi_min);
       const uint64_t sl2 = f2_pack(sl, sl);
 #pragma unroll
@@ -572,14 +582,15 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < C::COLS; ++c) pv[c] = (c >= lo && c <= hi) ? pv[c] : 0.0f;
       }
-      if (!(ok = fa_wait_warp(&bars->dp_full, uint32_t(ii) & 1u, watch, SITE_KV_DP))) break;
+      const int pb = ii % C::NDP;
+      if (!(ok = fa_wait_warp(&bars->dp_full[pb], uint32_t(ii / C::NDP) & 1u, watch, SITE_KV_DP))) break;
       tc_fence_after();
       // per 16-query chunk: load dP^T, form dS^T, then P^T and dS^T as fp16 pairs over
       // the chunk's consumed dP^T columns (see the TMEM map)
 #pragma unroll
       for (int ch = 0; ch < C::COLS / 16; ++ch) {
         float dp[16];
-        const uint32_t col = tmem + lane_addr + C::T_DP + w * C::COLS + 16 * ch;
+        const uint32_t col = tmem + lane_addr + C::T_DP + uint32_t(pb) * 128 + w * C::COLS + 16 * ch;
         tmem_ld_cols(col, dp);
         uint32_t pp[8], ps[8];
 #pragma unroll
@@ -604,7 +615,7 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->pd_ready);
+      mbar_arrive_warp(&bars->pd_ready[pb]);
     }
     // ------------------------------------------------------------ dK / dV epilogue
     // groups 0..NCW/2-1 write dV, the rest dK (times scale); each a D/(NCW/2)-column slice
@@ -653,32 +664,41 @@ struct DqCfg {
   static constexpr int PANELS = D / 64;
   static constexpr int PANEL_BYTES = 128 * 128;
   static constexpr int TILE_BYTES = PANELS * PANEL_BYTES;
-  static constexpr int NSLOT = D == 64 ? 8 : 5;  // ring of K_j, V_j tiles
+  // K_j stays until dQ(j) has read it, V_j only until dP(j); separate rings let
+  // V of a later tile load as soon as dP has freed a slot.
+  static constexpr int NK = D == 64 ? 4 : 3;  // ring of K_j tiles
+  static constexpr int NV = D == 64 ? 4 : 2;  // ring of V_j tiles
   static constexpr int Q_OFF = 0;
   static constexpr int DO_OFF = TILE_BYTES;
-  static constexpr int KV_OFF = 2 * TILE_BYTES;
-  static constexpr int BAR_OFF = KV_OFF + NSLOT * TILE_BYTES;
+  static constexpr int K_OFF = 2 * TILE_BYTES;
+  static constexpr int V_OFF = K_OFF + NK * TILE_BYTES;
+  static constexpr int BAR_OFF = V_OFF + NV * TILE_BYTES;
   static constexpr int SMEM_BYTES = BAR_OFF + 256;
   static constexpr int NCW = 4;  // compute warpgroups; each owns COLS key columns
   static constexpr int COLS = 128 / NCW;
   static constexpr int NCT = 128 * NCW;
   static constexpr int THREADS = 128 + NCT;
-  // TMEM: S at [0,128), dP at [128,256), dQ at [256,256+D). Once dP is
-  // consumed, the 16-key chunk kk of dS (fp16 pairs) sits at dP columns
-  // 16kk+0..7, inside the columns its compute group has read itself; S is
-  // free as soon as every group holds it in registers.
-  static constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 256;
+  // TMEM: S at [0,128); dP of tile j in buffer j % 2 at [128,256) or [256,384);
+  // dQ at [384,384+D). Once dP is consumed, the 16-key chunk kk of dS (fp16
+  // pairs) sits at its buffer's columns 16kk+0..7, inside the columns its compute
+  // group has read itself. S is free as soon as every group holds it in
+  // registers; with two dP buffers, S and dP of tile j+1 run on the tensor pipe
+  // while the compute groups form dS of tile j.
+  static constexpr int NDP = 2;
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 128 + 128 * NDP;
   static_assert(T_DQ + D <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
 struct DqBars {
   uint64_t q_full;
-  uint64_t kv_full[8], kv_empty[8];
-  uint64_t s_full, s_free, dp_full, ds_ready, acc_done, drain;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full, s_free, acc_done, drain;
+  uint64_t dp_full[2], ds_ready[2];  // per dP buffer
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(DqBars) <= 256, "barrier block");
 
 template <int D, bool DROP>
 __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
@@ -712,14 +732,20 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    for (int s = 0; s < C::NSLOT; ++s) {
-      mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+    for (int s = 0; s < C::NK; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < C::NV; ++s) {
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, C::NCT);
-    mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->ds_ready, C::NCT);
+    mbar_init(&bars->s_free, C::NCT / 32);  // one arrive per compute warp
+    for (int s = 0; s < C::NDP; ++s) {
+      mbar_init(&bars->dp_full[s], 1);
+      mbar_init(&bars->ds_ready[s], C::NCT / 32);
+    }
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
@@ -750,103 +776,92 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         tma_load_4d_w(smem + C::DO_OFF + pn * C::PANEL_BYTES, &tm_do, &bars->q_full, pn * 64, h, sq_.q_off + row0,
                     sq_.tb);
       }
-      int issued = 0;
-      bool ok = true;
-      for (int jj = 0; jj < n_blocks && ok; ++jj) {
-        for (int kv = 0; kv < 2; ++kv) {
-          const int it = 2 * jj + kv;
-          const int s = it % C::NSLOT;
-          if (!fa_wait_warp(&bars->kv_empty[s], (uint32_t(it / C::NSLOT) & 1u) ^ 1u, watch, SITE_DQ_EMPTY)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx_w(&bars->kv_full[s], C::TILE_BYTES);
-          const CUtensorMap* m = kv ? &tm_v : &tm_k;
-          for (int pn = 0; pn < C::PANELS; ++pn)
-            tma_load_4d_w(smem + C::KV_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, m, &bars->kv_full[s],
-                        pn * 64, hkv, sq_.k_off + (jb + jj) * 128, sq_.tb);
-          issued = it + 1;
-        }
+      int k_issued = 0, v_issued = 0;
+      for (int jj = 0; jj < n_blocks; ++jj) {
+        const int row = sq_.k_off + (jb + jj) * 128;
+        const int sk = jj % C::NK, sv = jj % C::NV;
+        if (!fa_wait_warp(&bars->k_empty[sk], (uint32_t(jj / C::NK) & 1u) ^ 1u, watch, SITE_DQ_EMPTY)) break;
+        mbar_arrive_expect_tx_w(&bars->k_full[sk], C::TILE_BYTES);
+        for (int pn = 0; pn < C::PANELS; ++pn)
+          tma_load_4d_w(smem + C::K_OFF + sk * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_k, &bars->k_full[sk],
+                        pn * 64, hkv, row, sq_.tb);
+        k_issued = jj + 1;
+        if (!fa_wait_warp(&bars->v_empty[sv], (uint32_t(jj / C::NV) & 1u) ^ 1u, watch, SITE_DQ_EMPTY)) break;
+        mbar_arrive_expect_tx_w(&bars->v_full[sv], C::TILE_BYTES);
+        for (int pn = 0; pn < C::PANELS; ++pn)
+          tma_load_4d_w(smem + C::V_OFF + sv * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_v, &bars->v_full[sv],
+                        pn * 64, hkv, row, sq_.tb);
+        v_issued = jj + 1;
       }
       drain_wait_b(&bars->q_full, 0);
-      for (int it = (issued > C::NSLOT ? issued - C::NSLOT : 0); it < issued; ++it)
-        drain_wait_b(&bars->kv_full[it % C::NSLOT], uint32_t(it / C::NSLOT) & 1u);
+      for (int jj = (k_issued > C::NK ? k_issued - C::NK : 0); jj < k_issued; ++jj)
+        drain_wait_b(&bars->k_full[jj % C::NK], uint32_t(jj / C::NK) & 1u);
+      for (int jj = (v_issued > C::NV ? v_issued - C::NV : 0); jj < v_issued; ++jj)
+        drain_wait_b(&bars->v_full[jj % C::NV], uint32_t(jj / C::NV) & 1u);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // Per key tile jj: S(jj+1) as soon as every compute group holds S(jj) in
-    // registers (it overlaps the exponentials of tile jj); once dS(jj) is
-    // formed, dQ(jj) and then dP(jj+1), which overwrites dS(jj) (read in
-    // order). Descriptors are built once per tile; each k-step is a constant
-    // added to the start-address field.
+    // registers, then dP(jj+1) into the other dP buffer; both run while the
+    // compute groups form dS(jj). Then dQ(jj) once dS(jj) is stored. dP(jj+2)
+    // overwrites dS(jj) only after dQ(jj) has been issued (read in order).
+    // Descriptors are built once per tile; each k-step is a constant added to
+    // the start-address field.
     // The whole warp runs the loop; one elected lane issues each MMA and commit.
     if (n_blocks > 0) {
       constexpr uint32_t ID_SS = idesc_f16_f32(128, 128, 0, 0);  // S = Q K^T, dP = dO V^T
       constexpr uint32_t ID_DQ = idesc_f16_f32(128, D, 0, 1);    // dQ: dS from TMEM, K MN-major
       const uint64_t q_desc = sdesc_sw128(smem_u32(smem + C::Q_OFF), 16, 1024);
       const uint64_t do_desc = sdesc_sw128(smem_u32(smem + C::DO_OFF), 16, 1024);
-      const uint64_t kv_kdesc = sdesc_sw128(smem_u32(smem + C::KV_OFF), 16, 1024);            // slot 0, K-major
-      const uint64_t kv_mdesc = sdesc_sw128(smem_u32(smem + C::KV_OFF), C::PANEL_BYTES, 1024);  // slot 0, MN-major
+      const uint64_t k_kdesc = sdesc_sw128(smem_u32(smem + C::K_OFF), 16, 1024);            // slot 0, K-major
+      const uint64_t k_mdesc = sdesc_sw128(smem_u32(smem + C::K_OFF), C::PANEL_BYTES, 1024);  // slot 0, MN-major
+      const uint64_t v_kdesc = sdesc_sw128(smem_u32(smem + C::V_OFF), 16, 1024);            // slot 0, K-major
       const uint32_t t_s = tmem + C::T_S, t_dp = tmem + C::T_DP, t_dq = tmem + C::T_DQ;
-      auto slot_bytes = [](int it) { return uint32_t(it % C::NSLOT) * C::TILE_BYTES; };
-      auto wait_full = [&](int it, uint32_t site) {
-        return fa_wait_warp(&bars->kv_full[it % C::NSLOT], uint32_t(it / C::NSLOT) & 1u, watch, site);
-      };
-      auto issue_s = [=](int jj) {  // S(jj) = Q K_jj^T
-        const uint64_t kd = sdesc_adv(kv_kdesc, slot_bytes(2 * jj));
+      auto issue_s = [&](int jj) {  // S(jj) = Q K_jj^T
+        if (!fa_wait_warp(&bars->k_full[jj % C::NK], uint32_t(jj / C::NK) & 1u, watch, SITE_DQ_K)) return false;
+        tc_fence_after();
+        const uint64_t kd = sdesc_adv(k_kdesc, uint32_t(jj % C::NK) * C::TILE_BYTES);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
           mma_ss_w(t_s, sdesc_adv(q_desc, off), sdesc_adv(kd, off), ID_SS, kk > 0 ? 1u : 0u);
         }
+        mma_commit_w(&bars->s_full);
+        return true;
       };
-      auto issue_dp = [=](int jj) {  // dP(jj) = dO V_jj^T
-        const uint64_t vd = sdesc_adv(kv_kdesc, slot_bytes(2 * jj + 1));
+      auto issue_dp = [&](int jj) {  // dP(jj) = dO V_jj^T into buffer jj % NDP
+        if (!fa_wait_warp(&bars->v_full[jj % C::NV], uint32_t(jj / C::NV) & 1u, watch, SITE_DQ_V)) return false;
+        tc_fence_after();
+        const uint64_t vd = sdesc_adv(v_kdesc, uint32_t(jj % C::NV) * C::TILE_BYTES);
+        const uint32_t dst = t_dp + uint32_t(jj % C::NDP) * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
-          mma_ss_w(t_dp, sdesc_adv(do_desc, off), sdesc_adv(vd, off), ID_SS, kk > 0 ? 1u : 0u);
+          mma_ss_w(dst, sdesc_adv(do_desc, off), sdesc_adv(vd, off), ID_SS, kk > 0 ? 1u : 0u);
         }
+        mma_commit_w(&bars->dp_full[jj % C::NDP]);
+        mma_commit_w(&bars->v_empty[jj % C::NV]);  // V_jj: only dP reads it
+        return true;
       };
-      bool ok = fa_wait_warp(&bars->q_full, 0, watch, SITE_DQ_Q) && wait_full(0, SITE_DQ_K);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-        mma_commit_w(&bars->s_full);
-      }
-      if (ok && (ok = wait_full(1, SITE_DQ_V))) {
-        tc_fence_after();
-        issue_dp(0);
-        mma_commit_w(&bars->dp_full);
-        mma_commit_w(&bars->kv_empty[1 % C::NSLOT]);  // V_0: only dP reads it
-      }
+      bool ok = fa_wait_warp(&bars->q_full, 0, watch, SITE_DQ_Q) && issue_s(0) && issue_dp(0);
       for (int jj = 0; jj < n_blocks && ok; ++jj) {
-        const bool more = jj + 1 < n_blocks;
-        if (more) {
+        if (jj + 1 < n_blocks) {
           if (!(ok = fa_wait_warp(&bars->s_free, uint32_t(jj) & 1u, watch, SITE_DQ_S))) break;
-          if (!(ok = wait_full(2 * (jj + 1), SITE_DQ_K))) break;
-          tc_fence_after();
-          issue_s(jj + 1);
-          mma_commit_w(&bars->s_full);
+          if (!(ok = issue_s(jj + 1) && issue_dp(jj + 1))) break;
         }
-        // dQ += dS K ; keys 16kk..16kk+15 of dS sit at dP columns 16kk+0..7
-        if (!(ok = fa_wait_warp(&bars->ds_ready, uint32_t(jj) & 1u, watch, SITE_DQ_DS))) break;
+        // dQ += dS K ; keys 16kk..16kk+15 of dS sit at its buffer's columns 16kk+0..7
+        const int pb = jj % C::NDP;
+        if (!(ok = fa_wait_warp(&bars->ds_ready[pb], uint32_t(jj / C::NDP) & 1u, watch, SITE_DQ_DS))) break;
         tc_fence_after();
         {
-          const uint64_t kd = sdesc_adv(kv_mdesc, slot_bytes(2 * jj));
+          const uint64_t kd = sdesc_adv(k_mdesc, uint32_t(jj % C::NK) * C::TILE_BYTES);
+          const uint32_t src = t_dp + uint32_t(pb) * 128;
           const uint32_t acc0 = jj > 0 ? 1u : 0u;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ts_w(t_dq, t_dp + kk * 16, sdesc_adv(kd, kk * 2048), ID_DQ, kk > 0 ? 1u : acc0);
+            mma_ts_w(t_dq, src + kk * 16, sdesc_adv(kd, kk * 2048), ID_DQ, kk > 0 ? 1u : acc0);
         }
-        mma_commit_w(&bars->kv_empty[(2 * jj) % C::NSLOT]);  // K_jj: read by S_jj and this dQ
-        if (more) {
-          if (!(ok = wait_full(2 * (jj + 1) + 1, SITE_DQ_V))) break;
-          tc_fence_after();
-          issue_dp(jj + 1);
-          mma_commit_w(&bars->dp_full);
-          mma_commit_w(&bars->kv_empty[(2 * (jj + 1) + 1) % C::NSLOT]);  // V_{jj+1}
-        }
+        mma_commit_w(&bars->k_empty[jj % C::NK]);  // K_jj: read by S_jj and this dQ
       }
       if (ok) {
         mma_commit_w(&bars->acc_done);
@@ -880,7 +895,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       float pv[C::COLS];
       tmem_ld_cols(tmem + lane_addr + C::T_S + w * C::COLS, pv);
       tc_fence_before();
-      mbar_arrive(&bars->s_free);
+      mbar_arrive_warp(&bars->s_free);
       const int kbase = (jb + jj) * 128;
       const bool need_mask = !(kbase >= tile_lo_max && kbase + 127 <= tile_hi_min);
       if (has_alibi) {
@@ -903,14 +918,15 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < C::COLS; ++c) pv[c] = (c >= lo && c <= hi) ? pv[c] : 0.0f;
       }
-      if (!(ok = fa_wait_warp(&bars->dp_full, uint32_t(jj) & 1u, watch, SITE_DQ_DP))) break;
+      const int pb = jj % C::NDP;
+      if (!(ok = fa_wait_warp(&bars->dp_full[pb], uint32_t(jj / C::NDP) & 1u, watch, SITE_DQ_DP))) break;
       tc_fence_after();
       // per 16-key chunk: load dP, form dS, store it as fp16 pairs over the chunk's
       // consumed dP columns (see the TMEM map)
 #pragma unroll
       for (int ch = 0; ch < C::COLS / 16; ++ch) {
         float dp[16];
-        const uint32_t col = tmem + lane_addr + C::T_DP + w * C::COLS + 16 * ch;
+        const uint32_t col = tmem + lane_addr + C::T_DP + uint32_t(pb) * 128 + w * C::COLS + 16 * ch;
         tmem_ld_cols(col, dp);
         uint32_t pk[8];
         uint32_t keep = 0;
@@ -932,7 +948,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->ds_ready);
+      mbar_arrive_warp(&bars->ds_ready[pb]);
     }
     // ------------------------------------------------------------ dQ epilogue (each group D/NCW columns)
     constexpr int SLICE = D / C::NCW;  // 16 or 32

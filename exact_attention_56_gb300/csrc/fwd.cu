@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->p_full[s], 128);
+      mbar_init(&bars->p_full[s], 4);  // one arrive per softmax warp
       mbar_init(&bars->pv_done[s], 1);
     }
     mbar_init(&bars->drain, 1);
@@ -409,7 +409,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->p_full[t]);
+      mbar_arrive_warp(&bars->p_full[t]);
     }
 
     // ------------------------------------------------------------ epilogue
