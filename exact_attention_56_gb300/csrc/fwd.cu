@@ -367,9 +367,13 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
       }
       l *= alpha;
       const float m_use = (m == -INFINITY) ? 0.0f : m;
-      // without ALiBi: p = 2^(x*sl - m); with ALiBi x is already in log2 units
+      // without ALiBi: p = 2^(x*sl - m); with ALiBi x is already in log2 units.
+      // Pairs of columns go through the paired f32x2 FMA and add (each lane
+      // rounds exactly as fmaf / + do); rs[k] sums the columns c with
+      // c % 4 == k.
       const float mul = has_alibi ? 1.0f : sl;
-      float rs[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      const uint64_t mul2 = f2_pack(mul, mul), nm2 = f2_pack(-m_use, -m_use);
+      uint64_t rs2[2] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f)};
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t pk[16];
@@ -377,10 +381,11 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int c = q4 * 32 + 2 * e;
-          float p0 = ex2_approx(fmaf(x[c], mul, -m_use));
-          float p1 = ex2_approx(fmaf(x[c + 1], mul, -m_use));
-          rs[(e & 1) * 2] += p0;
-          rs[(e & 1) * 2 + 1] += p1;
+          float a0, a1;
+          f2_unpack(f2_fma(f2_pack(x[c], x[c + 1]), mul2, nm2), a0, a1);
+          float p0 = ex2_approx(a0);
+          float p1 = ex2_approx(a1);
+          rs2[e & 1] = f2_add(rs2[e & 1], f2_pack(p0, p1));
           if (DROP) {
             if ((e & 1) == 0) keep = dropout_keep4(p.drop, b * p.H + h, i, (kbase + c) >> 2);
             const int sh = (c & 3);
@@ -391,6 +396,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
         }
         tmem_st_x16(tmem + lane_addr + sb * 128 + q4 * 16, pk);
       }
+      float rs[4];
+      f2_unpack(rs2[0], rs[0], rs[1]);
+      f2_unpack(rs2[1], rs[2], rs[3]);
       l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
       const bool rescale = alpha != 1.0f;
       if (__any_sync(0xffffffffu, rescale) && jj > 0) {
