@@ -8,7 +8,8 @@
 //
 // GB300 mapping (one CTA = NT query tiles of 128 rows of one (b, h)):
 //   warp 0        TMA producer: Q once, then K_j, V_j into a ring of smem slots
-//   warp 1        TMEM allocator and tcgen05.mma issuer (one thread):
+//   warp 1        TMEM allocator and tcgen05.mma issuer (the whole warp runs
+//                 the loop, one elected lane issues each MMA):
 //                   S_t = Q_t K_j^T  -> TMEM (fp32, 128 columns)
 //                   O_t += P_t V_j   -> TMEM (fp32, D columns), P_t read from TMEM
 //   warps 4..     one softmax warpgroup per query tile; thread r owns row r of
@@ -17,7 +18,10 @@
 //                 rescales its O row in TMEM when the running max moved by more
 //                 than 2^8, and finally normalises O and writes O and L.
 // The MMA order for NT = 2 interleaves the two tiles so each softmax group has
-// two MMAs' worth of time per K/V tile.
+// two MMAs' worth of time per K/V tile. At D = 64 a third S buffer fits in
+// TMEM; S of a tile's next K/V tile is then queued while its softmax still
+// runs, so each softmax group goes from one K/V tile to the next without
+// waiting for its PV and S MMAs.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -62,21 +66,28 @@ struct FwdCfg {
   static constexpr int BAR_OFF = KV_OFF + NSLOT * TILE_BYTES;
   static constexpr int SMEM_BYTES = BAR_OFF + 512 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t O_COL0 = 256;
-  static_assert(NT == 1 || 256 + NT * D <= 512, "TMEM budget");
+  // S buffers (128 columns each): two, or three where the TMEM budget allows
+  // (D = 64, two query tiles). With three, the n-th S tile (n = 2 j + t for
+  // key tile j, query tile t) uses buffer n % 3, so S of a query tile's next
+  // key tile is issued before that tile's softmax has finished.
+  static constexpr int NSB = (NT == 2 && D == 64) ? 3 : 2;
+  static constexpr uint32_t O_COL0 = NSB * 128;
+  static_assert(NT == 1 || O_COL0 + NT * D <= 512, "TMEM budget");
 };
 
 struct FwdBars {
   uint64_t q_full;
   uint64_t kv_full[8];
   uint64_t kv_empty[8];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t pv_done[2];
+  uint64_t s_full[3];   // per S buffer
+  uint64_t p_full[3];   // per S buffer (P is written over its S)
+  uint64_t pv_done[2];  // per query tile
+  uint64_t o_done[2];   // per query tile: one phase, after its last PV
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(FwdBars) <= 512, "barrier block");
 
 // Wait-site codes for the status word (kernel 1).
 enum : uint32_t {
@@ -148,10 +159,13 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::NSB; ++s) {
       mbar_init(&bars->s_full[s], 1);
       mbar_init(&bars->p_full[s], 4);  // one arrive per softmax warp
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->pv_done[s], 1);
+      mbar_init(&bars->o_done[s], 1);
     }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
@@ -231,6 +245,11 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
           mma_ss_w(ts, sdesc_adv(qd, off), sdesc_adv(kd, off), IDESC_S, kk > 0 ? 1u : 0u);
         }
       };
+      // The epilogue waits on o_done, which completes once, after the tile's last
+      // PV: pv_done can be more than one phase behind at that point.
+      auto last_pv = [&](int jj, int t) {
+        if (jj == n_blocks - 1) mma_commit_w(&bars->o_done[t]);
+      };
       auto issue_pv = [=](int jj, int t, int sbuf) {
         const uint64_t vd = sdesc_adv(kv_mdesc, uint32_t(slot_of(2 * jj + 1)) * C::TILE_BYTES);
         const uint32_t to = tmem + C::O_COL0 + uint32_t(t) * D, tp = tmem + uint32_t(sbuf) * 128;
@@ -241,7 +260,52 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
 
       bool ok = fa_wait_warp(&bars->q_full, 0, watch, SITE_MMA_Q);
       tc_fence_after();
-      if (NT == 2) {
+      if (NT == 2 && C::NSB == 3) {
+        // S tile n = 2 jj + t goes to buffer n % 3. Per key tile jj:
+        //   PV_0(jj), S_1(jj+1), PV_1(jj), S_0(jj+2).
+        // Each S overwrites the buffer whose P the PV just issued has read (in
+        // order), and S of a query tile's next key tile is already queued while
+        // its softmax runs.
+        auto s_tile = [&](int jj, int t) {  // S_t(jj) into its buffer
+          const int n = 2 * jj + t;
+          issue_s(jj, t, n % 3);
+          mma_commit_w(&bars->s_full[n % 3]);
+        };
+        auto pv_tile = [&](int jj, int t) {  // PV_t(jj) once its P is stored
+          const int n = 2 * jj + t;
+          if (!fa_wait_warp(&bars->p_full[n % 3], uint32_t(n / 3) & 1u, watch, SITE_MMA_P)) return false;
+          tc_fence_after();
+          issue_pv(jj, t, n % 3);
+          mma_commit_w(&bars->pv_done[t]);
+          last_pv(jj, t);
+          return true;
+        };
+        if ((ok = wait_full(0, SITE_MMA_K))) {
+          tc_fence_after();
+          s_tile(0, 0);
+          s_tile(0, 1);
+          mma_commit_w(&bars->kv_empty[slot_of(0)]);  // K_0: read by both S tiles
+          if (n_blocks > 1 && (ok = wait_full(2, SITE_MMA_K))) {
+            tc_fence_after();
+            s_tile(1, 0);
+          }
+        }
+        for (int jj = 0; jj < n_blocks && ok; ++jj) {
+          if (!(ok = wait_full(2 * jj + 1, SITE_MMA_V))) break;
+          if (!(ok = pv_tile(jj, 0))) break;
+          if (jj + 1 < n_blocks) {  // K_{jj+1} is already resident (S_0(jj+1) read it)
+            s_tile(jj + 1, 1);
+            mma_commit_w(&bars->kv_empty[slot_of(2 * (jj + 1))]);
+          }
+          if (!(ok = pv_tile(jj, 1))) break;
+          mma_commit_w(&bars->kv_empty[slot_of(2 * jj + 1)]);  // V_jj: read by both PV tiles
+          if (jj + 2 < n_blocks) {
+            if (!(ok = wait_full(2 * (jj + 2), SITE_MMA_K))) break;
+            tc_fence_after();
+            s_tile(jj + 2, 0);
+          }
+        }
+      } else if (NT == 2) {
         for (int jj = 0; jj < n_blocks && ok; ++jj) {
           if (!(ok = wait_full(2 * jj, SITE_MMA_K))) break;
           tc_fence_after();
@@ -252,6 +316,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
             tc_fence_after();
             issue_pv(jj - 1, 1, 1);
             mma_commit_w(&bars->pv_done[1]);
+            last_pv(jj - 1, 1);
             mma_commit_w(&bars->kv_empty[slot_of(2 * (jj - 1) + 1)]);
           }
           issue_s(jj, 1, 1);
@@ -262,6 +327,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
           tc_fence_after();
           issue_pv(jj, 0, 0);
           mma_commit_w(&bars->pv_done[0]);
+          last_pv(jj, 0);
         }
         if (ok) {
           const int jj = n_blocks - 1;
@@ -269,6 +335,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
             tc_fence_after();
             issue_pv(jj, 1, 1);
             mma_commit_w(&bars->pv_done[1]);
+            last_pv(jj, 1);
             mma_commit_w(&bars->kv_empty[slot_of(2 * jj + 1)]);
           }
         }
@@ -292,6 +359,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
           tc_fence_after();
           issue_pv(jj, 0, jj & 1);
           mma_commit_w(&bars->pv_done[0]);
+          last_pv(jj, 0);
           mma_commit_w(&bars->kv_empty[slot_of(2 * jj + 1)]);
         }
       }
@@ -322,8 +390,11 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
     float l = 0.0f;
     bool ok = true;
     for (int jj = 0; jj < n_blocks; ++jj) {
-      const int sb = (NT == 2) ? t : (jj & 1);
-      const uint32_t par = (NT == 2) ? (uint32_t(jj) & 1u) : (uint32_t(jj >> 1) & 1u);
+      // S buffer of this tile and the parity of its use (see FwdCfg::NSB)
+      const int n_s = 2 * jj + t;
+      const int sb = (C::NSB == 3) ? n_s % 3 : ((NT == 2) ? t : (jj & 1));
+      const uint32_t par = (C::NSB == 3) ? (uint32_t(n_s / 3) & 1u)
+                                         : ((NT == 2) ? (uint32_t(jj) & 1u) : (uint32_t(jj >> 1) & 1u));
       if (!(ok = fa_wait_warp(&bars->s_full[sb], par, watch, SITE_SM_S))) break;
       tc_fence_after();
       float x[128];
@@ -417,7 +488,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive_warp(&bars->p_full[t]);
+      mbar_arrive_warp(&bars->p_full[C::NSB == 3 ? sb : t]);
     }
 
     // ------------------------------------------------------------ epilogue
@@ -435,7 +506,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
         for (int e = 0; e < D / 8; ++e) dst[e] = z;
         p.lse[lrow] = -INFINITY;
       }
-    } else if (ok && fa_wait_warp(&bars->pv_done[t], uint32_t(n_blocks - 1) & 1u, watch, SITE_SM_EPI)) {
+    } else if (ok && fa_wait_warp(&bars->o_done[t], 0, watch, SITE_SM_EPI)) {
       tc_fence_after();
       const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
 #pragma unroll

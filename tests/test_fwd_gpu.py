@@ -46,14 +46,17 @@ def test_head_dims_ragged(D, causal):
     _run(2, 333, 333, 2, D, causal=causal, seed=10 + D)
 
 
-@pytest.mark.parametrize("Sq,Sk", [(77, 300), (300, 77), (1, 513), (257, 1), (130, 130)])
-def test_bottom_right_causal_rectangular(Sq, Sk):
-    _run(1, Sq, Sk, 3, 128, causal=True, seed=Sq * 7 + Sk)
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("Sq,Sk", [(77, 300), (300, 77), (1, 513), (257, 1), (130, 130), (200, 256)])
+def test_bottom_right_causal_rectangular(Sq, Sk, D):
+    _run(1, Sq, Sk, 3, D, causal=True, seed=Sq * 7 + Sk + D)
 
 
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("window", [(64, 0), (100, 37), (0, 0), (-1, 50), (300, -1)])
-def test_sliding_window(window):
-    _run(1, 500, 640, 2, 128, window=window, seed=sum(window) + 1000)
+def test_sliding_window(window, D):
+    # the live key range of a tile starts past key tile 0 for most rows
+    _run(1, 500, 640, 2, D, window=window, seed=sum(window) + 1000 + D)
 
 
 @pytest.mark.parametrize("causal", [False, True])
