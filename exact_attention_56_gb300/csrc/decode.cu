@@ -5,15 +5,18 @@
 // cache; the key range is cut into splits handled by separate thread blocks,
 // and a separate kernel merges the per-split results.
 //
-// Split kernel (one CTA per (split, head, batch x query row)); the caches are
-// dense (B, Sk, Hk, D) or pages addressed through a block table:
+// Split kernel (one CTA per (split, key/value head, batch, block of R query
+// pairs)): the Sq x group (query row, query head) pairs that read one key/value
+// head are served R at a time, so each K/V tile is read once for all of them
+// rather than once per query head and row. The caches are dense (B, Sk, Hk, D)
+// or pages addressed through a block table:
 //   warp 4      TMA producer: streams 32 KB stages (TK keys of K and of V,
 //               128-byte swizzled) through an mbarrier ring.
 //   warps 0..3  consumers: thread (g, c) owns 16-byte chunk c of the head dim
 //               and key lane g; a group of D/8 lanes shares one key at a time
-//               (dot product reduced with shuffles), keeps its own online
-//               softmax state (m, l) and its 8 output columns, and the groups
-//               are merged once at the end through shared memory.
+//               (dot products reduced with shuffles), keeps its own online
+//               softmax state (m, l) and its 8 output columns per query pair,
+//               and the groups are merged once at the end through shared memory.
 //   Output: per split the normalised partial O_s (fp32, D) and L_s (natural
 //   log) in the workspace; a split with no live key writes O_s = 0, L_s = -inf.
 // Merge kernel (one warp per (batch, query row, head)):
@@ -57,6 +60,7 @@ struct DecParams {
   int alibi_bstride;
   int B, Sq, Sk, H, n_splits;  // Sk: with a page table, the longest sequence
   int group;  // query heads per key/value head (H / Hk)
+  int n_rb;   // CTAs (row blocks) per key/value head: ceil(Sq * group / R)
   // Paged KV cache (page section "2.5：分页KV缓存"): NULL for the dense
   // (B, Sk, Hk, D) caches; else logical key block p of sequence b lives in page
   // block_table[b * max_pages + p] of (num_pages, page_size, Hk, D) caches and
@@ -95,7 +99,7 @@ __device__ __forceinline__ void named_bar_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-template <int D>
+template <int D, int R>
 __global__ void __launch_bounds__(DecCfg<D>::THREADS)
     fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                            const DecParams p) {
@@ -108,20 +112,40 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS)
   float* red_m = red_o + C::G * D;                               // [G]
   float* red_l = red_m + C::G;                                   // [G]
 
+  // This CTA serves up to R of the Sq x group (query row, query head) pairs
+  // that read key/value head hk; every K/V tile it loads is used by all of them.
   const int split = blockIdx.x;
-  const int h = blockIdx.y;
-  const int b = blockIdx.z / p.Sq;
-  const int i = blockIdx.z % p.Sq;
+  const int hk = blockIdx.y / p.n_rb;
+  const int rb = blockIdx.y % p.n_rb;
+  const int b = blockIdx.z;
+  const int n_pairs = p.Sq * p.group;
   // this sequence's keys, clamped to what the cache (or its page table) holds
   const int Sk = p.seqlens_k ? max(0, min(p.seqlens_k[b] + p.s_new, p.cap)) : p.Sk;
-  const RowRange rr = live_range(i, p.Sq, Sk, p.wl, p.wr);
-  // Splits cut the key range at whole tiles, so a tile never straddles a page;
-  // keys outside [ks, ke) (the live range clipped to this split) are masked.
+  // Splits cut the key range at whole tiles, so a tile never straddles a page.
+  // Row k sees keys [klo[k], khi[k]): its live range clipped to this split; the
+  // CTA streams the tiles covering the union of those ranges.
   const int n_all = (Sk + C::TK - 1) / C::TK;
-  int ks = int((long long)n_all * split / p.n_splits) * C::TK;
-  int ke = min(Sk, int((long long)n_all * (split + 1) / p.n_splits) * C::TK);  // exclusive
-  ks = max(ks, rr.lo);
-  ke = min(ke, rr.hi + 1);
+  const int s_lo = int((long long)n_all * split / p.n_splits) * C::TK;
+  const int s_hi = min(Sk, int((long long)n_all * (split + 1) / p.n_splits) * C::TK);  // exclusive
+  int ri[R], rh[R], klo[R], khi[R];
+  int ks = Sk, ke = 0;
+#pragma unroll
+  for (int k = 0; k < R; ++k) {
+    const int r = rb * R + k;
+    ri[k] = r / p.group;                  // query row
+    rh[k] = hk * p.group + r % p.group;   // query head
+    klo[k] = 1;
+    khi[k] = 0;
+    if (r < n_pairs) {
+      const RowRange rr = live_range(ri[k], p.Sq, Sk, p.wl, p.wr);
+      klo[k] = max(s_lo, rr.lo);
+      khi[k] = min(s_hi, rr.hi + 1);
+      if (khi[k] > klo[k]) {
+        ks = min(ks, klo[k]);
+        ke = max(ke, khi[k]);
+      }
+    }
+  }
   const int t0 = (ks / C::TK) * C::TK;  // first tile, aligned
   const int n_tiles = ke > ks ? (ke - t0 + C::TK - 1) / C::TK : 0;
 
@@ -135,8 +159,6 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS)
   }
   __syncthreads();
   const Watch watch{&bars->abort, p.status};
-
-  const size_t pidx = ((size_t(b) * p.Sq + i) * p.H + h) * p.n_splits + split;
 
   if (threadIdx.x >= 128) {
     // ------------------------------------------------------------ producer
@@ -157,8 +179,8 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS)
         }
 #pragma unroll
         for (int pn = 0; pn < C::PANELS; ++pn) {
-          tma_load_4d(st + pn * C::PANEL_BYTES, &tm_k, &bars->full[s], pn * 64, h / p.group, row, tb);
-          tma_load_4d(st + C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_v, &bars->full[s], pn * 64, h / p.group, row, tb);
+          tma_load_4d(st + pn * C::PANEL_BYTES, &tm_k, &bars->full[s], pn * 64, hk, row, tb);
+          tma_load_4d(st + C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_v, &bars->full[s], pn * 64, hk, row, tb);
         }
         issued = t + 1;
       }
@@ -180,29 +202,39 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS)
   const int tid = threadIdx.x;
   const int c = tid % C::CH;
   const int g = tid / C::CH;
-  float qf[8];
-  {
-    const __nv_bfloat16* qrow = p.q + ((size_t(b) * p.Sq + i) * p.H + h) * D;
-    bf16x8_to_f32(*reinterpret_cast<const uint4*>(qrow + c * 8), qf);
+  const bool has_alibi = p.alibi != nullptr;
+  float qf[R][8], slope_log2[R];
+  int c_i[R];
+#pragma unroll
+  for (int k = 0; k < R; ++k) {
+    c_i[k] = ri[k] + Sk - p.Sq;
+    slope_log2[k] = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) qf[k][e] = 0.0f;
+    if (khi[k] <= klo[k]) continue;  // no live key in this split (or no such pair)
+    const __nv_bfloat16* qrow = p.q + ((size_t(b) * p.Sq + ri[k]) * p.H + rh[k]) * D;
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(qrow + c * 8), qf[k]);
     if (p.rot.cos != nullptr && c * 8 < p.rot.dim) {  // rotary at the row's diagonal position
       float pq[8];
       if (!p.rot.interleaved)
         bf16x8_to_f32(*reinterpret_cast<const uint4*>(qrow + rotary_partner(c * 8, p.rot)), pq);
-      rotary8(qf, pq, c * 8, i + Sk - p.Sq, p.rot);
+      rotary8(qf[k], pq, c * 8, c_i[k], p.rot);
     }
 #pragma unroll
-    for (int e = 0; e < 8; ++e) qf[e] *= p.scale_log2;
+    for (int e = 0; e < 8; ++e) qf[k][e] *= p.scale_log2;
+    if (has_alibi) slope_log2[k] = p.alibi[b * p.alibi_bstride + rh[k]] * 1.4426950408889634f;
   }
-  const bool has_alibi = p.alibi != nullptr;
-  const float slope_log2 = has_alibi ? p.alibi[b * p.alibi_bstride + h] * 1.4426950408889634f : 0.0f;
-  const int c_i = i + Sk - p.Sq;
   const int pn = c / 8;
   const int cc = c % 8;
 
-  float m = -INFINITY, l = 0.0f;
-  float o[8];
+  float m[R], l[R], o[R][8];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) o[e] = 0.0f;
+  for (int k = 0; k < R; ++k) {
+    m[k] = -INFINITY;
+    l[k] = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[k][e] = 0.0f;
+  }
 
   for (int t = 0; t < n_tiles; ++t) {
     const int s = t % C::NSTAGE;
@@ -210,77 +242,96 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS)
     const uint8_t* kt = smem + s * C::STAGE_BYTES + pn * C::PANEL_BYTES;
     const uint8_t* vt = kt + C::TILE_BYTES;
     const int row0 = t0 + t * C::TK;
-    float sc[C::KPL];
+    float sc[R][C::KPL];
 #pragma unroll
     for (int u = 0; u < C::KPL; ++u) {
       const int kr = g + C::G * u;
       const uint4 kv = *reinterpret_cast<const uint4*>(kt + kr * 128 + ((cc ^ (kr & 7)) << 4));
       float kf[8];
       bf16x8_to_f32(kv, kf);
-      float d = 0.0f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) d = fmaf(qf[e], kf[e], d);
-#pragma unroll
-      for (int off = C::CH / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
       const int kj = row0 + kr;
-      if (has_alibi) d -= slope_log2 * fabsf(float(c_i - kj));
-      sc[u] = (kj >= ks && kj < ke) ? d : -INFINITY;
-    }
-    float mt = sc[0];
 #pragma unroll
-    for (int u = 1; u < C::KPL; ++u) mt = fmaxf(mt, sc[u]);
-    const float m_new = fmaxf(m, mt);
-    if (m_new != -INFINITY) {
-      if (m == -INFINITY) {
-        m = m_new;
-      } else if (m_new > m + 8.0f) {
-        const float alpha = ex2_approx(m - m_new);
-        l *= alpha;
+      for (int k = 0; k < R; ++k) {
+        float d = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] *= alpha;
-        m = m_new;
+        for (int e = 0; e < 8; ++e) d = fmaf(qf[k][e], kf[e], d);
+#pragma unroll
+        for (int off = C::CH / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+        if (has_alibi) d -= slope_log2[k] * fabsf(float(c_i[k] - kj));
+        sc[k][u] = (kj >= klo[k] && kj < khi[k]) ? d : -INFINITY;
       }
     }
-    const float m_use = (m == -INFINITY) ? 0.0f : m;
+    float m_use[R];
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+      float mt = sc[k][0];
+#pragma unroll
+      for (int u = 1; u < C::KPL; ++u) mt = fmaxf(mt, sc[k][u]);
+      const float m_new = fmaxf(m[k], mt);
+      if (m_new != -INFINITY) {
+        if (m[k] == -INFINITY) {
+          m[k] = m_new;
+        } else if (m_new > m[k] + 8.0f) {
+          const float alpha = ex2_approx(m[k] - m_new);
+          l[k] *= alpha;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[k][e] *= alpha;
+          m[k] = m_new;
+        }
+      }
+      m_use[k] = (m[k] == -INFINITY) ? 0.0f : m[k];
+    }
 #pragma unroll
     for (int u = 0; u < C::KPL; ++u) {
       const int kr = g + C::G * u;
-      const float pu = ex2_approx(sc[u] - m_use);
-      l += pu;
       const uint4 vv = *reinterpret_cast<const uint4*>(vt + kr * 128 + ((cc ^ (kr & 7)) << 4));
       float vf[8];
       bf16x8_to_f32(vv, vf);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = fmaf(pu, vf[e], o[e]);
+      for (int k = 0; k < R; ++k) {
+        const float pu = ex2_approx(sc[k][u] - m_use[k]);
+        l[k] += pu;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[k][e] = fmaf(pu, vf[e], o[k][e]);
+      }
     }
     mbar_arrive(&bars->empty[s]);
   }
 
-  // Merge the G key lanes of this CTA.
-  if (c == 0) {
-    red_m[g] = m;
-    red_l[g] = l;
+  // Merge the G key lanes of this CTA, one row at a time through shared memory.
+#pragma unroll
+  for (int k = 0; k < R; ++k) {
+    const int r = rb * R + k;
+    if (c == 0) {
+      red_m[g] = m[k];
+      red_l[g] = l[k];
+    }
+    named_bar_sync(1, 128);
+    float M = -INFINITY;
+#pragma unroll
+    for (int gg = 0; gg < C::G; ++gg) M = fmaxf(M, red_m[gg]);
+    const float Ms = (M == -INFINITY) ? 0.0f : M;
+    const float wg = (m[k] == -INFINITY) ? 0.0f : ex2_approx(m[k] - Ms);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) red_o[g * D + c * 8 + e] = o[k][e] * wg;
+    named_bar_sync(1, 128);
+    if (r < n_pairs) {  // a split with no live key for this row writes O_s = 0, L_s = -inf
+      float L = 0.0f;
+#pragma unroll
+      for (int gg = 0; gg < C::G; ++gg)
+        L += (red_m[gg] == -INFINITY) ? 0.0f : red_l[gg] * ex2_approx(red_m[gg] - Ms);
+      const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+      const size_t pidx = ((size_t(b) * p.Sq + ri[k]) * p.H + rh[k]) * p.n_splits + split;
+      for (int d = tid; d < D; d += 128) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int gg = 0; gg < C::G; ++gg) acc += red_o[gg * D + d];
+        p.part_o[pidx * D + d] = acc * inv;
+      }
+      if (tid == 0) p.part_l[pidx] = L > 0.0f ? (M + lg2_approx(L)) * 0.6931471805599453f : -INFINITY;
+    }
+    named_bar_sync(1, 128);  // red_* are reused by the next row
   }
-  named_bar_sync(1, 128);
-  float M = -INFINITY;
-#pragma unroll
-  for (int gg = 0; gg < C::G; ++gg) M = fmaxf(M, red_m[gg]);
-  const float Ms = (M == -INFINITY) ? 0.0f : M;
-  const float wg = (m == -INFINITY) ? 0.0f : ex2_approx(m - Ms);
-#pragma unroll
-  for (int e = 0; e < 8; ++e) red_o[g * D + c * 8 + e] = o[e] * wg;
-  named_bar_sync(1, 128);
-  float L = 0.0f;
-#pragma unroll
-  for (int gg = 0; gg < C::G; ++gg) L += (red_m[gg] == -INFINITY) ? 0.0f : red_l[gg] * ex2_approx(red_m[gg] - Ms);
-  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-  for (int d = tid; d < D; d += 128) {
-    float acc = 0.0f;
-#pragma unroll
-    for (int gg = 0; gg < C::G; ++gg) acc += red_o[gg * D + d];
-    p.part_o[pidx * D + d] = acc * inv;
-  }
-  if (tid == 0) p.part_l[pidx] = L > 0.0f ? (M + lg2_approx(L)) * 0.6931471805599453f : -INFINITY;
 }
 
 // Appends s_new rows of k_new, v_new (B, s_new, Hk, D) to the cache at
@@ -423,11 +474,17 @@ size_t decode_workspace_bytes(int B, int Sq, int H, int D, int n) {
   return align256(units * D * 4) + align256(units * 4);
 }
 
+// Query pairs a split CTA serves: up to four, as many as one key/value head has.
+static int decode_rows_per_cta(int Sq, int H, int Hk) {
+  const int pairs = Sq * (H / Hk);
+  return pairs >= 4 ? 4 : (pairs >= 2 ? 2 : 1);
+}
+
 int decode_auto_splits(int B, int Sq, int Sk, int H, int Hk, int D) {
-  (void)Hk;  // one split CTA per query head and row
   const int tk = (D == 64) ? 128 : (D == 128 ? 64 : 32);
   const long long slots = 2LL * device_sm_count();  // two split CTAs fit per SM
-  const long long units = (long long)B * Sq * H;
+  const int rpc = decode_rows_per_cta(Sq, H, Hk);
+  const long long units = (long long)B * Hk * ((Sq * (H / Hk) + rpc - 1) / rpc);  // CTAs per split
   int max_n = (Sk + 4 * tk - 1) / (4 * tk);  // at least four tiles per split
   if (max_n < 1) max_n = 1;
   if (max_n > 256) max_n = 256;
@@ -457,7 +514,8 @@ static int launch_decode_t(const AttnShape& s, const void* q, const void* k, con
   CUtensorMap mk, mv;
   if (!make_bshd_map(&mk, k, mb, mrows, s.Hk, D, C::TK) || !make_bshd_map(&mv, v, mb, mrows, s.Hk, D, C::TK))
     return FA_ERR_CUDA;
-  auto kern = fa_decode_split_kernel<D>;
+  const int rpc = decode_rows_per_cta(s.Sq, s.H, s.Hk);
+  auto kern = rpc == 4 ? fa_decode_split_kernel<D, 4> : (rpc == 2 ? fa_decode_split_kernel<D, 2> : fa_decode_split_kernel<D, 1>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
     return FA_ERR_CUDA;
   DecParams p;
@@ -472,6 +530,7 @@ static int launch_decode_t(const AttnShape& s, const void* q, const void* k, con
   p.Sk = s.Sk;
   p.H = s.H;
   p.group = s.H / s.Hk;
+  p.n_rb = (s.Sq * p.group + rpc - 1) / rpc;
   p.block_table = cg ? cg->block_table : nullptr;
   p.seqlens_k = cg ? cg->seqlens : nullptr;
   p.page_size = cg ? cg->page_size : 0;
@@ -485,8 +544,8 @@ static int launch_decode_t(const AttnShape& s, const void* q, const void* k, con
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.status = device_status_word();
   if (!p.status) return FA_ERR_CUDA;
-  if ((long long)s.B * s.Sq > 65535 || s.H > 65535) return FA_ERR_UNSUPPORTED;
-  dim3 grid(n, s.H, s.B * s.Sq);
+  if (s.B > 65535 || (long long)s.Hk * p.n_rb > 65535) return FA_ERR_UNSUPPORTED;
+  dim3 grid(n, s.Hk * p.n_rb, s.B);
   kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mk, mv, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   const int warps = s.B * s.Sq * s.H;

@@ -142,6 +142,33 @@ def test_decode_groups(Hk, D, Sq):
         assert_lse_close(lse.cpu().numpy().astype(np.float64), l_ref, f"L (splits {n})")
 
 
+@pytest.mark.parametrize("H,Hk,Sq", [(6, 2, 1), (6, 2, 3), (4, 4, 3), (16, 1, 2), (12, 4, 2)])
+def test_decode_query_pairs_share_a_cta(H, Hk, Sq):
+    # A split CTA serves up to four (query row, query head) pairs of one key/value
+    # head. These shapes leave partial blocks (3 or 9 pairs), mix query rows with
+    # different causal limits in one block, and put 32 pairs on one head (MQA).
+    import torch
+
+    import exact_attention_56_gb300 as fa
+
+    B, Sk, D = 2, 777, 128
+    inp = _inputs(B, Sq, Sk, H, Hk, D, 350 + H + Hk + Sq)
+    q, k, v = (to_dev(inp[n]) for n in ("q", "k", "v"))
+    f64 = [bf16_bits_to_f64(inp[x]) for x in ("q", "k", "v")]
+    cases = [dict(causal=True), dict(causal=False, window=(100, 0), alibi=alibi_slopes_geometric(H))]
+    for case in cases:
+        window, alibi = case.get("window", (-1, -1)), case.get("alibi")
+        for n in (0, 1, 5):
+            out, lse = fa.fa_decode_splitkv(q, k, v, causal=case["causal"], window_size=window,
+                                            alibi_slopes=_alibi(alibi, q.device), num_splits=n)
+            torch.cuda.synchronize()
+            st, word = fa.fa_device_status()
+            assert st == fa.FA_OK, hex(word)
+            o_ref, l_ref = oracle.attention_fwd(*f64, None, case["causal"], window, alibi)
+            assert_bf16_close(to_f64(out), o_ref, f"O ({case}, splits {n})")
+            assert_lse_close(lse.cpu().numpy().astype(np.float64), l_ref, f"L ({case}, splits {n})")
+
+
 def test_binding_rejects_heads_that_do_not_divide():
     import torch
 
