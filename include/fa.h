@@ -189,7 +189,9 @@ size_t fa_decode_workspace_size(int B, int Sq, int Sk, int H, int Hk, int D, int
  * Split-KV decode for short queries (section "2.2：针对推理进行优化": the
  * key/value loading is split across thread blocks and a separate kernel
  * merges the results). q (B,Sq,H,D) with 1 <= Sq <= 16; k_cache, v_cache
- * (B,Sk,H,D) contiguous. Each split writes its normalised partial output and
+ * (B,Sk,Hk,D) contiguous, Hk dividing H (query head h reads key/value head
+ * h / (H / Hk)); a split thread block serves up to four (query row, query
+ * head) pairs of one key/value head. Each split writes its normalised partial output and
  * logsumexp to the workspace; the combine kernel merges them exactly,
  * L = log sum_s exp(L_s), O = sum_s exp(L_s - L) O_s, and writes out (bf16)
  * and lse (fp32) in the fa_fwd layouts. Masks and ALiBi as in fa_fwd.
