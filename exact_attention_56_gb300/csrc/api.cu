@@ -63,11 +63,16 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool make_bshd_map(CUtensorMap* map, const void* base, int B, int S, int H, int D, int box_rows, bool f16) {
+  return make_bshd_map_box(map, base, B, S, H, D, 1, box_rows, f16);
+}
+
+bool make_bshd_map_box(CUtensorMap* map, const void* base, int B, int S, int H, int D, int box_heads, int box_rows,
+                       bool f16) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[4] = {cuuint64_t(D), cuuint64_t(H), cuuint64_t(S), cuuint64_t(B)};
   cuuint64_t strides[3] = {cuuint64_t(D) * 2, cuuint64_t(H) * D * 2, cuuint64_t(S) * H * D * 2};
-  cuuint32_t box[4] = {64, 1, cuuint32_t(box_rows), 1};
+  cuuint32_t box[4] = {64, cuuint32_t(box_heads), cuuint32_t(box_rows), 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

@@ -60,7 +60,8 @@ struct DecParams {
   int alibi_bstride;
   int B, Sq, Sk, H, n_splits;  // Sk: with a page table, the longest sequence
   int group;  // query heads per key/value head (H / Hk)
-  int n_rb;   // CTAs (row blocks) per key/value head: ceil(Sq * group / R)
+  int n_rb;   // CTAs (row blocks) per key/value head and split
+  int rows_i; // tensor-core kernel: query rows per block (rows_i * group <= 128)
   // Paged KV cache (page section "2.5：分页KV缓存"): NULL for the dense
   // (B, Sk, Hk, D) caches; else logical key block p of sequence b lives in page
   // block_table[b * max_pages + p] of (num_pages, page_size, Hk, D) caches and
@@ -334,6 +335,343 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS)
   }
 }
 
+
+// ============================================================================ grouped decode on tensor cores
+// The (query row, query head) pairs that read one key/value head are the rows
+// of one 128-row MMA tile (row r: query row i0 + r / group, query head
+// hk * group + r % group, one TMA box of group heads x rows_i rows). Per key
+// tile, as in the forward kernel: S = Q K^T into TMEM (two buffers), an online
+// softmax with one thread per row (its own mask, ALiBi slope and diagonal),
+// P (bf16) written over S, O += P V. Each K/V tile is read once for all the
+// pairs; the split's normalised O_s and L_s go to the same partials the merge
+// kernel reads.
+template <int D>
+struct DecMmaCfg {
+  static constexpr int PANELS = D / 64;
+  static constexpr int PANEL_BYTES = 128 * 128;
+  static constexpr int TILE_BYTES = PANELS * PANEL_BYTES;  // 128 rows (or keys) x D
+  static constexpr int TK = 128;                           // keys per tile
+  static constexpr int NSLOT = D == 64 ? 8 : (D == 128 ? 6 : 2);  // ring of K_j, V_j tiles
+  static constexpr int THREADS = 256;                      // producer, MMA, 2 idle, 4 softmax warps
+  static constexpr int Q_OFF = 0;
+  static constexpr int KV_OFF = TILE_BYTES;
+  static constexpr int BAR_OFF = KV_OFF + NSLOT * TILE_BYTES;
+  static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;  // + alignment slack
+  static constexpr uint32_t O_COL0 = 256;                  // TMEM: S buffers at 0 and 128, O after
+  static_assert(O_COL0 + D <= 512, "TMEM budget");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+struct DecMmaBars {
+  uint64_t q_full;
+  uint64_t kv_full[8], kv_empty[8];
+  uint64_t s_full[2], p_full[2];  // per S buffer (P is written over its S)
+  uint64_t pv_done, o_done, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(DecMmaBars) <= 256, "barrier block");
+
+enum : uint32_t {
+  SITE_DM_EMPTY = 0x61,
+  SITE_DM_Q = 0x62,
+  SITE_DM_K = 0x63,
+  SITE_DM_V = 0x64,
+  SITE_DM_P = 0x65,
+  SITE_DM_S = 0x66,
+  SITE_DM_PV = 0x67,
+  SITE_DM_EPI = 0x68,
+};
+
+// Timeout-only wait used while draining after an abort.
+__device__ __forceinline__ void dm_drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) return;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(DecMmaCfg<D>::THREADS, 1)
+    fa_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const DecParams p) {
+  using C = DecMmaCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  DecMmaBars* bars = reinterpret_cast<DecMmaBars*>(smem + C::BAR_OFF);
+  const int warp = int(warp_id());
+  const int lane = int(lane_id());
+
+  const int split = blockIdx.x;
+  const int hk = blockIdx.y / p.n_rb;
+  const int rb = blockIdx.y % p.n_rb;
+  const int b = blockIdx.z;
+  const int i0 = rb * p.rows_i;                   // first query row of this block
+  const int i1 = min(p.Sq, i0 + p.rows_i) - 1;    // last
+  // this sequence's keys, clamped to what the cache (or its page table) holds
+  const int Sk = p.seqlens_k ? max(0, min(p.seqlens_k[b] + p.s_new, p.cap)) : p.Sk;
+  // The split's whole tiles; the rows' live bounds grow with the row, so the
+  // first and last rows bound the keys any row of the block can see.
+  const int n_all = (Sk + C::TK - 1) / C::TK;
+  const int s_lo = int((long long)n_all * split / p.n_splits) * C::TK;
+  const int s_hi = min(Sk, int((long long)n_all * (split + 1) / p.n_splits) * C::TK);  // exclusive
+  const int ks = max(s_lo, live_range(i0, p.Sq, Sk, p.wl, p.wr).lo);
+  const int ke = min(s_hi, live_range(i1, p.Sq, Sk, p.wl, p.wr).hi + 1);
+  const int t0 = (ks / C::TK) * C::TK;
+  const int n_blocks = ke > ks ? (ke - t0 + C::TK - 1) / C::TK : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < C::NSLOT; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->p_full[s], 4);  // one arrive per softmax warp
+    }
+    mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const Watch watch{&bars->abort, p.status};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // The whole warp runs the loop; one elected lane issues each copy.
+    if (n_blocks > 0) {
+      tma_prefetch_desc_w(&tm_q);
+      tma_prefetch_desc_w(&tm_k);
+      tma_prefetch_desc_w(&tm_v);
+      // one box per 64-column panel: group heads x rows_i query rows (rows past
+      // Sq read zeros); the tile's rows past group * rows_i are never read back
+      mbar_arrive_expect_tx_w(&bars->q_full, C::PANELS * 128 * p.group * p.rows_i);
+      for (int pn = 0; pn < C::PANELS; ++pn)
+        tma_load_4d_w(smem + C::Q_OFF + pn * C::PANEL_BYTES, &tm_q, &bars->q_full, pn * 64, hk * p.group, i0, b);
+      int issued = 0;
+      bool ok = true;
+      for (int jj = 0; jj < n_blocks && ok; ++jj) {
+        int row = t0 + jj * C::TK, tb = b;
+        if (p.block_table) {  // (row in page, page) coordinates of this tile
+          tb = p.block_table[size_t(b) * p.max_pages + row / p.page_size];
+          row %= p.page_size;
+        }
+        for (int kv = 0; kv < 2; ++kv) {
+          const int it = 2 * jj + kv;
+          const int s = it % C::NSLOT;
+          if (!fa_wait_warp(&bars->kv_empty[s], (uint32_t(it / C::NSLOT) & 1u) ^ 1u, watch, SITE_DM_EMPTY)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx_w(&bars->kv_full[s], C::TILE_BYTES);
+          const CUtensorMap* m = kv ? &tm_v : &tm_k;
+          for (int pn = 0; pn < C::PANELS; ++pn)
+            tma_load_4d_w(smem + C::KV_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, m, &bars->kv_full[s],
+                          pn * 64, hk, row, tb);
+          issued = it + 1;
+        }
+      }
+      if (!ok) {  // let the copies in flight land before the CTA leaves
+        dm_drain_wait(&bars->q_full, 0);
+        for (int it = (issued > C::NSLOT ? issued - C::NSLOT : 0); it < issued; ++it)
+          dm_drain_wait(&bars->kv_full[it % C::NSLOT], uint32_t(it / C::NSLOT) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    // S(jj+1) into the other S buffer as soon as K(jj+1) is in; PV(jj) once P(jj)
+    // is stored. S(jj+1) overwrites P(jj-1), which PV(jj-1) has read (in order).
+    // The whole warp runs the loop; one elected lane issues each MMA and commit.
+    if (n_blocks > 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
+      constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);    // P from TMEM, V MN-major
+      const uint64_t q_desc = sdesc_sw128(smem_u32(smem + C::Q_OFF), 16, 1024);
+      const uint64_t kv_kdesc = sdesc_sw128(smem_u32(smem + C::KV_OFF), 16, 1024);
+      const uint64_t kv_mdesc = sdesc_sw128(smem_u32(smem + C::KV_OFF), C::PANEL_BYTES, 1024);
+      auto slot_of = [](int it) { return it % C::NSLOT; };
+      auto wait_full = [&](int it, uint32_t site) {
+        return fa_wait_warp(&bars->kv_full[slot_of(it)], uint32_t(it / C::NSLOT) & 1u, watch, site);
+      };
+      auto issue_s = [&](int jj) {
+        const uint64_t kd = sdesc_adv(kv_kdesc, uint32_t(slot_of(2 * jj)) * C::TILE_BYTES);
+        const uint32_t ts = tmem + uint32_t(jj & 1) * 128;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
+          mma_ss_w(ts, sdesc_adv(q_desc, off), sdesc_adv(kd, off), IDESC_S, kk > 0 ? 1u : 0u);
+        }
+        mma_commit_w(&bars->s_full[jj & 1]);
+        mma_commit_w(&bars->kv_empty[slot_of(2 * jj)]);
+      };
+      bool ok = fa_wait_warp(&bars->q_full, 0, watch, SITE_DM_Q) && wait_full(0, SITE_DM_K);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+      }
+      for (int jj = 0; jj < n_blocks && ok; ++jj) {
+        if (jj + 1 < n_blocks) {
+          if (!(ok = wait_full(2 * (jj + 1), SITE_DM_K))) break;
+          tc_fence_after();
+          issue_s(jj + 1);
+        }
+        if (!(ok = wait_full(2 * jj + 1, SITE_DM_V))) break;
+        // per-buffer P barriers: S(jj+1) is queued before this wait, so the softmax
+        // may finish tile jj+1 before it; its next use needs S(jj+2), issued later
+        if (!(ok = fa_wait_warp(&bars->p_full[jj & 1], uint32_t(jj >> 1) & 1u, watch, SITE_DM_P))) break;
+        tc_fence_after();
+        const uint64_t vd = sdesc_adv(kv_mdesc, uint32_t(slot_of(2 * jj + 1)) * C::TILE_BYTES);
+        const uint32_t to = tmem + C::O_COL0, tp = tmem + uint32_t(jj & 1) * 128;
+        const uint32_t acc0 = jj > 0 ? 1u : 0u;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ts_w(to, tp + kk * 8, sdesc_adv(vd, kk * 2048), IDESC_O, kk > 0 ? 1u : acc0);
+        mma_commit_w(&bars->pv_done);
+        if (jj == n_blocks - 1) mma_commit_w(&bars->o_done);
+        mma_commit_w(&bars->kv_empty[slot_of(2 * jj + 1)]);
+      }
+      if (!ok) {  // let issued MMAs finish before TMEM is released
+        mma_commit_w(&bars->drain);
+        dm_drain_wait(&bars->drain, 0);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax (thread = pair)
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_addr = uint32_t(wq * 32) << 16;
+    const int i = i0 + r / p.group;               // query row of this pair
+    const int h = hk * p.group + r % p.group;     // query head of this pair
+    const bool pair_ok = r < p.rows_i * p.group && i < p.Sq;
+    // this pair's keys: its live range clipped to the split
+    int klo = 1, khi = 0;
+    if (pair_ok) {
+      const RowRange rr = live_range(i, p.Sq, Sk, p.wl, p.wr);
+      klo = max(s_lo, rr.lo);
+      khi = min(s_hi, rr.hi + 1);
+    }
+    const bool has_alibi = p.alibi != nullptr;
+    const float slope_log2 = (has_alibi && pair_ok) ? p.alibi[b * p.alibi_bstride + h] * 1.4426950408889634f : 0.0f;
+    const int c_i = i + Sk - p.Sq;
+    const float sl = p.scale_log2;
+
+    float m = -INFINITY;  // reference max (log2 units) the running O and l are relative to
+    float l = 0.0f;
+    bool ok = true;
+    for (int jj = 0; jj < n_blocks; ++jj) {
+      if (!(ok = fa_wait_warp(&bars->s_full[jj & 1], uint32_t(jj >> 1) & 1u, watch, SITE_DM_S))) break;
+      tc_fence_after();
+      float x[128];
+      tmem_ld_x128f(tmem + lane_addr + uint32_t(jj & 1) * 128, x);
+      const int kbase = t0 + jj * C::TK;
+      // x = scale*log2(e)*qk - slope*log2(e)*|c(i) - j| in log2 units; keys outside [klo, khi) masked
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const int j = kbase + c;
+        float v = x[c] * sl;
+        if (has_alibi) v -= slope_log2 * fabsf(float(c_i - j));
+        x[c] = (j >= klo && j < khi) ? v : -INFINITY;
+      }
+      float mq[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mq[k] = fmaxf(x[2 * k], x[2 * k + 1]);
+#pragma unroll
+      for (int c = 8; c < 128; c += 8) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mq[k] = max3f(mq[k], x[c + 2 * k], x[c + 2 * k + 1]);
+      }
+      const float m_blk = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      const float m_new = fmaxf(m, m_blk);
+      float alpha = 1.0f;
+      if (m_new != -INFINITY) {
+        if (m == -INFINITY) {
+          m = m_new;  // first live key: O and l are still exactly 0
+        } else if (m_new > m + 8.0f) {
+          alpha = ex2_approx(m - m_new);
+          m = m_new;
+        }
+      }
+      l *= alpha;
+      const float m_use = (m == -INFINITY) ? 0.0f : m;
+      float rs = 0.0f;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c = q4 * 32 + 2 * e;
+          const float p0 = ex2_approx(x[c] - m_use);
+          const float p1 = ex2_approx(x[c + 1] - m_use);
+          rs += p0 + p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st_x16(tmem + lane_addr + uint32_t(jj & 1) * 128 + q4 * 16, pk);
+      }
+      l += rs;
+      if (__any_sync(0xffffffffu, alpha != 1.0f) && jj > 0) {
+        // O must hold P_{j-1} V_{j-1} before it is rescaled (P_j is already in TMEM).
+        if (!(ok = fa_wait_warp(&bars->pv_done, uint32_t(jj - 1) & 1u, watch, SITE_DM_PV))) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          const uint32_t oa = tmem + lane_addr + C::O_COL0 + cc * 32;
+          tmem_ld_x32(oa, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st_x32(oa, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive_warp(&bars->p_full[jj & 1]);
+    }
+
+    // ------------------------------------------------------------ partials of this split
+    const size_t pidx = ((size_t(b) * p.Sq + (pair_ok ? i : 0)) * p.H + h) * p.n_splits + split;
+    if (n_blocks == 0) {
+      if (pair_ok) {
+        for (int d = 0; d < D; ++d) p.part_o[pidx * D + d] = 0.0f;
+        p.part_l[pidx] = -INFINITY;
+      }
+    } else if (ok && fa_wait_warp(&bars->o_done, 0, watch, SITE_DM_EPI)) {
+      tc_fence_after();
+      const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld_x32(tmem + lane_addr + C::O_COL0 + cc * 32, o);
+        if (pair_ok) {
+          float4* dst = reinterpret_cast<float4*>(p.part_o + pidx * D + cc * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
+                                 __uint_as_float(o[4 * e + 2]) * inv, __uint_as_float(o[4 * e + 3]) * inv);
+        }
+      }
+      if (pair_ok) p.part_l[pidx] = (l > 0.0f) ? (m + lg2_approx(l)) * 0.6931471805599453f : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // Appends s_new rows of k_new, v_new (B, s_new, Hk, D) to the cache at
 // positions seqlens[b] + s, the keys rotated at their positions (page section
 // "2.2": flash_attn_with_kvcache updates the KV cache in place and applies
@@ -480,11 +818,25 @@ static int decode_rows_per_cta(int Sq, int H, int Hk) {
   return pairs >= 4 ? 4 : (pairs >= 2 ? 2 : 1);
 }
 
+// The tensor-core kernel serves a key/value head's pairs as the rows of one
+// MMA tile: worth it from 8 pairs on, possible while one query row's group
+// heads fit the 128 rows.
+static bool decode_mma_ok(int Sq, int H, int Hk) {
+  const int g = H / Hk;
+  return g <= 128 && Sq * g >= 8;
+}
+static int decode_mma_rows(int Sq, int H, int Hk) {  // query rows per block
+  return std::min(Sq, 128 / (H / Hk));
+}
+
 int decode_auto_splits(int B, int Sq, int Sk, int H, int Hk, int D) {
-  const int tk = (D == 64) ? 128 : (D == 128 ? 64 : 32);
-  const long long slots = 2LL * device_sm_count();  // two split CTAs fit per SM
+  const bool mma = decode_mma_ok(Sq, H, Hk);
+  const int tk = mma ? 128 : ((D == 64) ? 128 : (D == 128 ? 64 : 32));
+  const long long slots = (mma ? 1LL : 2LL) * device_sm_count();  // CTAs that fit per SM
   const int rpc = decode_rows_per_cta(Sq, H, Hk);
-  const long long units = (long long)B * Hk * ((Sq * (H / Hk) + rpc - 1) / rpc);  // CTAs per split
+  const int rows_i = decode_mma_rows(Sq, H, Hk);
+  const long long units = mma ? (long long)B * Hk * ((Sq + rows_i - 1) / rows_i)  // CTAs per split
+                              : (long long)B * Hk * ((Sq * (H / Hk) + rpc - 1) / rpc);
   int max_n = (Sk + 4 * tk - 1) / (4 * tk);  // at least four tiles per split
   if (max_n < 1) max_n = 1;
   if (max_n > 256) max_n = 256;
@@ -508,6 +860,11 @@ static int launch_decode_t(const AttnShape& s, const void* q, const void* k, con
                            void* ws, int n, const CacheArgs* cg, cudaStream_t stream) {
   using C = DecCfg<D>;
   const bool paged = cg && cg->block_table;
+  // Tensor-core path: pairs of a key/value head as MMA rows. Rotary rotates q in
+  // registers, which the TMA-loaded tile does not pass through: that case stays
+  // on the CUDA-core kernel, as do pages smaller than its 128-key tiles.
+  const bool mma = decode_mma_ok(s.Sq, s.H, s.Hk) && !(cg && cg->rot.cos) &&
+                   !(paged && cg->page_size % DecMmaCfg<D>::TK != 0);
   if (paged && cg->page_size % C::TK != 0) return FA_ERR_UNSUPPORTED;
   // Dense caches are (B, rows, Hk, D); pages are (num_pages, page_size, Hk, D).
   const int mb = paged ? cg->num_pages : s.B, mrows = paged ? cg->page_size : (cg ? cg->cap : s.Sk);
@@ -516,7 +873,7 @@ static int launch_decode_t(const AttnShape& s, const void* q, const void* k, con
     return FA_ERR_CUDA;
   const int rpc = decode_rows_per_cta(s.Sq, s.H, s.Hk);
   auto kern = rpc == 4 ? fa_decode_split_kernel<D, 4> : (rpc == 2 ? fa_decode_split_kernel<D, 2> : fa_decode_split_kernel<D, 1>);
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+  if (!mma && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
     return FA_ERR_CUDA;
   DecParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);
@@ -531,6 +888,7 @@ static int launch_decode_t(const AttnShape& s, const void* q, const void* k, con
   p.H = s.H;
   p.group = s.H / s.Hk;
   p.n_rb = (s.Sq * p.group + rpc - 1) / rpc;
+  p.rows_i = 0;  // tensor-core kernel only
   p.block_table = cg ? cg->block_table : nullptr;
   p.seqlens_k = cg ? cg->seqlens : nullptr;
   p.page_size = cg ? cg->page_size : 0;
@@ -544,9 +902,23 @@ static int launch_decode_t(const AttnShape& s, const void* q, const void* k, con
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.status = device_status_word();
   if (!p.status) return FA_ERR_CUDA;
-  if (s.B > 65535 || (long long)s.Hk * p.n_rb > 65535) return FA_ERR_UNSUPPORTED;
-  dim3 grid(n, s.Hk * p.n_rb, s.B);
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mk, mv, p);
+  if (mma) {
+    using M = DecMmaCfg<D>;
+    p.rows_i = decode_mma_rows(s.Sq, s.H, s.Hk);
+    p.n_rb = (s.Sq + p.rows_i - 1) / p.rows_i;
+    CUtensorMap mq, mk2, mv2;
+    if (!make_bshd_map_box(&mq, q, s.B, s.Sq, s.H, D, p.group, p.rows_i) ||
+        !make_bshd_map(&mk2, k, mb, mrows, s.Hk, D, M::TK) || !make_bshd_map(&mv2, v, mb, mrows, s.Hk, D, M::TK))
+      return FA_ERR_CUDA;
+    auto mk_kern = fa_decode_mma_kernel<D>;
+    if (cudaFuncSetAttribute(mk_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, M::SMEM_BYTES) != cudaSuccess)
+      return FA_ERR_CUDA;
+    if (s.B > 65535 || (long long)s.Hk * p.n_rb > 65535) return FA_ERR_UNSUPPORTED;
+    mk_kern<<<dim3(n, s.Hk * p.n_rb, s.B), M::THREADS, M::SMEM_BYTES, stream>>>(mq, mk2, mv2, p);
+  } else {
+    if (s.B > 65535 || (long long)s.Hk * p.n_rb > 65535) return FA_ERR_UNSUPPORTED;
+    kern<<<dim3(n, s.Hk * p.n_rb, s.B), C::THREADS, C::SMEM_BYTES, stream>>>(mk, mv, p);
+  }
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   const int warps = s.B * s.Sq * s.H;
   fa_decode_combine_kernel<D><<<(warps + 7) / 8, 256, 0, stream>>>(

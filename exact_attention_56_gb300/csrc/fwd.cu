@@ -355,7 +355,10 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
             mma_commit_w(&bars->kv_empty[slot_of(2 * (jj + 1))]);
           }
           if (!(ok = wait_full(2 * jj + 1, SITE_MMA_V))) break;
-          if (!(ok = fa_wait_warp(&bars->p_full[0], uint32_t(jj) & 1u, watch, SITE_MMA_P))) break;
+          // P barriers per S buffer: S(jj+1) is queued before this wait, so the
+          // softmax may finish tile jj+1 before it; buffer jj & 1 is next used by
+          // S(jj+2), issued after PV(jj)
+          if (!(ok = fa_wait_warp(&bars->p_full[jj & 1], uint32_t(jj >> 1) & 1u, watch, SITE_MMA_P))) break;
           tc_fence_after();
           issue_pv(jj, 0, jj & 1);
           mma_commit_w(&bars->pv_done[0]);
@@ -488,7 +491,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive_warp(&bars->p_full[C::NSB == 3 ? sb : t]);
+      mbar_arrive_warp(&bars->p_full[(C::NSB == 3 || NT == 1) ? sb : t]);
     }
 
     // ------------------------------------------------------------ epilogue

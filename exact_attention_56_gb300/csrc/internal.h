@@ -52,6 +52,10 @@ int device_sm_count();
 // fp16 with `f16` set): box of 64 head-dim elements (128 B, 128-byte swizzle)
 // x 1 head x `box_rows` rows x 1 batch. Returns false if the driver rejects it.
 bool make_bshd_map(CUtensorMap* map, const void* base, int B, int S, int H, int D, int box_rows, bool f16 = false);
+// As make_bshd_map with a box of box_heads consecutive heads x box_rows rows
+// (smem rows ordered row-major over (row, head)).
+bool make_bshd_map_box(CUtensorMap* map, const void* base, int B, int S, int H, int D, int box_heads, int box_rows,
+                       bool f16 = false);
 
 // Kernel launchers (return an fa_status value).
 int fwd_launch(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,
