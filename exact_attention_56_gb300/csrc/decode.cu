@@ -351,14 +351,19 @@ struct DecMmaCfg {
   static constexpr int PANEL_BYTES = 128 * 128;
   static constexpr int TILE_BYTES = PANELS * PANEL_BYTES;  // 128 rows (or keys) x D
   static constexpr int TK = 128;                           // keys per tile
+  // Softmax warpgroups: two where TMEM holds two O accumulators (D <= 128);
+  // group w takes the CTA's key tiles w, w + NW, ... with its own S buffer and O,
+  // and the two running states are merged exactly at the end.
+  static constexpr int NW = D <= 128 ? 2 : 1;
   static constexpr int NSLOT = D == 64 ? 8 : (D == 128 ? 6 : 2);  // ring of K_j, V_j tiles
-  static constexpr int THREADS = 256;                      // producer, MMA, 2 idle, 4 softmax warps
+  static constexpr int THREADS = 128 + 128 * NW;           // producer, MMA, 2 idle, softmax warps
   static constexpr int Q_OFF = 0;
   static constexpr int KV_OFF = TILE_BYTES;
   static constexpr int BAR_OFF = KV_OFF + NSLOT * TILE_BYTES;
-  static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;  // + alignment slack
+  static constexpr int XCH_OFF = BAR_OFF + 256;            // group 1's (m, l) per row for the merge
+  static constexpr int SMEM_BYTES = XCH_OFF + 1024 + 1024;  // + alignment slack
   static constexpr uint32_t O_COL0 = 256;                  // TMEM: S buffers at 0 and 128, O after
-  static_assert(O_COL0 + D <= 512, "TMEM budget");
+  static_assert(O_COL0 + NW * D <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
@@ -366,7 +371,8 @@ struct DecMmaBars {
   uint64_t q_full;
   uint64_t kv_full[8], kv_empty[8];
   uint64_t s_full[2], p_full[2];  // per S buffer (P is written over its S)
-  uint64_t pv_done, o_done, drain;
+  uint64_t pv_done[2], o_done[2];  // per softmax group
+  uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -397,10 +403,13 @@ __global__ void __launch_bounds__(DecMmaCfg<D>::THREADS, 1)
     fa_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const DecParams p) {
   using C = DecMmaCfg<D>;
+  constexpr int NW = C::NW;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   DecMmaBars* bars = reinterpret_cast<DecMmaBars*>(smem + C::BAR_OFF);
+  float* xch_m = reinterpret_cast<float*>(smem + C::XCH_OFF);  // [128]
+  float* xch_l = xch_m + 128;                                  // [128]
   const int warp = int(warp_id());
   const int lane = int(lane_id());
 
@@ -421,6 +430,8 @@ __global__ void __launch_bounds__(DecMmaCfg<D>::THREADS, 1)
   const int ke = min(s_hi, live_range(i1, p.Sq, Sk, p.wl, p.wr).hi + 1);
   const int t0 = (ks / C::TK) * C::TK;
   const int n_blocks = ke > ks ? (ke - t0 + C::TK - 1) / C::TK : 0;
+  // key tiles of softmax group w: w, w + NW, ...
+  auto tiles_of = [&](int w) { return n_blocks > w ? (n_blocks - w + NW - 1) / NW : 0; };
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -431,9 +442,9 @@ __global__ void __launch_bounds__(DecMmaCfg<D>::THREADS, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
       mbar_init(&bars->p_full[s], 4);  // one arrive per softmax warp
+      mbar_init(&bars->pv_done[s], 1);
+      mbar_init(&bars->o_done[s], 1);
     }
-    mbar_init(&bars->pv_done, 1);
-    mbar_init(&bars->o_done, 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_barrier_init();
@@ -491,8 +502,6 @@ __global__ void __launch_bounds__(DecMmaCfg<D>::THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // S(jj+1) into the other S buffer as soon as K(jj+1) is in; PV(jj) once P(jj)
-    // is stored. S(jj+1) overwrites P(jj-1), which PV(jj-1) has read (in order).
     // The whole warp runs the loop; one elected lane issues each MMA and commit.
     if (n_blocks > 0) {
       constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
@@ -504,41 +513,59 @@ __global__ void __launch_bounds__(DecMmaCfg<D>::THREADS, 1)
       auto wait_full = [&](int it, uint32_t site) {
         return fa_wait_warp(&bars->kv_full[slot_of(it)], uint32_t(it / C::NSLOT) & 1u, watch, site);
       };
-      auto issue_s = [&](int jj) {
+      auto issue_s = [&](int jj, int sb) {  // S of key tile jj into S buffer sb
+        if (!wait_full(2 * jj, SITE_DM_K)) return false;
+        tc_fence_after();
         const uint64_t kd = sdesc_adv(kv_kdesc, uint32_t(slot_of(2 * jj)) * C::TILE_BYTES);
-        const uint32_t ts = tmem + uint32_t(jj & 1) * 128;
+        const uint32_t ts = tmem + uint32_t(sb) * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
           mma_ss_w(ts, sdesc_adv(q_desc, off), sdesc_adv(kd, off), IDESC_S, kk > 0 ? 1u : 0u);
         }
-        mma_commit_w(&bars->s_full[jj & 1]);
+        mma_commit_w(&bars->s_full[sb]);
         mma_commit_w(&bars->kv_empty[slot_of(2 * jj)]);
+        return true;
       };
-      bool ok = fa_wait_warp(&bars->q_full, 0, watch, SITE_DM_Q) && wait_full(0, SITE_DM_K);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-      }
-      for (int jj = 0; jj < n_blocks && ok; ++jj) {
-        if (jj + 1 < n_blocks) {
-          if (!(ok = wait_full(2 * (jj + 1), SITE_DM_K))) break;
-          tc_fence_after();
-          issue_s(jj + 1);
-        }
-        if (!(ok = wait_full(2 * jj + 1, SITE_DM_V))) break;
-        // per-buffer P barriers: S(jj+1) is queued before this wait, so the softmax
-        // may finish tile jj+1 before it; its next use needs S(jj+2), issued later
-        if (!(ok = fa_wait_warp(&bars->p_full[jj & 1], uint32_t(jj >> 1) & 1u, watch, SITE_DM_P))) break;
+      // PV of key tile jj for softmax group w = jj % NW, P read from S buffer sb
+      auto issue_pv = [&](int jj, int sb, uint32_t p_parity) {
+        const int w = jj % NW, j = jj / NW;  // group and its local tile index
+        if (!wait_full(2 * jj + 1, SITE_DM_V)) return false;
+        if (!fa_wait_warp(&bars->p_full[sb], p_parity, watch, SITE_DM_P)) return false;
         tc_fence_after();
         const uint64_t vd = sdesc_adv(kv_mdesc, uint32_t(slot_of(2 * jj + 1)) * C::TILE_BYTES);
-        const uint32_t to = tmem + C::O_COL0, tp = tmem + uint32_t(jj & 1) * 128;
-        const uint32_t acc0 = jj > 0 ? 1u : 0u;
+        const uint32_t to = tmem + C::O_COL0 + uint32_t(w) * D, tp = tmem + uint32_t(sb) * 128;
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) mma_ts_w(to, tp + kk * 8, sdesc_adv(vd, kk * 2048), IDESC_O, kk > 0 ? 1u : acc0);
-        mma_commit_w(&bars->pv_done);
-        if (jj == n_blocks - 1) mma_commit_w(&bars->o_done);
+        mma_commit_w(&bars->pv_done[w]);
+        if (j == tiles_of(w) - 1) mma_commit_w(&bars->o_done[w]);  // the group's last PV
         mma_commit_w(&bars->kv_empty[slot_of(2 * jj + 1)]);
+        return true;
+      };
+      bool ok = fa_wait_warp(&bars->q_full, 0, watch, SITE_DM_Q);
+      if (NW == 2) {
+        // Per pair of tiles: S_0(a), PV_1(a - 1), S_1(a + 1), PV_0(a) (a = 2j): each
+        // group's S overwrites its own P, read by its PV issued before (in order),
+        // and each group has the other's MMAs' worth of time per tile.
+        for (int a = 0; a < n_blocks && ok; a += 2) {
+          if (!(ok = issue_s(a, 0))) break;
+          if (a > 0 && !(ok = issue_pv(a - 1, 1, uint32_t((a - 1) / 2) & 1u))) break;
+          if (a + 1 < n_blocks && !(ok = issue_s(a + 1, 1))) break;
+          if (!(ok = issue_pv(a, 0, uint32_t(a / 2) & 1u))) break;
+        }
+        // the loop issued PV_1 of every odd tile but the last one when the count is even
+        if (ok && n_blocks % 2 == 0) ok = issue_pv(n_blocks - 1, 1, uint32_t((n_blocks - 1) / 2) & 1u);
+      } else {
+        // One group, two S buffers: S(jj+1) into the other buffer as soon as K(jj+1)
+        // is in; it overwrites P(jj-1), read by PV(jj-1) before (in order). P
+        // barriers are per buffer: S(jj+1) is queued before PV(jj)'s wait, so the
+        // softmax may finish tile jj+1 first; buffer jj & 1 is next used by S(jj+2).
+        ok = ok && issue_s(0, 0);
+        for (int jj = 0; jj < n_blocks && ok; ++jj) {
+          if (jj + 1 < n_blocks && !(ok = issue_s(jj + 1, (jj + 1) & 1))) break;
+          if (!(ok = issue_pv(jj, jj & 1, uint32_t(jj >> 1) & 1u))) break;
+        }
       }
       if (!ok) {  // let issued MMAs finish before TMEM is released
         mma_commit_w(&bars->drain);
@@ -547,6 +574,7 @@ __global__ void __launch_bounds__(DecMmaCfg<D>::THREADS, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax (thread = pair)
+    const int w = (warp - 4) / 4;  // softmax group
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const uint32_t lane_addr = uint32_t(wq * 32) << 16;
@@ -564,23 +592,28 @@ __global__ void __launch_bounds__(DecMmaCfg<D>::THREADS, 1)
     const float slope_log2 = (has_alibi && pair_ok) ? p.alibi[b * p.alibi_bstride + h] * 1.4426950408889634f : 0.0f;
     const int c_i = i + Sk - p.Sq;
     const float sl = p.scale_log2;
+    const uint32_t o_col = C::O_COL0 + uint32_t(w) * D;
 
     float m = -INFINITY;  // reference max (log2 units) the running O and l are relative to
     float l = 0.0f;
     bool ok = true;
-    for (int jj = 0; jj < n_blocks; ++jj) {
-      if (!(ok = fa_wait_warp(&bars->s_full[jj & 1], uint32_t(jj >> 1) & 1u, watch, SITE_DM_S))) break;
+    const int n_mine = tiles_of(w);
+    for (int j = 0; j < n_mine; ++j) {
+      const int jj = j * NW + w;  // key tile
+      const int sb = (NW == 2) ? w : (j & 1);
+      const uint32_t par = (NW == 2) ? (uint32_t(j) & 1u) : (uint32_t(j >> 1) & 1u);
+      if (!(ok = fa_wait_warp(&bars->s_full[sb], par, watch, SITE_DM_S))) break;
       tc_fence_after();
       float x[128];
-      tmem_ld_x128f(tmem + lane_addr + uint32_t(jj & 1) * 128, x);
+      tmem_ld_x128f(tmem + lane_addr + uint32_t(sb) * 128, x);
       const int kbase = t0 + jj * C::TK;
       // x = scale*log2(e)*qk - slope*log2(e)*|c(i) - j| in log2 units; keys outside [klo, khi) masked
 #pragma unroll
       for (int c = 0; c < 128; ++c) {
-        const int j = kbase + c;
+        const int kj = kbase + c;
         float v = x[c] * sl;
-        if (has_alibi) v -= slope_log2 * fabsf(float(c_i - j));
-        x[c] = (j >= klo && j < khi) ? v : -INFINITY;
+        if (has_alibi) v -= slope_log2 * fabsf(float(c_i - kj));
+        x[c] = (kj >= klo && kj < khi) ? v : -INFINITY;
       }
       float mq[4];
 #pragma unroll
@@ -615,17 +648,17 @@ __global__ void __launch_bounds__(DecMmaCfg<D>::THREADS, 1)
           rs += p0 + p1;
           pk[e] = pack_bf16x2(p0, p1);
         }
-        tmem_st_x16(tmem + lane_addr + uint32_t(jj & 1) * 128 + q4 * 16, pk);
+        tmem_st_x16(tmem + lane_addr + uint32_t(sb) * 128 + q4 * 16, pk);
       }
       l += rs;
-      if (__any_sync(0xffffffffu, alpha != 1.0f) && jj > 0) {
-        // O must hold P_{j-1} V_{j-1} before it is rescaled (P_j is already in TMEM).
-        if (!(ok = fa_wait_warp(&bars->pv_done, uint32_t(jj - 1) & 1u, watch, SITE_DM_PV))) break;
+      if (__any_sync(0xffffffffu, alpha != 1.0f) && j > 0) {
+        // O must hold this group's P V of its previous tile before it is rescaled.
+        if (!(ok = fa_wait_warp(&bars->pv_done[w], uint32_t(j - 1) & 1u, watch, SITE_DM_PV))) break;
         tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
-          const uint32_t oa = tmem + lane_addr + C::O_COL0 + cc * 32;
+          const uint32_t oa = tmem + lane_addr + o_col + cc * 32;
           tmem_ld_x32(oa, o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
@@ -634,32 +667,53 @@ __global__ void __launch_bounds__(DecMmaCfg<D>::THREADS, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive_warp(&bars->p_full[jj & 1]);
+      mbar_arrive_warp(&bars->p_full[sb]);
     }
 
     // ------------------------------------------------------------ partials of this split
-    const size_t pidx = ((size_t(b) * p.Sq + (pair_ok ? i : 0)) * p.H + h) * p.n_splits + split;
-    if (n_blocks == 0) {
-      if (pair_ok) {
-        for (int d = 0; d < D; ++d) p.part_o[pidx * D + d] = 0.0f;
-        p.part_l[pidx] = -INFINITY;
+    // Group 1 hands its (m, l) to group 0, which merges the two states exactly
+    // (O rows of both groups sit in the same TMEM lanes) and writes O_s, L_s.
+    if (NW == 2) {
+      if (w == 1) {
+        xch_m[r] = ok ? m : -INFINITY;
+        xch_l[r] = ok ? l : 0.0f;
       }
-    } else if (ok && fa_wait_warp(&bars->o_done, 0, watch, SITE_DM_EPI)) {
-      tc_fence_after();
-      const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
+      named_bar_sync(2, 256);
+    }
+    if (w == 0) {
+      const size_t pidx = ((size_t(b) * p.Sq + (pair_ok ? i : 0)) * p.H + h) * p.n_splits + split;
+      const float m1 = (NW == 2) ? xch_m[r] : -INFINITY;
+      const float l1 = (NW == 2) ? xch_l[r] : 0.0f;
+      bool done = ok && (n_mine == 0 || fa_wait_warp(&bars->o_done[0], 0, watch, SITE_DM_EPI));
+      if (NW == 2 && tiles_of(1) > 0) done = done && fa_wait_warp(&bars->o_done[1], 0, watch, SITE_DM_EPI);
+      if (done) {
+        tc_fence_after();
+        const float M = fmaxf(m, m1);
+        const float w0 = (m == -INFINITY) ? 0.0f : ex2_approx(m - M);
+        const float w1 = (m1 == -INFINITY) ? 0.0f : ex2_approx(m1 - M);
+        const float L = l * w0 + l1 * w1;
+        const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
+        const bool use0 = m != -INFINITY, use1 = m1 != -INFINITY;  // a group with no live key has no O
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t o[32];
-        tmem_ld_x32(tmem + lane_addr + C::O_COL0 + cc * 32, o);
-        if (pair_ok) {
-          float4* dst = reinterpret_cast<float4*>(p.part_o + pidx * D + cc * 32);
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o0[32], o1[32];
+          tmem_ld_x32(tmem + lane_addr + C::O_COL0 + cc * 32, o0);
+          if (NW == 2) tmem_ld_x32(tmem + lane_addr + C::O_COL0 + D + cc * 32, o1);
+          if (pair_ok) {
+            float v[32];
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
-                                 __uint_as_float(o[4 * e + 2]) * inv, __uint_as_float(o[4 * e + 3]) * inv);
+            for (int e = 0; e < 32; ++e) {
+              float acc = use0 ? __uint_as_float(o0[e]) * w0 : 0.0f;
+              if (NW == 2 && use1) acc += __uint_as_float(o1[e]) * w1;
+              v[e] = acc * inv;
+            }
+            float4* dst = reinterpret_cast<float4*>(p.part_o + pidx * D + cc * 32);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+          }
         }
+        if (pair_ok) p.part_l[pidx] = (L > 0.0f) ? (M + lg2_approx(L)) * 0.6931471805599453f : -INFINITY;
       }
-      if (pair_ok) p.part_l[pidx] = (l > 0.0f) ? (m + lg2_approx(l)) * 0.6931471805599453f : -INFINITY;
     }
   }
 
@@ -819,11 +873,12 @@ static int decode_rows_per_cta(int Sq, int H, int Hk) {
 }
 
 // The tensor-core kernel serves a key/value head's pairs as the rows of one
-// MMA tile: worth it from 8 pairs on, possible while one query row's group
-// heads fit the 128 rows.
+// MMA tile: worth it from 4 pairs on (fewer pairs leave the CUDA-core kernel
+// bound by the cache read), possible while one query row's group heads fit the
+// 128 rows.
 static bool decode_mma_ok(int Sq, int H, int Hk) {
   const int g = H / Hk;
-  return g <= 128 && Sq * g >= 8;
+  return g <= 128 && Sq * g >= 4;
 }
 static int decode_mma_rows(int Sq, int H, int Hk) {  // query rows per block
   return std::min(Sq, 128 / (H / Hk));
@@ -837,7 +892,10 @@ int decode_auto_splits(int B, int Sq, int Sk, int H, int Hk, int D) {
   const int rows_i = decode_mma_rows(Sq, H, Hk);
   const long long units = mma ? (long long)B * Hk * ((Sq + rows_i - 1) / rows_i)  // CTAs per split
                               : (long long)B * Hk * ((Sq * (H / Hk) + rpc - 1) / rpc);
-  int max_n = (Sk + 4 * tk - 1) / (4 * tk);  // at least four tiles per split
+  // at least four tiles per split (eight for the tensor-core kernel, whose
+  // per-CTA start, one Q tile and the first K/V tiles, costs more)
+  const int min_tiles = mma ? 8 : 4;
+  int max_n = (Sk + min_tiles * tk - 1) / (min_tiles * tk);
   if (max_n < 1) max_n = 1;
   if (max_n > 256) max_n = 256;
   int best = 1;
