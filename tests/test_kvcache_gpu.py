@@ -98,6 +98,15 @@ def test_append_only_and_rotary_only():
     _run(2, 4, 2, 128, [10, 300], 0, 2, 128, False, seed=705)         # rotary on the query only
 
 
+def test_append_without_rotary_many_query_pairs():
+    # no rotary and eight (query row, query head) pairs per key/value head: the
+    # appended rows are read by the tensor-core decode (dense and paged caches,
+    # one sequence filling its capacity)
+    _run(2, 8, 2, 128, [100, 1021], 4, 2, 0, False, seed=709)
+    _run(2, 8, 2, 64, [100, 700], 2, 2, 0, False, seed=710, paged=True)
+    _run(3, 16, 2, 128, [0, 257, 900], 1, 1, 0, False, seed=711, window=(300, 0))
+
+
 def test_long_head_dim_and_masks():
     _run(2, 4, 2, 256, [77, 600], 2, 2, 256, False, seed=706)
     _run(2, 8, 2, 128, [300, 900], 2, 2, 128, True, seed=707, window=(100, 0))
