@@ -142,17 +142,19 @@ def test_decode_groups(Hk, D, Sq):
         assert_lse_close(lse.cpu().numpy().astype(np.float64), l_ref, f"L (splits {n})")
 
 
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("H,Hk,Sq", [(6, 2, 1), (6, 2, 3), (4, 4, 3), (16, 1, 2), (12, 4, 2)])
-def test_decode_query_pairs_share_a_cta(H, Hk, Sq):
-    # A split CTA serves up to four (query row, query head) pairs of one key/value
-    # head. These shapes leave partial blocks (3 or 9 pairs), mix query rows with
+def test_decode_query_pairs_share_a_cta(H, Hk, Sq, D):
+    # The (query row, query head) pairs of one key/value head share a split CTA:
+    # up to four in the CUDA-core kernel, from four on as the rows of a tensor-core
+    # tile. These shapes leave partial blocks (3 or 9 pairs), mix query rows with
     # different causal limits in one block, and put 32 pairs on one head (MQA).
     import torch
 
     import exact_attention_56_gb300 as fa
 
-    B, Sk, D = 2, 777, 128
-    inp = _inputs(B, Sq, Sk, H, Hk, D, 350 + H + Hk + Sq)
+    B, Sk = 2, 777
+    inp = _inputs(B, Sq, Sk, H, Hk, D, 350 + H + Hk + Sq + D)
     q, k, v = (to_dev(inp[n]) for n in ("q", "k", "v"))
     f64 = [bf16_bits_to_f64(inp[x]) for x in ("q", "k", "v")]
     cases = [dict(causal=True), dict(causal=False, window=(100, 0), alibi=alibi_slopes_geometric(H))]
