@@ -210,6 +210,14 @@ def oracle_sample(budget_s=12.0, points=None):
     return flops / t_used / 1e12, desc, t_used
 
 
+def bench_config(ws):
+    """The workload both arms report on."""
+    return {"workload": "training-shaped sweep: hidden 2048 as D64/H32 and D128/H16, S 512..16k, "
+                        "B=16384/S, causal off+on, fwd+bwd; plus split-KV decode B16 H32 D128 Sk 4k/32k/128k",
+            "global_batch_tokens": TOKENS * ws, "parallelism": f"replicas x{ws}",
+            "l2": "inputs larger than L2 (each sweep pass reads >= 320 MiB; decode caches >= 1 GiB)"}
+
+
 def run_reference(args):
     ws, rank, _ = _dist()
     if rank != 0:
@@ -231,8 +239,9 @@ def run_reference(args):
         "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * secs / max(args.steps, 1), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "training-shaped sweep, hidden 2048, tokens 16384 (oracle sample)",
-                   "impl_note": "fp64 CPU oracle (test infrastructure), one head per step sample"},
+        "config": bench_config(ws),
+        "impl_note": "fp64 CPU oracle (test infrastructure) on the host cores; each step a bounded sample of "
+                     "single (b, h) heads of this workload",
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -398,11 +407,7 @@ def run_ours(args):
             "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
             "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "training-shaped sweep: hidden 2048 as D64/H32 and D128/H16, S 512..16k, "
-                                   "B=16384/S, causal off+on, fwd+bwd; plus split-KV decode B16 H32 D128 "
-                                   "Sk 4k/32k/128k",
-                       "global_batch_tokens": TOKENS * ws, "parallelism": f"replicas x{ws}",
-                       "l2": "inputs larger than L2 (each sweep pass reads >= 320 MiB; decode caches >= 1 GiB)"},
+            "config": bench_config(ws),
             "fwd_tflops": fwd_value,
             "fwd_frac": fwd_value / ws / float(peaks.get("bf16_tflops_sustained", 1700.0)),
             "fwdbwd_frac": value / ws / float(peaks.get("bf16_tflops_sustained", 1700.0)),
