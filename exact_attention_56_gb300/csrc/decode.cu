@@ -345,7 +345,11 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS)
 // P (bf16) written over S, O += P V. Each K/V tile is read once for all the
 // pairs; the split's normalised O_s and L_s go to the same partials the merge
 // kernel reads.
-template <int D>
+// ROT: the query was rotated (rotary) in fp32 by a separate kernel and comes as a
+// bf16 pair q_hi + q_lo (q_lo = the rounding residual), two Q tiles whose
+// products with K accumulate in fp32: S keeps about 16 bits of the rotated q
+// rather than bf16's 8.
+template <int D, bool ROT = false>
 struct DecMmaCfg {
   static constexpr int PANELS = D / 64;
   static constexpr int PANEL_BYTES = 128 * 128;
@@ -355,10 +359,11 @@ struct DecMmaCfg {
   // group w takes the CTA's key tiles w, w + NW, ... with its own S buffer and O,
   // and the two running states are merged exactly at the end.
   static constexpr int NW = D <= 128 ? 2 : 1;
-  static constexpr int NSLOT = D == 64 ? 8 : (D == 128 ? 6 : 2);  // ring of K_j, V_j tiles
+  static constexpr int NQ = ROT ? 2 : 1;                   // Q tiles (q_hi, q_lo)
+  static constexpr int NSLOT = D == 64 ? 8 : (D == 128 ? (ROT ? 5 : 6) : 2);  // ring of K_j, V_j tiles
   static constexpr int THREADS = 128 + 128 * NW;           // producer, MMA, 2 idle, softmax warps
   static constexpr int Q_OFF = 0;
-  static constexpr int KV_OFF = TILE_BYTES;
+  static constexpr int KV_OFF = NQ * TILE_BYTES;
   static constexpr int BAR_OFF = KV_OFF + NSLOT * TILE_BYTES;
   static constexpr int XCH_OFF = BAR_OFF + 256;            // group 1's (m, l) per row for the merge
   static constexpr int SMEM_BYTES = XCH_OFF + 1024 + 1024;  // + alignment slack
@@ -398,11 +403,12 @@ __device__ __forceinline__ void dm_drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <int D>
-__global__ void __launch_bounds__(DecMmaCfg<D>::THREADS, 1)
-    fa_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v, const DecParams p) {
-  using C = DecMmaCfg<D>;
+template <int D, bool ROT>
+__global__ void __launch_bounds__(DecMmaCfg<D, ROT>::THREADS, 1)
+    fa_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_q_lo,
+                         const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                         const DecParams p) {
+  using C = DecMmaCfg<D, ROT>;
   constexpr int NW = C::NW;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -464,13 +470,18 @@ __global__ void __launch_bounds__(DecMmaCfg<D>::THREADS, 1)
     // The whole warp runs the loop; one elected lane issues each copy.
     if (n_blocks > 0) {
       tma_prefetch_desc_w(&tm_q);
+      if (ROT) tma_prefetch_desc_w(&tm_q_lo);
       tma_prefetch_desc_w(&tm_k);
       tma_prefetch_desc_w(&tm_v);
       // one box per 64-column panel: group heads x rows_i query rows (rows past
       // Sq read zeros); the tile's rows past group * rows_i are never read back
-      mbar_arrive_expect_tx_w(&bars->q_full, C::PANELS * 128 * p.group * p.rows_i);
-      for (int pn = 0; pn < C::PANELS; ++pn)
+      mbar_arrive_expect_tx_w(&bars->q_full, C::NQ * C::PANELS * 128 * p.group * p.rows_i);
+      for (int pn = 0; pn < C::PANELS; ++pn) {
         tma_load_4d_w(smem + C::Q_OFF + pn * C::PANEL_BYTES, &tm_q, &bars->q_full, pn * 64, hk * p.group, i0, b);
+        if (ROT)
+          tma_load_4d_w(smem + C::Q_OFF + C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_q_lo, &bars->q_full, pn * 64,
+                        hk * p.group, i0, b);
+      }
       int issued = 0;
       bool ok = true;
       for (int jj = 0; jj < n_blocks && ok; ++jj) {
@@ -522,6 +533,13 @@ __global__ void __launch_bounds__(DecMmaCfg<D>::THREADS, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
           mma_ss_w(ts, sdesc_adv(q_desc, off), sdesc_adv(kd, off), IDESC_S, kk > 0 ? 1u : 0u);
+        }
+        if (ROT) {  // + q_lo K^T, accumulated
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = C::TILE_BYTES + (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
+            mma_ss_w(ts, sdesc_adv(q_desc, off), sdesc_adv(kd, off - C::TILE_BYTES), IDESC_S, 1u);
+          }
         }
         mma_commit_w(&bars->s_full[sb]);
         mma_commit_w(&bars->kv_empty[slot_of(2 * jj)]);
@@ -861,9 +879,48 @@ int kv_append_launch(const AttnShape& s, const void* k_new, const void* v_new, v
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+// Workspace: the split partials O_s (fp32) and L_s, then room for the rotated
+// query as a bf16 pair q_hi, q_lo (the tensor-core kernel's query tile arrives
+// by TMA, so rotary is applied before it, into these copies).
 size_t decode_workspace_bytes(int B, int Sq, int H, int D, int n) {
   const size_t units = size_t(B) * Sq * H * n;
-  return align256(units * D * 4) + align256(units * 4);
+  return align256(units * D * 4) + align256(units * 4) + 2 * align256(size_t(B) * Sq * H * D * 2);
+}
+
+// Rotary of the queries for the tensor-core decode: q rotated in fp32 at each
+// row's diagonal position i + Sk_b - Sq (as the CUDA-core kernel does in
+// registers), stored as q_hi = bf16(q_rot) and q_lo = bf16(q_rot - q_hi); one
+// thread per 16-byte chunk.
+template <int D>
+__global__ void __launch_bounds__(256)
+    fa_decode_rotate_q_kernel(const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ q_hi,
+                              __nv_bfloat16* __restrict__ q_lo, const int* __restrict__ seqlens, int B, int Sq,
+                              int H, int Sk, int s_new, int cap, Rotary rot) {
+  constexpr int CH = D / 8;
+  const long long n = (long long)B * Sq * H * CH;
+  for (long long t = blockIdx.x * 256LL + threadIdx.x; t < n; t += (long long)gridDim.x * 256) {
+    const int c = int(t % CH);
+    const long long row = t / CH;  // (b, i, h)
+    const int i = int((row / H) % Sq);
+    const int b = int(row / ((long long)H * Sq));
+    const int skb = seqlens ? max(0, min(seqlens[b] + s_new, cap)) : Sk;
+    const __nv_bfloat16* src = q + row * D;
+    float x[8], pq[8];
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + c * 8), x);
+    if (c * 8 < rot.dim) {
+      if (!rot.interleaved) bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + rotary_partner(c * 8, rot)), pq);
+      rotary8(x, pq, c * 8, i + skb - Sq, rot);
+    }
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      hi[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
+      const float h0 = __uint_as_float(hi[e] << 16), h1 = __uint_as_float(hi[e] & 0xFFFF0000u);
+      lo[e] = pack_bf16x2(x[2 * e] - h0, x[2 * e + 1] - h1);
+    }
+    *reinterpret_cast<uint4*>(q_hi + row * D + c * 8) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(q_lo + row * D + c * 8) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  }
 }
 
 // Query pairs a split CTA serves: up to four, as many as one key/value head has.
@@ -918,11 +975,12 @@ static int launch_decode_t(const AttnShape& s, const void* q, const void* k, con
                            void* ws, int n, const CacheArgs* cg, cudaStream_t stream) {
   using C = DecCfg<D>;
   const bool paged = cg && cg->block_table;
-  // Tensor-core path: pairs of a key/value head as MMA rows. Rotary rotates q in
-  // registers, which the TMA-loaded tile does not pass through: that case stays
-  // on the CUDA-core kernel, as do pages smaller than its 128-key tiles.
-  const bool mma = decode_mma_ok(s.Sq, s.H, s.Hk) && !(cg && cg->rot.cos) &&
-                   !(paged && cg->page_size % DecMmaCfg<D>::TK != 0);
+  // Tensor-core path: pairs of a key/value head as MMA rows. Pages smaller than
+  // its 128-key tiles stay on the CUDA-core kernel, as does rotary at D = 256
+  // (its two query tiles leave no room for the K/V ring).
+  const bool rot = cg && cg->rot.cos;
+  const bool mma = decode_mma_ok(s.Sq, s.H, s.Hk) && !(paged && cg->page_size % DecMmaCfg<D>::TK != 0) &&
+                   !(rot && D > 128);
   if (paged && cg->page_size % C::TK != 0) return FA_ERR_UNSUPPORTED;
   // Dense caches are (B, rows, Hk, D); pages are (num_pages, page_size, Hk, D).
   const int mb = paged ? cg->num_pages : s.B, mrows = paged ? cg->page_size : (cg ? cg->cap : s.Sk);
@@ -964,15 +1022,42 @@ static int launch_decode_t(const AttnShape& s, const void* q, const void* k, con
     using M = DecMmaCfg<D>;
     p.rows_i = decode_mma_rows(s.Sq, s.H, s.Hk);
     p.n_rb = (s.Sq + p.rows_i - 1) / p.rows_i;
-    CUtensorMap mq, mk2, mv2;
-    if (!make_bshd_map_box(&mq, q, s.B, s.Sq, s.H, D, p.group, p.rows_i) ||
+    // with rotary, the query tiles come from the rotated pair in the workspace
+    const void* qsrc = q;
+    const void* qlo = q;
+    if (rot) {
+      const size_t qbytes = align256(size_t(s.B) * s.Sq * s.H * D * 2);
+      auto* qh = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(ws) + align256(units * D * 4) +
+                                                  align256(units * 4));
+      auto* ql = reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<uint8_t*>(qh) + qbytes);
+      const long long chunks = (long long)s.B * s.Sq * s.H * (D / 8);
+      const int rgrid = int(std::max(1LL, std::min((long long)device_sm_count() * 8, (chunks + 255) / 256)));
+      fa_decode_rotate_q_kernel<D><<<rgrid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(q), qh, ql,
+                                                               p.seqlens_k, s.B, s.Sq, s.H, s.Sk, p.s_new, p.cap,
+                                                               p.rot);
+      if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+      qsrc = qh;
+      qlo = ql;
+    }
+    CUtensorMap mq, mql, mk2, mv2;
+    if (!make_bshd_map_box(&mq, qsrc, s.B, s.Sq, s.H, D, p.group, p.rows_i) ||
+        !make_bshd_map_box(&mql, qlo, s.B, s.Sq, s.H, D, p.group, p.rows_i) ||
         !make_bshd_map(&mk2, k, mb, mrows, s.Hk, D, M::TK) || !make_bshd_map(&mv2, v, mb, mrows, s.Hk, D, M::TK))
       return FA_ERR_CUDA;
-    auto mk_kern = fa_decode_mma_kernel<D>;
-    if (cudaFuncSetAttribute(mk_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, M::SMEM_BYTES) != cudaSuccess)
-      return FA_ERR_CUDA;
     if (s.B > 65535 || (long long)s.Hk * p.n_rb > 65535) return FA_ERR_UNSUPPORTED;
-    mk_kern<<<dim3(n, s.Hk * p.n_rb, s.B), M::THREADS, M::SMEM_BYTES, stream>>>(mq, mk2, mv2, p);
+    const dim3 mgrid(n, s.Hk * p.n_rb, s.B);
+    if (rot) {
+      using MR = DecMmaCfg<D, D <= 128>;
+      auto kr = fa_decode_mma_kernel<D, D <= 128>;
+      if (cudaFuncSetAttribute(kr, cudaFuncAttributeMaxDynamicSharedMemorySize, MR::SMEM_BYTES) != cudaSuccess)
+        return FA_ERR_CUDA;
+      kr<<<mgrid, MR::THREADS, MR::SMEM_BYTES, stream>>>(mq, mql, mk2, mv2, p);
+    } else {
+      auto kq = fa_decode_mma_kernel<D, false>;
+      if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, M::SMEM_BYTES) != cudaSuccess)
+        return FA_ERR_CUDA;
+      kq<<<mgrid, M::THREADS, M::SMEM_BYTES, stream>>>(mq, mql, mk2, mv2, p);
+    }
   } else {
     if (s.B > 65535 || (long long)s.Hk * p.n_rb > 65535) return FA_ERR_UNSUPPORTED;
     kern<<<dim3(n, s.Hk * p.n_rb, s.B), C::THREADS, C::SMEM_BYTES, stream>>>(mk, mv, p);

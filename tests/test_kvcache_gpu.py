@@ -107,6 +107,14 @@ def test_append_without_rotary_many_query_pairs():
     _run(3, 16, 2, 128, [0, 257, 900], 1, 1, 0, False, seed=711, window=(300, 0))
 
 
+def test_rotary_many_query_pairs():
+    # rotary with four or more (query row, query head) pairs per key/value head:
+    # the query is rotated in fp32 and carried as a bf16 pair into the
+    # tensor-core decode (D = 64, interleaved, partial rotary dims)
+    _run(2, 8, 2, 64, [31, 900], 1, 2, 32, True, seed=712)
+    _run(2, 16, 2, 128, [500, 1000], 3, 3, 128, False, seed=713, paged=True)
+
+
 def test_long_head_dim_and_masks():
     _run(2, 4, 2, 256, [77, 600], 2, 2, 256, False, seed=706)
     _run(2, 8, 2, 128, [300, 900], 2, 2, 128, True, seed=707, window=(100, 0))
