@@ -1,4 +1,7 @@
-// Split-KV decode for short queries, plus the merge kernel.
+// Split-KV decode for short queries: two split kernels (CUDA cores for up to
+// three query pairs per key/value head, tensor cores from four on), the query
+// rotation the tensor-core kernel reads, the KV-cache append, and the merge
+// kernel.
 //
 // Page "FlashAttention：快速且内存高效的准确注意力机制", section
 // "2.2：针对推理进行优化": with a very short query the cost is reading the KV
@@ -19,6 +22,8 @@
 //               and the groups are merged once at the end through shared memory.
 //   Output: per split the normalised partial O_s (fp32, D) and L_s (natural
 //   log) in the workspace; a split with no live key writes O_s = 0, L_s = -inf.
+// Tensor-core split kernel (fa_decode_mma_kernel, described where it is
+// defined): the pairs of one key/value head as the rows of a 128-row MMA tile.
 // Merge kernel (one warp per (batch, query row, head)):
 //   L = log sum_s exp(L_s), O = sum_s exp(L_s - L) O_s, vectorised 16-byte loads.
 #include <cuda.h>
