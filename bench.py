@@ -509,6 +509,8 @@ PROFILE_CASES = {
     "decode": dict(op="decode", B=16, S=32768, H=32, D=128, causal=True),
     # decode with a 1.07 GB cache: small enough for multi-pass captures
     "decode4k": dict(op="decode", B=16, S=4096, H=32, D=128, causal=True),
+    # grouped decode (8 key/value heads, 4 query heads each): the tensor-core split kernel
+    "decode_gqa4k": dict(op="decode", B=16, S=4096, H=32, Hk=8, D=128, causal=True),
 }
 
 
@@ -526,11 +528,12 @@ def run_profile(name):
     dev = torch.device("cuda", 0)
     B, S, H, D = c["B"], c["S"], c["H"], c["D"]
     if c["op"] == "decode":
+        Hk = c.get("Hk", H)
         q = device_normal_bf16((B, 1, H, D), 1, dev)
-        k = device_normal_bf16((B, S, H, D), 2, dev)
-        v = device_normal_bf16((B, S, H, D), 3, dev)
-        n = fa.fa_decode_num_splits(B, 1, S, H, D)
-        ws = torch.empty(fa.fa_decode_workspace_size(B, 1, S, H, D, n), dtype=torch.uint8, device=dev)
+        k = device_normal_bf16((B, S, Hk, D), 2, dev)
+        v = device_normal_bf16((B, S, Hk, D), 3, dev)
+        n = fa.fa_decode_num_splits(B, 1, S, H, D, Hk=Hk)
+        ws = torch.empty(fa.fa_decode_workspace_size(B, 1, S, H, D, n, Hk=Hk), dtype=torch.uint8, device=dev)
         run = lambda: fa.fa_decode_splitkv(q, k, v, causal=True, num_splits=n, workspace=ws)  # noqa: E731
     else:
         q, k, v, do = (device_normal_bf16((B, S, H, D), i, dev) for i in range(4))
