@@ -143,12 +143,15 @@ def test_decode_groups(Hk, D, Sq):
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
-@pytest.mark.parametrize("H,Hk,Sq", [(6, 2, 1), (6, 2, 3), (4, 4, 3), (16, 1, 2), (12, 4, 2)])
+@pytest.mark.parametrize("H,Hk,Sq", [(6, 2, 1), (6, 2, 3), (4, 4, 3), (16, 1, 2), (12, 4, 2), (8, 2, 16),
+                                     (64, 1, 3), (128, 1, 2)])
 def test_decode_query_pairs_share_a_cta(H, Hk, Sq, D):
     # The (query row, query head) pairs of one key/value head share a split CTA:
     # up to four in the CUDA-core kernel, from four on as the rows of a tensor-core
     # tile. These shapes leave partial blocks (3 or 9 pairs), mix query rows with
     # different causal limits in one block, and put 32 pairs on one head (MQA).
+    # G * Sq above 128 (64 x 3, 128 x 2) splits a head's pairs over several
+    # tensor-core row blocks; Sq = 16 is the largest query length decode takes.
     import torch
 
     import exact_attention_56_gb300 as fa
