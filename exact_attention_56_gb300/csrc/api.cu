@@ -98,6 +98,8 @@ static int check_common(int B, int Sq, int Sk, int H, int Hk, int D, float scale
   }
   // Index ranges: rows and tiles are addressed with 32-bit ints, elements with 64-bit offsets.
   if (Sq > (1 << 30) || Sk > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  // Heads and batches index gridDim.y and gridDim.z, which allow at most 65535.
+  if (B > 65535 || H > 65535) return FA_ERR_UNSUPPORTED;
   s->B = B;
   s->Sq = Sq;
   s->Sk = Sk;
@@ -380,6 +382,8 @@ int fa_decode_kvcache(const void* q, void* k_cache, void* v_cache, const int* ca
   const fa::CacheArgs cg{block_table, cache_seqlens, num_pages, page_size, max_pages_per_seq, S_new, cap,
                          fa::Rotary{rotary_cos, rotary_sin, rotary_dim, rotary_len, rotary_interleaved ? 1 : 0}};
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // nothing is appended to the cache by a call that cannot run its attention
+  if ((st = fa::decode_check(s, &cg)) != FA_OK) return st;
   st = fa::kv_append_launch(s, k_new, v_new, k_cache, v_cache, cg, cs);
   if (st != FA_OK) return st;
   return fa::decode_launch(s, q, k_cache, v_cache, out, lse, workspace, n, &cg, cs);

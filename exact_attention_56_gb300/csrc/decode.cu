@@ -945,6 +945,30 @@ static bool decode_mma_ok(int Sq, int H, int Hk) {
 static int decode_mma_rows(int Sq, int H, int Hk) {  // query rows per block
   return std::min(Sq, 128 / (H / Hk));
 }
+// The split kernel the launcher runs: the tensor-core one unless the pages
+// are smaller than its 128-key tiles or rotary is asked for at D = 256 (its
+// two query tiles leave no room for the K/V ring).
+static bool decode_uses_mma(const AttnShape& s, const CacheArgs* cg) {
+  const bool paged = cg && cg->block_table;
+  const bool rot = cg && cg->rot.cos;
+  return decode_mma_ok(s.Sq, s.H, s.Hk) && !(paged && cg->page_size % DecMmaCfg<64>::TK != 0) &&
+         !(rot && s.D > 128);
+}
+
+int decode_check(const AttnShape& s, const CacheArgs* cg) {
+  long long blocks;  // gridDim.y = Hk x blocks of query pairs
+  if (decode_uses_mma(s, cg)) {
+    const int rows_i = decode_mma_rows(s.Sq, s.H, s.Hk);
+    blocks = (s.Sq + rows_i - 1) / rows_i;
+  } else {
+    const int rpc = decode_rows_per_cta(s.Sq, s.H, s.Hk);
+    blocks = ((long long)s.Sq * (s.H / s.Hk) + rpc - 1) / rpc;
+  }
+  if (s.B > 65535 || (long long)s.Hk * blocks > 65535) return FA_ERR_UNSUPPORTED;
+  // the combine kernel numbers the (batch, query row, head) triples with 32-bit ints
+  if ((long long)s.B * s.Sq * s.H > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
 
 int decode_auto_splits(int B, int Sq, int Sk, int H, int Hk, int D) {
   const bool mma = decode_mma_ok(Sq, H, Hk);
@@ -980,12 +1004,14 @@ static int launch_decode_t(const AttnShape& s, const void* q, const void* k, con
                            void* ws, int n, const CacheArgs* cg, cudaStream_t stream) {
   using C = DecCfg<D>;
   const bool paged = cg && cg->block_table;
-  // Tensor-core path: pairs of a key/value head as MMA rows. Pages smaller than
-  // its 128-key tiles stay on the CUDA-core kernel, as does rotary at D = 256
-  // (its two query tiles leave no room for the K/V ring).
+  // Tensor-core path: pairs of a key/value head as MMA rows (decode_uses_mma).
+  static_assert(DecMmaCfg<D>::TK == DecMmaCfg<64>::TK, "one key tile for every D");
   const bool rot = cg && cg->rot.cos;
-  const bool mma = decode_mma_ok(s.Sq, s.H, s.Hk) && !(paged && cg->page_size % DecMmaCfg<D>::TK != 0) &&
-                   !(rot && D > 128);
+  const bool mma = decode_uses_mma(s, cg);
+  {
+    const int st = decode_check(s, cg);
+    if (st != FA_OK) return st;
+  }
   if (paged && cg->page_size % C::TK != 0) return FA_ERR_UNSUPPORTED;
   // Dense caches are (B, rows, Hk, D); pages are (num_pages, page_size, Hk, D).
   const int mb = paged ? cg->num_pages : s.B, mrows = paged ? cg->page_size : (cg ? cg->cap : s.Sk);
@@ -1049,7 +1075,6 @@ static int launch_decode_t(const AttnShape& s, const void* q, const void* k, con
         !make_bshd_map_box(&mql, qlo, s.B, s.Sq, s.H, D, p.group, p.rows_i) ||
         !make_bshd_map(&mk2, k, mb, mrows, s.Hk, D, M::TK) || !make_bshd_map(&mv2, v, mb, mrows, s.Hk, D, M::TK))
       return FA_ERR_CUDA;
-    if (s.B > 65535 || (long long)s.Hk * p.n_rb > 65535) return FA_ERR_UNSUPPORTED;
     const dim3 mgrid(n, s.Hk * p.n_rb, s.B);
     if (rot) {
       using MR = DecMmaCfg<D, D <= 128>;
@@ -1064,12 +1089,11 @@ static int launch_decode_t(const AttnShape& s, const void* q, const void* k, con
       kq<<<mgrid, M::THREADS, M::SMEM_BYTES, stream>>>(mq, mql, mk2, mv2, p);
     }
   } else {
-    if (s.B > 65535 || (long long)s.Hk * p.n_rb > 65535) return FA_ERR_UNSUPPORTED;
     kern<<<dim3(n, s.Hk * p.n_rb, s.B), C::THREADS, C::SMEM_BYTES, stream>>>(mk, mv, p);
   }
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  const int warps = s.B * s.Sq * s.H;
-  fa_decode_combine_kernel<D><<<(warps + 7) / 8, 256, 0, stream>>>(
+  const long long warps = (long long)s.B * s.Sq * s.H;
+  fa_decode_combine_kernel<D><<<unsigned((warps + 7) / 8), 256, 0, stream>>>(
       p.part_o, p.part_l, static_cast<__nv_bfloat16*>(out), lse, s.B, s.Sq, s.H, n);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

@@ -72,6 +72,7 @@ extern "C" int fa_decode_splitkv_noalloc(const void* q, const void* k_cache, con
     if (alibi_batch_stride != 0 && alibi_batch_stride != H) return FA_ERR_INVALID;
   }
   if (Sq > 16 || Sk > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  if (B > 65535 || H > 65535) return FA_ERR_UNSUPPORTED;  // gridDim.y and gridDim.z limits
   if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
   if (num_splits < 0 || num_splits > 256) return FA_ERR_INVALID;
   const int n = num_splits == 0 ? fa::decode_auto_splits(B, Sq, Sk, H, Hk, D) : num_splits;

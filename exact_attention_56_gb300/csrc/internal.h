@@ -67,6 +67,9 @@ int decode_launch(const AttnShape& s, const void* q, const void* k, const void* 
 int kv_append_launch(const AttnShape& s, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                      const CacheArgs& cache, cudaStream_t stream);
 size_t decode_workspace_bytes(int B, int Sq, int H, int D, int num_splits);
+// FA_ERR_UNSUPPORTED when the split kernel's grid would exceed the hardware's
+// limits; checked before the first launch of a decode call.
+int decode_check(const AttnShape& s, const CacheArgs* cache);
 int decode_auto_splits(int B, int Sq, int Sk, int H, int Hk, int D);
 int bwd_launch(const AttnShape& s, const void* dout, const void* q, const void* k, const void* v,
                const void* out, const float* lse, void* dq, void* dk, void* dv, void* workspace,

@@ -82,3 +82,20 @@ def test_workspace_sizes(lib):
     assert lib.fa_decode_workspace_size(2, 1, 1000, 4, 4, 128, 3) >= 2 * 4 * 3 * (128 + 1) * 4
     assert lib.fa_decode_workspace_size(2, 1, 1000, 4, 1, 128, 3) >= 2 * 4 * 3 * (128 + 1) * 4
     assert lib.fa_decode_workspace_size(2, 17, 1000, 4, 4, 128, 3) == 0
+
+
+def test_grid_limits_without_gpu(lib):
+    """Shapes whose grids exceed gridDim.y/z (65535) are refused before any launch."""
+    import exact_attention_56_gb300 as fa
+
+    assert _fwd(lib, B=65536) == fa.FA_ERR_UNSUPPORTED
+    assert _fwd(lib, H=65536) == fa.FA_ERR_UNSUPPORTED
+    # Decode with an append: Sq = 3 rows of one query head per key/value head
+    # run on the CUDA-core kernel in blocks of 2 pairs, so 40000 key/value heads
+    # need 80000 grid rows. The call must refuse before it appends to the cache.
+    P = ctypes.c_void_p
+    H = Hk = 40000
+    st = lib.fa_decode_kvcache(P(16), P(16), P(16), P(16), P(16), P(16), 1, None, None, 0, 0, 0, None, 0, 0, 0,
+                               P(16), P(16), P(256), ctypes.c_size_t(1 << 62), 1, 3, 1024, H, Hk, 64,
+                               ctypes.c_float(0.0), 1, -1, -1, None, 0, 1, P(None))
+    assert st == fa.FA_ERR_UNSUPPORTED
