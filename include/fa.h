@@ -23,6 +23,11 @@
  *   "代码解读博客：FlashCrossAttention") without saying which query heads share
  *   a key/value head; consecutive groups of H / Hk is the reading taken.
  * - D (head dim) is 64, 128 or 256 (backward: 64 or 128).
+ * - Size limits, FA_ERR_UNSUPPORTED beyond them: B and H at most 65535 (they
+ *   index grid dimensions); Sq, Sk and the packed totals at most 2^30. Decode
+ *   also refuses a call whose split grid (Hk x blocks of query pairs) exceeds
+ *   65535 rows, or B * Sq * H above 2^31 - 1. It checks this before any
+ *   launch, so a refused fa_decode_kvcache leaves the cache unchanged.
  * - scale <= 0 (or NaN) selects the default 1/sqrt(D) (section "参数说明").
  * - causal != 0 masks key j for query row i unless j <= i + Sk - Sq: the mask
  *   is aligned to the bottom-right corner of the score matrix (section
