@@ -558,24 +558,50 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
       mbar_arrive_warp(&bars->s_free);
       const bool need_mask = !(tile_keys_ok && i0 >= qlo_max && i0 + 127 <= qhi_min);
       const uint64_t sl2 = f2_pack(sl, sl);
+      const int dd0 = ib + off - j;  // c(i) - j for the group's first query
+      if (has_alibi && (dd0 >= 0 || dd0 + C::COLS - 1 <= 0)) {
+        // ALiBi with this key's queries all on one side of the diagonal:
+        // slope * |c(i) - j| = (+-slope) * (c(i) - j) runs on column pairs,
+        // rounding as the scalar form below does (the distances are exact).
+        const float ms = dd0 >= 0 ? slope_log2 : -slope_log2;
+        const uint64_t ms2 = f2_pack(ms, ms), st2 = f2_pack(4.0f, 4.0f);
+        uint64_t distA = f2_pack(float(dd0), float(dd0) + 1.0f);
+        uint64_t distB = f2_pack(float(dd0) + 2.0f, float(dd0) + 3.0f);
 #pragma unroll
-      for (int c4 = 0; c4 < C::COLS / 4; ++c4) {
-        const float4 l4 = l2v[c4];
-        float b0 = -l4.x, b1 = -l4.y, b2 = -l4.z, b3 = -l4.w;
-        if (has_alibi) {
-          const float dd = float(ib + off - j + 4 * c4);
-          b0 -= slope_log2 * fabsf(dd);
-          b1 -= slope_log2 * fabsf(dd + 1.0f);
-          b2 -= slope_log2 * fabsf(dd + 2.0f);
-          b3 -= slope_log2 * fabsf(dd + 3.0f);
+        for (int c4 = 0; c4 < C::COLS / 4; ++c4) {
+          const float4 l4 = l2v[c4];
+          const uint64_t bA = f2_sub(f2_pack(-l4.x, -l4.y), f2_mul(distA, ms2));
+          const uint64_t bB = f2_sub(f2_pack(-l4.z, -l4.w), f2_mul(distB, ms2));
+          distA = f2_add(distA, st2);
+          distB = f2_add(distB, st2);
+          float a0, a1, a2, a3;
+          f2_unpack(f2_fma(f2_pack(pv[4 * c4], pv[4 * c4 + 1]), sl2, bA), a0, a1);
+          f2_unpack(f2_fma(f2_pack(pv[4 * c4 + 2], pv[4 * c4 + 3]), sl2, bB), a2, a3);
+          pv[4 * c4] = ex2_approx(a0);
+          pv[4 * c4 + 1] = ex2_approx(a1);
+          pv[4 * c4 + 2] = ex2_approx(a2);
+          pv[4 * c4 + 3] = ex2_approx(a3);
         }
-        float a0, a1, a2, a3;
-        f2_unpack(f2_fma(f2_pack(pv[4 * c4], pv[4 * c4 + 1]), sl2, f2_pack(b0, b1)), a0, a1);
-        f2_unpack(f2_fma(f2_pack(pv[4 * c4 + 2], pv[4 * c4 + 3]), sl2, f2_pack(b2, b3)), a2, a3);
-        pv[4 * c4] = ex2_approx(a0);
-        pv[4 * c4 + 1] = ex2_approx(a1);
-        pv[4 * c4 + 2] = ex2_approx(a2);
-        pv[4 * c4 + 3] = ex2_approx(a3);
+      } else {
+#pragma unroll
+        for (int c4 = 0; c4 < C::COLS / 4; ++c4) {
+          const float4 l4 = l2v[c4];
+          float b0 = -l4.x, b1 = -l4.y, b2 = -l4.z, b3 = -l4.w;
+          if (has_alibi) {
+            const float dd = float(dd0 + 4 * c4);
+            b0 -= slope_log2 * fabsf(dd);
+            b1 -= slope_log2 * fabsf(dd + 1.0f);
+            b2 -= slope_log2 * fabsf(dd + 2.0f);
+            b3 -= slope_log2 * fabsf(dd + 3.0f);
+          }
+          float a0, a1, a2, a3;
+          f2_unpack(f2_fma(f2_pack(pv[4 * c4], pv[4 * c4 + 1]), sl2, f2_pack(b0, b1)), a0, a1);
+          f2_unpack(f2_fma(f2_pack(pv[4 * c4 + 2], pv[4 * c4 + 3]), sl2, f2_pack(b2, b3)), a2, a3);
+          pv[4 * c4] = ex2_approx(a0);
+          pv[4 * c4 + 1] = ex2_approx(a1);
+          pv[4 * c4 + 2] = ex2_approx(a2);
+          pv[4 * c4 + 3] = ex2_approx(a3);
+        }
       }
       if (need_mask) {
         const int lo = qlo - ib, hi = qhi - ib;
@@ -898,7 +924,27 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       mbar_arrive_warp(&bars->s_free);
       const int kbase = (jb + jj) * 128;
       const bool need_mask = !(kbase >= tile_lo_max && kbase + 127 <= tile_hi_min);
-      if (has_alibi) {
+      if (has_alibi && (kb + C::COLS - 1 <= c_i || kb >= c_i)) {
+        // keys on one side of the diagonal: the bias on column pairs, with the
+        // signed slope (same rounding as the scalar form below)
+        const float d0 = float(c_i - kb);
+        const float ns = (kb >= c_i) ? slope_log2 : -slope_log2;
+        const uint64_t ns2 = f2_pack(ns, ns), sl2 = f2_pack(sl, sl), nl2 = f2_pack(-l2, -l2);
+        const uint64_t st2 = f2_pack(4.0f, 4.0f);
+        uint64_t dist[2] = {f2_pack(d0, d0 - 1.0f), f2_pack(d0 - 2.0f, d0 - 3.0f)};
+#pragma unroll
+        for (int c = 0; c < C::COLS; c += 4) {
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int cc = c + 2 * k;
+            float a0, a1;
+            f2_unpack(f2_fma(f2_pack(pv[cc], pv[cc + 1]), sl2, f2_add(f2_mul(dist[k], ns2), nl2)), a0, a1);
+            pv[cc] = ex2_approx(a0);
+            pv[cc + 1] = ex2_approx(a1);
+            dist[k] = f2_sub(dist[k], st2);
+          }
+        }
+      } else if (has_alibi) {
         const float d0 = float(c_i - kb);
 #pragma unroll
         for (int c = 0; c < C::COLS; ++c)

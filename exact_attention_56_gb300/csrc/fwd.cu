@@ -152,6 +152,14 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
   const int kv_hi = last_rr.hi;
   const int jb = kv_lo / 128;
   const int n_blocks = (kv_hi >= kv_lo) ? (kv_hi / 128 + 1 - jb) : 0;
+  // Order of the key tiles. ALiBi's bias peaks at each row's diagonal key, so
+  // the tile holding the last row's diagonal goes first, then the tiles to its
+  // left (falling bias), then those to its right: the running max is set early
+  // and O is rarely rescaled. Without ALiBi (jd = 0) the order is ascending.
+  const int jd = (p.alibi != nullptr && n_blocks > 0)
+                     ? min(max((last_row + Sk - Sq) / 128 - jb, 0), n_blocks - 1)
+                     : 0;
+  auto key_tile = [jb, jd](int jj) { return jb + (jj <= jd ? jd - jj : jj); };
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -208,7 +216,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
           const CUtensorMap* m = kv ? &tm_v : &tm_k;
           for (int pn = 0; pn < C::PANELS; ++pn)
             tma_load_4d_w(smem + C::KV_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, m, &bars->kv_full[s],
-                        pn * 64, hkv, k_off + (jb + jj) * 128, tb);
+                        pn * 64, hkv, k_off + key_tile(jj) * 128, tb);
           issued = it + 1;
         }
       }
@@ -403,13 +411,34 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
       float x[128];
       tmem_ld_x128f(tmem + lane_addr + sb * 128, x);
 
-      const int kbase = (jb + jj) * 128;
+      const int kbase = key_tile(jj) * 128;
       const bool need_mask = !(kbase >= tile_lo_max && kbase + 127 <= tile_hi_min);
       if (has_alibi) {
         // x = scale*log2(e)*qk - slope*log2(e)*|c(i) - j|, in log2 units
         const float d0 = float(c_i - kbase);
+        if (kbase + 127 <= c_i || kbase >= c_i) {
+          // All keys on one side of the diagonal: |c(i) - j| = +-(d0 - c), so the
+          // bias runs on column pairs. The distances are exact integers and the
+          // signed slope times d rounds as -slope * |d| does, so the values are
+          // those of the scalar form below.
+          const float ns = (kbase >= c_i) ? slope_log2 : -slope_log2;
+          const uint64_t ns2 = f2_pack(ns, ns), sl2 = f2_pack(sl, sl), st2 = f2_pack(8.0f, 8.0f);
+          uint64_t dist[4];  // four independent chains of column pairs, 8 columns apart
 #pragma unroll
-        for (int c = 0; c < 128; ++c) x[c] = fmaf(x[c], sl, -slope_log2 * fabsf(d0 - float(c)));
+          for (int k = 0; k < 4; ++k) dist[k] = f2_pack(d0 - float(2 * k), d0 - float(2 * k + 1));
+#pragma unroll
+          for (int c = 0; c < 128; c += 8) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int cc = c + 2 * k;
+              f2_unpack(f2_fma(f2_pack(x[cc], x[cc + 1]), sl2, f2_mul(dist[k], ns2)), x[cc], x[cc + 1]);
+              dist[k] = f2_sub(dist[k], st2);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) x[c] = fmaf(x[c], sl, -slope_log2 * fabsf(d0 - float(c)));
+        }
       }
       if (need_mask) {
         const int lo = rr.lo - kbase, hi = rr.hi - kbase;

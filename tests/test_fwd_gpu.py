@@ -114,3 +114,14 @@ def test_one_key_window_returns_that_value_exactly(Sq, Sk, D):
     q64, k64 = bf16_bits_to_f64(inp["q"])[0], bf16_bits_to_f64(inp["k"])[0]
     l_ref = np.einsum("ihd,ihd->hi", q64[live], k64[c[live]]) / math.sqrt(D)
     assert np.max(np.abs(lse.cpu().numpy()[0][:, live] - l_ref)) <= 1e-3
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("causal,window", [(False, (-1, -1)), (True, (-1, -1)), (False, (200, 100))])
+@pytest.mark.parametrize("Sq,Sk", [(300, 700), (700, 300)])
+def test_alibi_several_key_tiles_each_side(D, causal, window, Sq, Sk):
+    # With ALiBi the key tiles of a query block run from the diagonal tile
+    # leftward, then rightward. Several tiles on each side of the diagonal and a
+    # steep slope (0.7, so the max moves by far more than the rescale threshold
+    # across tiles in ascending order) exercise that order against the oracle.
+    _run(1, Sq, Sk, 2, D, causal=causal, window=window, alibi=np.array([0.7, 0.05], dtype=np.float32), seed=11)
