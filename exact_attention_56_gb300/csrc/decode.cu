@@ -443,6 +443,11 @@ __global__ void __launch_bounds__(DecMmaCfg<D, ROT>::THREADS, 1)
   const int n_blocks = ke > ks ? (ke - t0 + C::TK - 1) / C::TK : 0;
   // key tiles of softmax group w: w, w + NW, ...
   auto tiles_of = [&](int w) { return n_blocks > w ? (n_blocks - w + NW - 1) / NW : 0; };
+  // First key of tile jj. A decode row's diagonal key lies at the end of the
+  // cache, where ALiBi's bias peaks, so with ALiBi the tiles run from the last
+  // one down: the running max is set by the first tile and O is rarely rescaled.
+  const bool rev = p.alibi != nullptr;
+  auto key_row = [t0, n_blocks, rev](int jj) { return t0 + (rev ? n_blocks - 1 - jj : jj) * C::TK; };
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -490,7 +495,7 @@ __global__ void __launch_bounds__(DecMmaCfg<D, ROT>::THREADS, 1)
       int issued = 0;
       bool ok = true;
       for (int jj = 0; jj < n_blocks && ok; ++jj) {
-        int row = t0 + jj * C::TK, tb = b;
+        int row = key_row(jj), tb = b;
         if (p.block_table) {  // (row in page, page) coordinates of this tile
           tb = p.block_table[size_t(b) * p.max_pages + row / p.page_size];
           row %= p.page_size;
@@ -629,14 +634,37 @@ __global__ void __launch_bounds__(DecMmaCfg<D, ROT>::THREADS, 1)
       tc_fence_after();
       float x[128];
       tmem_ld_x128f(tmem + lane_addr + uint32_t(sb) * 128, x);
-      const int kbase = t0 + jj * C::TK;
-      // x = scale*log2(e)*qk - slope*log2(e)*|c(i) - j| in log2 units; keys outside [klo, khi) masked
+      const int kbase = key_row(jj);
+      if (has_alibi) {
+        // x = scale*log2(e)*qk - slope*log2(e)*|c(i) - j|, in log2 units
+        const float d0 = float(c_i - kbase);
+        if (kbase + 127 <= c_i || kbase >= c_i) {
+          // keys on one side of the diagonal: the bias on column pairs with the
+          // signed slope (the distances are exact integers)
+          const float ns = (kbase >= c_i) ? slope_log2 : -slope_log2;
+          const uint64_t ns2 = f2_pack(ns, ns), sl2 = f2_pack(sl, sl), st2 = f2_pack(8.0f, 8.0f);
+          uint64_t dist[4];
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const int kj = kbase + c;
-        float v = x[c] * sl;
-        if (has_alibi) v -= slope_log2 * fabsf(float(c_i - kj));
-        x[c] = (kj >= klo && kj < khi) ? v : -INFINITY;
+          for (int k = 0; k < 4; ++k) dist[k] = f2_pack(d0 - float(2 * k), d0 - float(2 * k + 1));
+#pragma unroll
+          for (int c = 0; c < 128; c += 8) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int cc = c + 2 * k;
+              f2_unpack(f2_fma(f2_pack(x[cc], x[cc + 1]), sl2, f2_mul(dist[k], ns2)), x[cc], x[cc + 1]);
+              dist[k] = f2_sub(dist[k], st2);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) x[c] = fmaf(x[c], sl, -slope_log2 * fabsf(d0 - float(c)));
+        }
+      }
+      // keys outside this pair's [klo, khi) are masked; a tile inside it needs no mask
+      if (!(kbase >= klo && kbase + 127 < khi)) {
+        const int lo = klo - kbase, hi = khi - kbase;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) x[c] = (c >= lo && c < hi) ? x[c] : -INFINITY;
       }
       float mq[4];
 #pragma unroll
@@ -646,7 +674,9 @@ __global__ void __launch_bounds__(DecMmaCfg<D, ROT>::THREADS, 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k) mq[k] = max3f(mq[k], x[c + 2 * k], x[c + 2 * k + 1]);
       }
-      const float m_blk = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      // block max in log2 units (without ALiBi, x still holds raw q.k and scale > 0)
+      const float m_blk = has_alibi ? mx : mx * sl;
       const float m_new = fmaxf(m, m_blk);
       float alpha = 1.0f;
       if (m_new != -INFINITY) {
@@ -659,21 +689,33 @@ __global__ void __launch_bounds__(DecMmaCfg<D, ROT>::THREADS, 1)
       }
       l *= alpha;
       const float m_use = (m == -INFINITY) ? 0.0f : m;
-      float rs = 0.0f;
+      // p = 2^(x*sl - m) without ALiBi; with ALiBi x is already in log2 units.
+      // Column pairs go through the paired FMA and add; rs2[k] sums the pairs
+      // e with e % 2 == k.
+      const float mul = has_alibi ? 1.0f : sl;
+      const uint64_t mul2 = f2_pack(mul, mul), nm2 = f2_pack(-m_use, -m_use);
+      uint64_t rs2[2] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f)};
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int c = q4 * 32 + 2 * e;
-          const float p0 = ex2_approx(x[c] - m_use);
-          const float p1 = ex2_approx(x[c + 1] - m_use);
-          rs += p0 + p1;
+          float a0, a1;
+          f2_unpack(f2_fma(f2_pack(x[c], x[c + 1]), mul2, nm2), a0, a1);
+          const float p0 = ex2_approx(a0);
+          const float p1 = ex2_approx(a1);
+          rs2[e & 1] = f2_add(rs2[e & 1], f2_pack(p0, p1));
           pk[e] = pack_bf16x2(p0, p1);
         }
         tmem_st_x16(tmem + lane_addr + uint32_t(sb) * 128 + q4 * 16, pk);
       }
-      l += rs;
+      {
+        float r0, r1, r2, r3;
+        f2_unpack(rs2[0], r0, r1);
+        f2_unpack(rs2[1], r2, r3);
+        l += (r0 + r1) + (r2 + r3);
+      }
       if (__any_sync(0xffffffffu, alpha != 1.0f) && j > 0) {
         // O must hold this group's P V of its previous tile before it is rescaled.
         if (!(ok = fa_wait_warp(&bars->pv_done[w], uint32_t(j - 1) & 1u, watch, SITE_DM_PV))) break;

@@ -160,7 +160,9 @@ def test_decode_query_pairs_share_a_cta(H, Hk, Sq, D):
     inp = _inputs(B, Sq, Sk, H, Hk, D, 350 + H + Hk + Sq + D)
     q, k, v = (to_dev(inp[n]) for n in ("q", "k", "v"))
     f64 = [bf16_bits_to_f64(inp[x]) for x in ("q", "k", "v")]
-    cases = [dict(causal=True), dict(causal=False, window=(100, 0), alibi=alibi_slopes_geometric(H))]
+    # the causal ALiBi case spans all 7 key tiles (run from the last tile down with ALiBi)
+    cases = [dict(causal=True), dict(causal=False, window=(100, 0), alibi=alibi_slopes_geometric(H)),
+             dict(causal=True, alibi=alibi_slopes_geometric(H))]
     for case in cases:
         window, alibi = case.get("window", (-1, -1)), case.get("alibi")
         for n in (0, 1, 5):
