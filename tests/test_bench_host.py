@@ -74,3 +74,41 @@ def test_reference_arm_json_line():
 def test_reference_arm_other_ranks_exit_quietly(rank):
     r = _bench(["--impl", "reference", "--steps", "1", "--warmup", "3"], {"RANK": rank, "WORLD_SIZE": "2"})
     assert r.returncode == 0 and not r.stdout.strip()
+
+
+def test_clock_sampler_with_a_fake_nvidia_smi(tmp_path, monkeypatch):
+    """The sampler waits for its first sample, keeps every line the tool prints
+    while the region runs, and reports the median loaded clock and any active
+    throttle reason."""
+    import time
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text("#!/bin/sh\n"
+                    "i=0\n"
+                    "while true; do\n"
+                    "  if [ $i -eq 2 ]; then r='Active'; else r='Not Active'; fi\n"
+                    "  echo \"2055, 2070, 900.0, Not Active, Not Active, Not Active, $r\"\n"
+                    "  i=$((i+1)); sleep 0.02\n"
+                    "done\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{tmp_path}{os.pathsep}{os.environ['PATH']}")
+    with bench.ClockSampler(0) as clk:
+        assert clk.lines, "the timed region must not start before the first sample"
+        time.sleep(0.3)
+    s = clk.summary()
+    assert s["samples"] >= 5
+    assert s["sm_mhz"] == 2055.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+
+    monkeypatch.setenv("PATH", str(tmp_path))  # no nvidia-smi anywhere
+    with bench.ClockSampler(0) as clk:
+        pass
+    assert clk.summary()["samples"] == 0
