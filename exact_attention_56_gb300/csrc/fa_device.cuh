@@ -33,4 +33,25 @@ __host__ __device__ __forceinline__ RowRange live_range(int i, int Sq, int Sk, i
   return RowRange{lo, hi};
 }
 
+#ifdef __CUDACC__
+// Block coordinates with x as the rank of a CTA's work unit within its (y, z) =
+// (head, batch). When the units of one (head, batch) differ in work (masks bounded
+// on the right), the grid is renumbered with the rank slowest. The hardware issues
+// CTAs roughly in linear order, so each wave then takes the same rank from every
+// (head, batch), and the longest units run first across the whole grid, not only
+// within one (head, batch). Otherwise consecutive CTAs share a head's K/V in L2,
+// which matters more when the units are short.
+struct BlockCoord {
+  int x, y, z;
+};
+__device__ __forceinline__ BlockCoord block_coord(bool rank_slowest) {
+  if (!rank_slowest) return BlockCoord{int(blockIdx.x), int(blockIdx.y), int(blockIdx.z)};
+  const unsigned long long yz = (unsigned long long)gridDim.y * gridDim.z;
+  const unsigned long long lin =
+      blockIdx.x + (unsigned long long)gridDim.x * (blockIdx.y + (unsigned long long)gridDim.y * blockIdx.z);
+  const unsigned int rem = unsigned(lin % yz);
+  return BlockCoord{int(lin / yz), int(rem % gridDim.y), int(rem / gridDim.y)};
+}
+#endif
+
 }  // namespace fa

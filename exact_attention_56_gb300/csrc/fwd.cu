@@ -127,9 +127,14 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
   const int warp = int(warp_id());
   const int lane = int(lane_id());
 
-  const int h = blockIdx.y;
+  // x: rank of this CTA's query group, longest first for right-bounded masks.
+  // With 16 or more groups per head the ranks are ordered across the whole
+  // grid (block_coord); with fewer, a head's groups stay together, where the
+  // balance is already fine and its K/V stays in L2.
+  const BlockCoord bc = block_coord(p.wr >= 0 && gridDim.x >= 16);
+  const int h = bc.y;
   const int hkv = h / p.group;  // key/value head of this query head
-  const int b = blockIdx.z;
+  const int b = bc.z;
   // This sequence's lengths and first rows; tb is the TMA batch coordinate.
   int Sq = p.Sq, Sk = p.Sk, q_off = 0, k_off = 0, tb = b;
   if (VARLEN) {
@@ -140,9 +145,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
     tb = 0;
   }
   const int n_groups = (Sq + NT * 128 - 1) / (NT * 128);
-  if (int(blockIdx.x) >= n_groups) return;  // shorter than the longest sequence: no rows here
+  if (bc.x >= n_groups) return;  // shorter than the longest sequence: no rows here
   // Groups with more live keys first (causal / right-bounded windows).
-  const int qg = (p.wr >= 0) ? (n_groups - 1 - int(blockIdx.x)) : int(blockIdx.x);
+  const int qg = (p.wr >= 0) ? (n_groups - 1 - bc.x) : bc.x;
   const int row0 = qg * NT * 128;
   const int last_row = min(Sq, row0 + NT * 128) - 1;
 

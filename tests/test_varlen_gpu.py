@@ -122,3 +122,11 @@ def test_equal_lengths_match_the_padded_layout_bitwise():
     assert torch.equal(lse.permute(1, 0, 2).reshape(H, B * S), lse_p)
     for a, b in ((dq, dq_p), (dk, dk_p), (dv, dv_p)):
         assert torch.equal(a.reshape(B * S, H, D).view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("window", [(-1, 0), (1000, 0)])
+def test_forward_packed_long_sequence_among_short_ones(window):
+    # A 4500-row sequence gives the grid 18 query groups per head, enough for the
+    # forward to order the groups across the whole grid; the short sequences'
+    # CTAs past their own groups must leave without writing.
+    _run_fwd(2, 1, 64, window=window, seed=31, len_q=[300, 4500, 129], len_k=[700, 4500, 1])
