@@ -13,10 +13,9 @@ section names below refer to that page.
 Parity status: every function here is pinned by tests under
 ``tests/test_oracle_*.py`` (worked mask examples, closed forms,
 invariants, an independent library routine and finite differences).
-One partial exception: the dropout generator ``philox4x32_10`` is pinned in
-structure (independently inverted rounds) and statistics, but not against
-published known-answer vectors, so its constants rest on the published
-definition as written here (parity partially pinned).
+The dropout generator ``philox4x32_10`` is pinned by the published
+known-answer vectors of Philox4x32-10 (Random123's kat_vectors), besides
+independently inverted rounds and output statistics.
 """
 from .attention import (  # noqa: F401
     live_mask,

@@ -3,24 +3,27 @@ section "参数说明": dropout_p) and its Philox4x32-10 generator (Salmon et al
 "Parallel random numbers: as easy as 1, 2, 3", SC 2011), both readings stated in
 the oracle since the pages give no generator.
 
-Generator: each round is inverted independently (modular inverses of the
-multipliers, Python integers), so the round structure and key schedule are
-checked by recovering the counter; output bits are balanced, the drop fraction
-matches p, and one flipped counter bit changes about half the output bits. No
-published known-answer vector is used, so the constants themselves rest on the
-definition as written (the GPU generator, written separately from the same
-definition, is compared mask for mask in the GPU tests).
+Generator: the published known-answer vectors of Philox4x32-10 (Random123's
+kat_vectors, tests/golden/philox4x32_10_kat.txt) fix the multipliers, the key
+increments, the round count and the output word order; each round is also
+inverted independently (modular inverses of the multipliers, Python integers),
+so the round structure and key schedule are checked by recovering the counter;
+output bits are balanced, the drop fraction matches p, and one flipped counter
+bit changes about half the output bits.
 Dropout: p = 0 gives the plain result; the forward and autograd backward of an
 explicit torch float64 formula with the same mask agree; D = rowsum(dO o O)
 still equals sum_j P o dP; averaged over many seeds the output is unbiased.
 """
 import math
+import os
 
 import numpy as np
 import pytest
 import torch
 
 import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "philox4x32_10_kat.txt")
 
 M0, M1, W0, W1 = oracle.attention.PHILOX_M0, oracle.attention.PHILOX_M1, oracle.attention.PHILOX_W0, \
     oracle.attention.PHILOX_W1
@@ -37,6 +40,28 @@ def _inverse_philox(y, k0, k1):
         x3 = y2 ^ ((M0 * x0) >> 32) ^ kr1
         y0, y1, y2, y3 = x0, x1, x2, x3
     return y0, y1, y2, y3
+
+
+def _kat_rows():
+    rows = []
+    with open(GOLDEN) as f:
+        for ln in f:
+            if ln.strip() and not ln.startswith("#"):
+                rows.append([int(t, 16) for t in ln.split()])
+    return rows
+
+
+def test_known_answer_vectors():
+    rows = _kat_rows()
+    assert len(rows) == 3
+    for w in rows:
+        y = [int(a[0]) for a in oracle.philox4x32_10(*([c] for c in w[:4]), w[4], w[5])]
+        assert y == w[6:], [hex(t) for t in y]
+    # the same vectors as one batch of counters (the array path the dropout mask uses)
+    cols = np.array([w[:4] for w in rows], dtype=np.uint64).T
+    for w, k in zip(rows, range(len(rows))):
+        y = oracle.philox4x32_10(*(c[k:k + 1] for c in cols), w[4], w[5])
+        assert [int(t[0]) for t in y] == w[6:]
 
 
 def test_rounds_invert_to_the_counter():
