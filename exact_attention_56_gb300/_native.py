@@ -2,7 +2,6 @@
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 import threading
 
@@ -125,7 +124,9 @@ def _need(t, name, dtype, shape=None, device=None):
 
 
 def _scale(softmax_scale, D):
-    return float(softmax_scale) if softmax_scale is not None else 1.0 / math.sqrt(D)
+    """The scale argument as the C ABI takes it: None passes 0, which the library
+    folds to its default 1/sqrt(D) (as it does any value <= 0)."""
+    return float(softmax_scale) if softmax_scale is not None else 0.0
 
 
 def _alibi(alibi_slopes, B, H, device):

@@ -80,14 +80,7 @@ bool make_bshd_map_box(CUtensorMap* map, const void* base, int B, int S, int H, 
   return r == CUDA_SUCCESS;
 }
 
-}  // namespace fa
-
-using fa::AttnShape;
-
-static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-// Shared validation; fills `s`. D support is checked by the caller.
-static int check_common(int B, int Sq, int Sk, int H, int Hk, int D, float scale, int causal, int wl, int wr,
+int check_common(int B, int Sq, int Sk, int H, int Hk, int D, float scale, int causal, int wl, int wr,
                         const float* alibi, int alibi_bstride, AttnShape* s) {
   if (B < 1 || Sq < 1 || Sk < 1 || H < 1 || D < 1) return FA_ERR_INVALID;
   if (Hk < 1 || H % Hk != 0) return FA_ERR_INVALID;
@@ -113,6 +106,13 @@ static int check_common(int B, int Sq, int Sk, int H, int Hk, int D, float scale
   s->alibi_bstride = alibi ? alibi_bstride : 0;
   return FA_OK;
 }
+
+}  // namespace fa
+
+using fa::AttnShape;
+using fa::check_common;
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 extern "C" {
 

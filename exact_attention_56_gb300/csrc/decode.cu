@@ -929,9 +929,10 @@ int kv_append_launch(const AttnShape& s, const void* k_new, const void* v_new, v
 // Workspace: the split partials O_s (fp32) and L_s, then room for the rotated
 // query as a bf16 pair q_hi, q_lo (the tensor-core kernel's query tile arrives
 // by TMA, so rotary is applied before it, into these copies).
-size_t decode_workspace_bytes(int B, int Sq, int H, int D, int n) {
+size_t decode_workspace_bytes(int B, int Sq, int H, int D, int n, bool with_rotary) {
   const size_t units = size_t(B) * Sq * H * n;
-  return align256(units * D * 4) + align256(units * 4) + 2 * align256(size_t(B) * Sq * H * D * 2);
+  const size_t part = align256(units * D * 4) + align256(units * 4);
+  return with_rotary ? part + 2 * align256(size_t(B) * Sq * H * D * 2) : part;
 }
 
 // Rotary of the queries for the tensor-core decode: q rotated in fp32 at each

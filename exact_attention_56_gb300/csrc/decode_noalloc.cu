@@ -11,9 +11,11 @@
 //
 // Rules of use:
 //  * The array holds kScratchBytes on every GPU that loads the library, for
-//    the life of the process. Requests whose partials would not fit
-//    (fa_decode_workspace_size() > kScratchBytes) are rejected with
-//    FA_ERR_WORKSPACE.
+//    the life of the process. It holds only split partials,
+//    B * Sq * H * splits * (D + 1) fp32 values (each part rounded up to 256
+//    bytes). With num_splits == 0 the automatic split count is lowered until
+//    they fit; a request that does not fit even so, or an explicit
+//    num_splits whose partials do not fit, is rejected with FA_ERR_WORKSPACE.
 //  * Its device address is looked up once per device, on the first call
 //    made with that device current; make that first call before any stream
 //    capture.
@@ -64,32 +66,23 @@ extern "C" int fa_decode_splitkv_noalloc(const void* q, const void* k_cache, con
   if (!q || !k_cache || !v_cache || !out || !lse) return FA_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(lse))
     return FA_ERR_INVALID;
-  if (B < 1 || Sq < 1 || Sk < 1 || H < 1 || D < 1) return FA_ERR_INVALID;
-  if (Hk < 1 || H % Hk != 0) return FA_ERR_INVALID;
-  if (window_left < -1 || window_right < -1) return FA_ERR_INVALID;
-  if (alibi_slopes) {
-    if (reinterpret_cast<uintptr_t>(alibi_slopes) & 3u) return FA_ERR_INVALID;
-    if (alibi_batch_stride != 0 && alibi_batch_stride != H) return FA_ERR_INVALID;
-  }
-  if (Sq > 16 || Sk > (1 << 30)) return FA_ERR_UNSUPPORTED;
-  if (B > 65535 || H > 65535) return FA_ERR_UNSUPPORTED;  // gridDim.y and gridDim.z limits
+  fa::AttnShape s;
+  const int st = fa::check_common(B, Sq, Sk, H, Hk, D, scale, causal, window_left, window_right, alibi_slopes,
+                                  alibi_batch_stride, &s);
+  if (st != FA_OK) return st;
   if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
+  if (Sq > 16) return FA_ERR_UNSUPPORTED;
   if (num_splits < 0 || num_splits > 256) return FA_ERR_INVALID;
-  const int n = num_splits == 0 ? fa::decode_auto_splits(B, Sq, Sk, H, Hk, D) : num_splits;
-  if (fa::decode_workspace_bytes(B, Sq, H, D, n) > kScratchBytes) return FA_ERR_WORKSPACE;
+  // This call never runs rotary, so the array holds only the split partials.
+  auto fits = [&](int n) { return fa::decode_workspace_bytes(B, Sq, H, D, n, false) <= kScratchBytes; };
+  int n = num_splits;
+  if (n == 0) {
+    // the automatic count, lowered until its partials fit the array
+    n = fa::decode_auto_splits(B, Sq, Sk, H, Hk, D);
+    while (n > 1 && !fits(n)) --n;
+  }
+  if (!fits(n)) return FA_ERR_WORKSPACE;
   void* ws = scratch_address();
   if (!ws) return FA_ERR_CUDA;
-  fa::AttnShape s;
-  s.B = B;
-  s.Sq = Sq;
-  s.Sk = Sk;
-  s.H = H;
-  s.Hk = Hk;
-  s.D = D;
-  s.scale = (scale > 0.0f && isfinite(scale)) ? scale : 1.0f / sqrtf(float(D));
-  s.wl = window_left;
-  s.wr = causal ? 0 : window_right;
-  s.alibi = alibi_slopes;
-  s.alibi_bstride = alibi_slopes ? alibi_batch_stride : 0;
   return fa::decode_launch(s, q, k_cache, v_cache, out, lse, ws, n, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -42,6 +42,14 @@ struct CacheArgs {
   Rotary rot;
 };
 
+// Argument checks shared by every attention entry point: sizes, head groups,
+// window bounds, ALiBi pointer and stride, and the grid limits (B, H <= 65535,
+// Sq, Sk <= 2^30). Fills `s` with the defaults folded in (scale <= 0 or NaN ->
+// 1/sqrt(D), causal -> window right = 0). Returns FA_OK or a negative fa_status;
+// the supported head dims are checked by each caller.
+int check_common(int B, int Sq, int Sk, int H, int Hk, int D, float scale, int causal, int wl, int wr,
+                 const float* alibi, int alibi_bstride, AttnShape* s);
+
 // Status word of the current device (device pointer), or NULL on failure.
 unsigned int* device_status_word();
 
@@ -66,7 +74,9 @@ int decode_launch(const AttnShape& s, const void* q, const void* k, const void* 
 // seqlens[b], the keys rotated (cache.rot); run before decode_launch.
 int kv_append_launch(const AttnShape& s, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                      const CacheArgs& cache, cudaStream_t stream);
-size_t decode_workspace_bytes(int B, int Sq, int H, int D, int num_splits);
+// Workspace of a decode call: the split partials, then (with_rotary) the rotated
+// query pair that only a rotary call on the tensor-core kernel writes.
+size_t decode_workspace_bytes(int B, int Sq, int H, int D, int num_splits, bool with_rotary = true);
 // FA_ERR_UNSUPPORTED when the split kernel's grid would exceed the hardware's
 // limits; checked before the first launch of a decode call.
 int decode_check(const AttnShape& s, const CacheArgs* cache);

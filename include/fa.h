@@ -270,8 +270,12 @@ int fa_decode_kvcache(const void* q, void* k_cache, void* v_cache, const int* ca
  * results are those of fa_decode_splitkv minus the workspace: the split
  * partials live in an 8 MiB array of the library's own device memory, which
  * every GPU that loads the library holds until the process exits.
- * - Returns FA_ERR_WORKSPACE if fa_decode_workspace_size() for the request
- *   exceeds 8 MiB (8388608 bytes).
+ * - The array holds only the split partials, B * Sq * H * splits * (D + 1)
+ *   fp32 values, each of the two parts rounded up to 256 bytes; it never
+ *   holds a rotated query, since this call takes no rotary tables.
+ * - num_splits == 0 takes fa_decode_num_splits() and lowers it until the
+ *   partials fit in 8 MiB (8388608 bytes). Returns FA_ERR_WORKSPACE if they do
+ *   not fit even with one split, or if an explicit num_splits does not fit.
  * - The first call on a device looks up the array's device address (with
  *   that device current); make it before any stream capture.
  * - All calls share the array: calls whose kernels may overlap on the GPU
