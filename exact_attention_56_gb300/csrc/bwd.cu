@@ -12,7 +12,11 @@
 //
 //   fa_bwd_pre       D_i = rowsum(dO_i * O_i) and L2_i = L_i*log2(e), padded to
 //                    128-row tiles (+inf on padding and on rows without keys),
-//                    and fp16 copies of Q, K, V and dO.
+//                    fp16 copies of Q, K, V and dO, and each (sequence,
+//                    key/value head) group's largest |q|, |k|, |v|, |dO|.
+//   fa_bwd_rescale   copies again, times a power of two, the groups whose
+//                    magnitudes lie outside what fp16 keeps exactly (see
+//                    "operand range" below); nothing else for the rest.
 //   fa_bwd_dkdv      one CTA per (128-key tile, key/value head, batch), looping
 //                    over the live 128-row query tiles of every query head
 //                    that shares the key/value head:
@@ -34,10 +38,9 @@
 // is bitwise reproducible; the deterministic flag costs nothing.
 //
 // Precision and MMA rate: every product takes fp16 operands (P, dS and exact
-// fp16 copies of the bf16 inputs). fp16 keeps 11 significant bits, enough for
-// the gradients to stay at bf16's own output rounding against an fp64
-// reference with one MMA per product; it limits the backward's inputs to the
-// fp16 range (|x| < 65504).
+// fp16 copies of the bf16 inputs, scaled per group by a power of two). fp16
+// keeps 11 significant bits, enough for the gradients to stay at bf16's own
+// output rounding against an fp64 reference with one MMA per product.
 //
 // Both main kernels follow one schedule: the score tile of the next step is
 // issued as soon as the compute warps hold the current one in registers, and
@@ -68,6 +71,13 @@ struct BwdParams {
   uint16_t* do16;
   uint16_t* k16;
   uint16_t* v16;
+  // (B, Hk, 4) uint32: largest |x| of q, k, v, dout over each (sequence,
+  // key/value head) group, as bf16 magnitude bits; see group_exps()
+  uint32_t* amax;
+  // (B, Hk, AMAX_REPS, 4) uint32: the same maxima as the pre-pass gathers them,
+  // spread over replicas so that concurrent atomics rarely share an address
+  uint32_t* amax_rep;
+  int n_chunks;  // 64-token chunks per sequence (rescale pass)
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -102,6 +112,7 @@ enum : uint32_t {
   SITE_KV_ACC = 0x39,
   SITE_KV_DOEMPTY = 0x3A,
   SITE_KV_ALIGN = 0x3B,
+  SITE_KV_FAC = 0x3C,
   SITE_DQ_EMPTY = 0x41,
   SITE_DQ_Q = 0x42,
   SITE_DQ_K = 0x43,
@@ -111,6 +122,7 @@ enum : uint32_t {
   SITE_DQ_DP = 0x47,
   SITE_DQ_ACC = 0x48,
   SITE_DQ_ALIGN = 0x49,
+  SITE_DQ_FAC = 0x4A,
 };
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -170,15 +182,143 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 u) {
   return make_uint4(bf16x2_to_f16x2(u.x), bf16x2_to_f16x2(u.y), bf16x2_to_f16x2(u.z), bf16x2_to_f16x2(u.w));
 }
 
-// ============================================================================ pre-pass
-// One 16-byte chunk (8 elements) of one row per item:
+// ============================================================================ operand range
+// The products run on fp16 copies of the bf16 inputs. fp16 has bf16's
+// precision and more, but a far smaller range: normal from 2^-14 to 65504.
+// Gradients with respect to the output are often 1e-5 .. 1e-8, where fp16
+// loses most of its bits, and large inputs overflow. So each (sequence,
+// key/value head) group of q, k, v and dout gets a power-of-two factor 2^e,
+// copied as x * 2^e, which is exact wherever the product stays in fp16's
+// normal range. The factors come back out exactly:
+//   S'  = (Q 2^eq)(K 2^ek)^T = 2^(eq+ek) S       -> scale folded as 2^-(eq+ek)
+//   dP' = (dO 2^edo)(V 2^ev)^T = 2^(edo+ev) dP    -> D kept as 2^(edo+ev) D
+//   dS' = P o (dP' - D') = 2^(edo+ev) dS
+//   dV' = P^T (dO 2^edo)                          -> times 2^-edo
+//   dK' = dS'^T (Q 2^eq), dQ' = dS' (K 2^ek)      -> times scale 2^-(edo+ev+eq|ek)
+// e puts the group's largest magnitude in [4, 8): then |dP'| <= |dO'_i| |V'_j|
+// <= 64 D and |dS'| <= 128 D, inside fp16's range for D <= 128. A group
+// already in [1, 8) keeps e = 0, so inputs of natural size are copied as they
+// are. A group of zeros, or holding inf or NaN, keeps e = 0 too.
+struct GroupExp {
+  int q, k, v, dO;
+};
+// e for a group whose largest magnitude has bf16 bits `a` (sign cleared)
+__device__ __forceinline__ int range_exp(uint32_t a) {
+  if (a == 0 || a >= 0x7F80u) return 0;
+  const int ef = int(a >> 7);  // biased exponent; 0 for subnormals (a * 2^-133)
+  const int fl = ef > 0 ? ef - 127 : (31 - __clz(int(a & 0x7Fu))) - 133;  // floor(log2 |x|max)
+  if (fl >= 0 && fl <= 2) return 0;
+  return max(-120, min(120, 2 - fl));
+}
+__device__ __forceinline__ GroupExp group_exps(const uint32_t* amax, int b, int hk, int Hk) {
+  const uint4 a = *reinterpret_cast<const uint4*>(amax + (size_t(b) * Hk + hk) * 4);
+  return GroupExp{range_exp(a.x), range_exp(a.y), range_exp(a.z), range_exp(a.w)};
+}
+// 2^e as a float, |e| <= 126 (exact)
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float(uint32_t(127 + e) << 23); }
+// scale * 2^-E as two factors m1 * m2, each exact; m2 = 1 unless |E| > 100, so
+// x * m1 * m2 rounds once whenever the result can be represented at all.
+__device__ __forceinline__ void unscale_factors(float scale, int E, float& m1, float& m2) {
+  const int e1 = max(-100, min(100, E));
+  m1 = scale * pow2f(-e1);
+  m2 = pow2f(-max(-126, min(126, E - e1)));
+}
+// bf16 pair times m -> fp16 pair (exact while |x m| stays in fp16's normal range)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_mul(uint32_t v, float m) {
+  return pack_f16x2(__uint_as_float(v << 16) * m, __uint_as_float(v & 0xFFFF0000u) * m);
+}
+__device__ __forceinline__ uint4 bf16x8_to_f16x8_mul(uint4 u, float m) {
+  return make_uint4(bf16x2_to_f16x2_mul(u.x, m), bf16x2_to_f16x2_mul(u.y, m), bf16x2_to_f16x2_mul(u.z, m),
+                    bf16x2_to_f16x2_mul(u.w, m));
+}
+// running max of the magnitudes of eight bf16 values, as two 16-bit halves
+__device__ __forceinline__ uint32_t absmax8(uint32_t m, uint4 u) {
+  m = __vmaxu2(m, u.x & 0x7FFF7FFFu);
+  m = __vmaxu2(m, u.y & 0x7FFF7FFFu);
+  m = __vmaxu2(m, u.z & 0x7FFF7FFFu);
+  return __vmaxu2(m, u.w & 0x7FFF7FFFu);
+}
+// fp32 sum over eight element pairs of (a * ma) * (o * mo), in a fixed order
+__device__ __forceinline__ float dot8_mul(uint4 a, uint4 o, float ma, float mo, float acc) {
+  const uint32_t x[4] = {a.x, a.y, a.z, a.w};
+  const uint32_t y[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    acc = fmaf(__uint_as_float(x[t] << 16) * ma, __uint_as_float(y[t] << 16) * mo, acc);
+    acc = fmaf(__uint_as_float(x[t] & 0xFFFF0000u) * ma, __uint_as_float(y[t] & 0xFFFF0000u) * mo, acc);
+  }
+  return acc;
+}
+
+// Tokens per chunk of the rescale pass.
+constexpr int CHUNK_TOK = 64;
+// Replicas of each group's maxima in the pre-pass (block x writes replica x % AMAX_REPS).
+constexpr int AMAX_REPS = 32;
+
+// The query rows of one group in one chunk: items (token, head of the group,
+// 16-byte chunk) with the chunk fastest, so a row's D/8 chunks sit on
+// consecutive lanes of one warp. fn(live, token, g, element offset) runs on
+// every lane, live or past the end; the loop is warp-uniform, so fn may shuffle.
+template <int D, typename F>
+__device__ __forceinline__ void for_q_items(const BwdParams& p, const SeqInfo& si, int b, int hk, int t0, F fn) {
+  constexpr int CPR = D / 8;
+  const long long per_tok = (long long)p.group * CPR;
+  const int n_tok = max(0, min(CHUNK_TOK, si.Sq - t0));
+  const long long items = n_tok * per_tok;
+  const int lane = int(threadIdx.x & 31);
+  for (long long base = (long long)threadIdx.x - lane; base < items; base += blockDim.x) {
+    const long long it = base + lane;
+    const int tl = int(it / per_tok);
+    const long long rem = it - tl * per_tok;
+    const size_t tok = p.cu_q ? size_t(si.q_off) + t0 + tl : size_t(b) * p.Sq + t0 + tl;
+    fn(it < items, t0 + tl, int(rem / CPR), (tok * p.H + size_t(hk) * p.group) * D + size_t(rem) * 8);
+  }
+}
+// The key rows of one key/value head in one chunk: items (token, chunk).
+template <int D, typename F>
+__device__ __forceinline__ void for_k_items(const BwdParams& p, const SeqInfo& si, int b, int hk, int t0, F fn) {
+  constexpr int CPR = D / 8;
+  const int n_tok = max(0, min(CHUNK_TOK, si.Sk - t0));
+  const long long items = (long long)n_tok * CPR;
+  for (long long it = threadIdx.x; it < items; it += blockDim.x) {
+    const int tl = int(it / CPR);
+    const size_t tok = p.cu_q ? size_t(si.k_off) + t0 + tl : size_t(b) * p.Sk + t0 + tl;
+    fn((tok * p.Hk + hk) * D + size_t(it - (long long)tl * CPR) * 8);
+  }
+}
+
+// Sequence holding packed token `tok` (last b with cu[b] <= tok), searched
+// from b0, a sequence at or before it.
+__device__ __forceinline__ int seq_of(const int* cu, int B, long long tok, int b0) {
+  int lo = b0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu[mid] <= tok) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Largest magnitude over a row's R lanes (pairs of 16-bit magnitudes in), as
+// one 16-bit magnitude; every lane of the warp must call it.
+template <int R>
+__device__ __forceinline__ uint32_t row_absmax(uint32_t m) {
+#pragma unroll
+  for (int off = R / 2; off > 0; off >>= 1) m = __vmaxu2(m, __shfl_xor_sync(0xffffffffu, m, off));
+  return max(m & 0xFFFFu, m >> 16);
+}
+// Pre-pass, one 16-byte chunk (8 elements) of one row per item:
 //   query rows: D_i = rowsum(dO_i o O_i), L2_i = L_i*log2(e) (+inf where L_i = -inf),
 //               fp16 copies of Q_i and dO_i;
 //   key rows:   fp16 copies of K_j and V_j;
 //   padding:    D = 0 and L2 = +inf on the vector rows of each (b, h) past its
-//               sequence, up to the whole 128-row tiles of Sq_pad.
+//               sequence, up to the whole 128-row tiles of Sq_pad;
+//   range:      each row's largest |q|, |dO| (|k|, |v|) into one replica of its
+//               group's maxima (amax_rep, zeroed before), one atomic per row.
 // The three item ranges start on multiples of 32, so each warp works inside one
-// of them and the D/8 lanes of a query row are consecutive lanes of one warp.
+// of them and the D/8 lanes of a row are consecutive lanes of one warp. The
+// grid strides over the items, so the blocks sweep memory together. The copies
+// are taken with e = 0; fa_bwd_rescale_kernel redoes those of groups that need
+// a range factor.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
   constexpr int CPR = D / 8;
@@ -197,23 +337,22 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
     if (wb < k0) {
       const bool live = i < n_q;
       float acc = 0.0f;
+      uint32_t mq = 0, mdo = 0;
       if (live) {
         const long long e = i * 8;  // = row * D + chunk * 8
         const uint4 qv = *reinterpret_cast<const uint4*>(p.q + e);
         const uint4 dov = *reinterpret_cast<const uint4*>(p.dout + e);
         const uint4 ov = *reinterpret_cast<const uint4*>(p.out + e);
-        *reinterpret_cast<uint4*>(p.q16 + e) = bf16x8_to_f16x8(qv);
-        *reinterpret_cast<uint4*>(p.do16 + e) = bf16x8_to_f16x8(dov);
-        const uint32_t a[4] = {dov.x, dov.y, dov.z, dov.w};
-        const uint32_t o[4] = {ov.x, ov.y, ov.z, ov.w};
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          acc = fmaf(__uint_as_float(a[t] << 16), __uint_as_float(o[t] << 16), acc);
-          acc = fmaf(__uint_as_float(a[t] & 0xFFFF0000u), __uint_as_float(o[t] & 0xFFFF0000u), acc);
-        }
+        *reinterpret_cast<uint4*>(p.q16 + e) = bf16x8_to_f16x8_mul(qv, 1.0f);
+        *reinterpret_cast<uint4*>(p.do16 + e) = bf16x8_to_f16x8_mul(dov, 1.0f);
+        mq = absmax8(0, qv);
+        mdo = absmax8(0, dov);
+        acc = dot8_mul(dov, ov, 1.0f, 1.0f, 0.0f);
       }
 #pragma unroll
       for (int off = CPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      mq = row_absmax<CPR>(mq);
+      mdo = row_absmax<CPR>(mdo);
       if (live && (i % CPR) == 0) {
         const long long row = i / CPR;  // token * H + h
         const int h = int(row % p.H);
@@ -221,12 +360,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
         int b, s;
         size_t li;
         if (p.cu_q) {  // the sequence holding this token: last b with cu_q[b] <= tok
-          int lo = 0, hi = p.B - 1;
-          while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (p.cu_q[mid] <= tok) lo = mid; else hi = mid - 1;
-          }
-          b = lo;
+          b = seq_of(p.cu_q, p.B, tok, 0);
           s = int(tok - p.cu_q[b]);
           li = size_t(h) * p.total_q + size_t(tok);
         } else {
@@ -238,13 +372,32 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
         p.dvec[vi] = acc;
         const float L = p.lse[li];
         p.l2[vi] = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
+        uint32_t* g = p.amax_rep + (((size_t)b * p.Hk + h / p.group) * AMAX_REPS + blockIdx.x % AMAX_REPS) * 4;
+        if (mq) atomicMax(g + 0, mq);
+        if (mdo) atomicMax(g + 3, mdo);
       }
     } else if (wb < p0) {
       const long long t = i - k0;
-      if (t < n_k) {
+      const bool live = t < n_k;
+      uint32_t mk = 0, mv = 0;
+      if (live) {
         const long long e = t * 8;
-        *reinterpret_cast<uint4*>(p.k16 + e) = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(p.k + e));
-        *reinterpret_cast<uint4*>(p.v16 + e) = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(p.v + e));
+        const uint4 kv = *reinterpret_cast<const uint4*>(p.k + e);
+        const uint4 vv = *reinterpret_cast<const uint4*>(p.v + e);
+        *reinterpret_cast<uint4*>(p.k16 + e) = bf16x8_to_f16x8_mul(kv, 1.0f);
+        *reinterpret_cast<uint4*>(p.v16 + e) = bf16x8_to_f16x8_mul(vv, 1.0f);
+        mk = absmax8(0, kv);
+        mv = absmax8(0, vv);
+      }
+      mk = row_absmax<CPR>(mk);
+      mv = row_absmax<CPR>(mv);
+      if (live && (t % CPR) == 0) {
+        const long long row = t / CPR;  // token * Hk + hk
+        const long long tok = row / p.Hk;
+        const int b = p.cu_q ? seq_of(p.cu_k, p.B, tok, 0) : int(tok / p.Sk);
+        uint32_t* g = p.amax_rep + (((size_t)b * p.Hk + int(row - tok * p.Hk)) * AMAX_REPS + blockIdx.x % AMAX_REPS) * 4;
+        if (mk) atomicMax(g + 1, mk);
+        if (mv) atomicMax(g + 2, mv);
       }
     } else {
       const long long t = i - p0;
@@ -257,6 +410,67 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
           p.l2[t] = INFINITY;
         }
       }
+    }
+  }
+}
+
+// Folds each group's replicas into its maxima (amax, block x = 0 writes them)
+// and redoes the fp16 copies (and D) of the groups whose range factor is not
+// 1. Block (x, hk, b) takes the 64-token chunks x, x + gridDim.x, ... of group
+// (b, hk); a group that keeps e = 0 everywhere costs each of its blocks one
+// read of its replicas.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_rescale_kernel(const BwdParams p) {
+  constexpr int CPR = D / 8;
+  const int lane = int(threadIdx.x & 31);
+  const int hk = blockIdx.y, b = blockIdx.z;
+  GroupExp ge;
+  {
+    // warp 0: lane r holds replica r; every warp computes the same maxima
+    static_assert(AMAX_REPS == 32, "one replica per lane");
+    const uint4 r = *reinterpret_cast<const uint4*>(p.amax_rep + (((size_t)b * p.Hk + hk) * AMAX_REPS + lane) * 4);
+    uint32_t m[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m[t] = max(m[t], __shfl_xor_sync(0xffffffffu, m[t], off));
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+      *reinterpret_cast<uint4*>(p.amax + ((size_t)b * p.Hk + hk) * 4) = make_uint4(m[0], m[1], m[2], m[3]);
+    ge = GroupExp{range_exp(m[0]), range_exp(m[1]), range_exp(m[2]), range_exp(m[3])};
+  }
+  if ((ge.q | ge.k | ge.v | ge.dO) == 0) return;
+  const SeqInfo si = seq_info(p, b);
+  const float mq = pow2f(ge.q), mk = pow2f(ge.k), mv = pow2f(ge.v), mdo = pow2f(ge.dO);
+  const bool redo_d = (ge.dO | ge.v) != 0;
+  for (int chunk = blockIdx.x; chunk < p.n_chunks; chunk += gridDim.x) {
+    const int t0 = chunk * CHUNK_TOK;
+    if (ge.q | ge.dO | ge.v) {
+      for_q_items<D>(p, si, b, hk, t0, [&](bool live, int s, int g, size_t e) {
+        float acc = 0.0f;
+        if (live) {
+          if (ge.q)
+            *reinterpret_cast<uint4*>(p.q16 + e) = bf16x8_to_f16x8_mul(*reinterpret_cast<const uint4*>(p.q + e), mq);
+          if (redo_d) {
+            const uint4 dov = *reinterpret_cast<const uint4*>(p.dout + e);
+            if (ge.dO) *reinterpret_cast<uint4*>(p.do16 + e) = bf16x8_to_f16x8_mul(dov, mdo);
+            // D' = rowsum((dO 2^edo) o (O 2^ev)): each factor scaled before the product
+            acc = dot8_mul(dov, *reinterpret_cast<const uint4*>(p.out + e), mdo, mv, 0.0f);
+          }
+        }
+        if (redo_d) {
+#pragma unroll
+          for (int off = CPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+          if (live && (lane % CPR) == 0) p.dvec[(size_t(b) * p.H + hk * p.group + g) * p.Sq_pad + s] = acc;
+        }
+      });
+    }
+    if (ge.k | ge.v) {
+      for_k_items<D>(p, si, b, hk, t0, [&](size_t e) {
+        if (ge.k)
+          *reinterpret_cast<uint4*>(p.k16 + e) = bf16x8_to_f16x8_mul(*reinterpret_cast<const uint4*>(p.k + e), mk);
+        if (ge.v)
+          *reinterpret_cast<uint4*>(p.v16 + e) = bf16x8_to_f16x8_mul(*reinterpret_cast<const uint4*>(p.v + e), mv);
+      });
     }
   }
 }
@@ -304,6 +518,8 @@ struct KvBars {
   uint64_t do_full[4], do_empty[4];
   uint64_t s_full, s_free, acc_done, drain;
   uint64_t dp_full[2], pd_ready[2];  // per dP^T buffer
+  uint64_t fac_ready;                 // fac[] written (warp 2)
+  float fac[4];                       // scale_log2 for S^T, dV factor, dK factors m1, m2
   uint32_t tmem_base;
   int abort;
 };
@@ -363,6 +579,7 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
     }
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->drain, 1);
+    mbar_init(&bars->fac_ready, 1);
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -512,6 +729,15 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
         drain_wait_b(&bars->drain, 0);
       }
     }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ range factors of the group
+    if (lane == 0) {
+      const GroupExp ge = group_exps(p.amax, b, hk, p.Hk);
+      bars->fac[0] = p.scale_log2 * pow2f(-ge.q) * pow2f(-ge.k);
+      bars->fac[1] = pow2f(-ge.dO);
+      unscale_factors(p.scale, ge.dO + ge.v + ge.q, bars->fac[2], bars->fac[3]);
+      mbar_arrive(&bars->fac_ready);
+    }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ compute (thread = key row)
     const int w = (warp - 4) / 4;  // query-column group: columns [w*COLS, (w+1)*COLS)
@@ -538,8 +764,9 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
     qbounds(j0, dummy, qhi_min);
     const bool tile_keys_ok = j0 + 127 < Sk;
     const bool has_alibi = p.alibi != nullptr;
-    const float sl = p.scale_log2;
-    bool ok = true;
+    // the group's range factors (warp 2): S^T arrives as 2^(eq+ek) S^T
+    bool ok = fa_wait_warp(&bars->fac_ready, 0, watch, SITE_KV_FAC);
+    const float sl = bars->fac[0];
     for (int ii = 0; ii < n_iter && ok; ++ii) {
       const int d = ii % C::NDO;
       const int hq = hk * p.group + ii / n_qtl;
@@ -653,7 +880,9 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
     const bool row_ok = j < e_sq.Sk;
     const size_t krow = p.cu_q ? size_t(e_sq.k_off) + j : size_t(b) * e_sq.Sk + j;
     __nv_bfloat16* dst = (is_dv ? p.dv : p.dk) + (krow * p.Hk + hk) * size_t(D) + col0;
-    const float mul = is_dv ? 1.0f : p.scale;
+    // dV' = 2^edo dV, dK' = 2^(edo+ev+eq) dK / scale
+    const float mul = is_dv ? bars->fac[1] : bars->fac[2];
+    const float mul2 = is_dv ? 1.0f : bars->fac[3];
     if (n_iter == 0) {
       if (row_ok)
         for (int e = 0; e < SLICE / 8; ++e) reinterpret_cast<uint4*>(dst)[e] = make_uint4(0, 0, 0, 0);
@@ -666,7 +895,7 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
         if (row_ok) {
           uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(a[2 * e] * mul, a[2 * e + 1] * mul);
+          for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(a[2 * e] * mul * mul2, a[2 * e + 1] * mul * mul2);
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             reinterpret_cast<uint4*>(dst + cc * 32)[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
@@ -721,6 +950,8 @@ struct DqBars {
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full, s_free, acc_done, drain;
   uint64_t dp_full[2], ds_ready[2];  // per dP buffer
+  uint64_t fac_ready;                 // fac[] written (warp 2)
+  float fac[4];                       // scale_log2 for S, dQ factors m1, m2
   uint32_t tmem_base;
   int abort;
 };
@@ -774,6 +1005,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     }
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->drain, 1);
+    mbar_init(&bars->fac_ready, 1);
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -896,6 +1128,14 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         drain_wait_b(&bars->drain, 0);
       }
     }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ range factors of the group
+    if (lane == 0) {
+      const GroupExp ge = group_exps(p.amax, b, hkv, p.Hk);
+      bars->fac[0] = p.scale_log2 * pow2f(-ge.q) * pow2f(-ge.k);
+      unscale_factors(p.scale, ge.dO + ge.v + ge.k, bars->fac[1], bars->fac[2]);
+      mbar_arrive(&bars->fac_ready);
+    }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ compute (thread = query row)
     const int w = (warp - 4) / 4;  // key-column group: columns [w*COLS, (w+1)*COLS)
@@ -912,8 +1152,9 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     const bool has_alibi = p.alibi != nullptr;
     const float slope_log2 = has_alibi ? p.alibi[b * p.alibi_bstride + h] * 1.4426950408889634f : 0.0f;
     const int c_i = i + Sk - Sq;
-    const float sl = p.scale_log2;
-    bool ok = true;
+    // the group's range factors (warp 2): S arrives as 2^(eq+ek) S
+    bool ok = fa_wait_warp(&bars->fac_ready, 0, watch, SITE_DQ_FAC);
+    const float sl = bars->fac[0];
     for (int jj = 0; jj < n_blocks && ok; ++jj) {
       const int kb = (jb + jj) * 128 + w * C::COLS;  // first key of this group
       if (!(ok = fa_wait_warp(&bars->s_full, uint32_t(jj) & 1u, watch, SITE_DQ_S))) break;
@@ -1010,8 +1251,9 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       tmem_ld_cols(tmem + lane_addr + C::T_DQ + w * SLICE, a);
       if (row_ok) {
         uint32_t pk[SLICE / 2];
+        const float mul = bars->fac[1], mul2 = bars->fac[2];  // dQ' = 2^(edo+ev+ek) dQ / scale
 #pragma unroll
-        for (int e = 0; e < SLICE / 2; ++e) pk[e] = pack_bf16x2(a[2 * e] * p.scale, a[2 * e + 1] * p.scale);
+        for (int e = 0; e < SLICE / 2; ++e) pk[e] = pack_bf16x2(a[2 * e] * mul * mul2, a[2 * e + 1] * mul * mul2);
 #pragma unroll
         for (int e = 0; e < SLICE / 8; ++e)
           reinterpret_cast<uint4*>(dst)[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
@@ -1032,15 +1274,17 @@ static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Workspace: L2 and D vectors (B, H, Sq_pad) fp32 (Sq_pad: the longest query
 // sequence rounded up to 128 rows), then fp16 copies of Q, dO (rows_q tokens,
-// H heads) and K, V (rows_k tokens, Hk heads), each region 256-byte aligned.
+// H heads) and K, V (rows_k tokens, Hk heads), then the group maxima (B, Hk, 4)
+// and their replicas (B, Hk, AMAX_REPS, 4) uint32, each region 256-byte aligned.
 struct BwdWs {
-  size_t vec, qside, kside;
-  size_t total() const { return 2 * vec + 2 * qside + 2 * kside; }
+  size_t vec, qside, kside, amax, reps;
+  size_t total() const { return 2 * vec + 2 * qside + 2 * kside + amax + reps; }
 };
 static BwdWs bwd_ws(int B, int max_sq, long long rows_q, long long rows_k, int H, int Hk, int D) {
   const size_t sq_pad = size_t((max_sq + 127) / 128) * 128;
   return BwdWs{al256(size_t(B) * H * sq_pad * 4), al256(size_t(rows_q) * H * D * 2),
-               al256(size_t(rows_k) * Hk * D * 2)};
+               al256(size_t(rows_k) * Hk * D * 2), al256(size_t(B) * Hk * 16),
+               al256(size_t(B) * Hk * AMAX_REPS * 16)};
 }
 
 size_t bwd_workspace_bytes(int B, int Sq, int Sk, int H, int Hk, int D, int deterministic) {
@@ -1081,6 +1325,9 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
   p.do16 = reinterpret_cast<uint16_t*>(w + 2 * L.vec + L.qside);
   p.k16 = reinterpret_cast<uint16_t*>(w + 2 * L.vec + 2 * L.qside);
   p.v16 = reinterpret_cast<uint16_t*>(w + 2 * L.vec + 2 * L.qside + L.kside);
+  p.amax = reinterpret_cast<uint32_t*>(w + 2 * L.vec + 2 * L.qside + 2 * L.kside);
+  p.amax_rep = reinterpret_cast<uint32_t*>(w + 2 * L.vec + 2 * L.qside + 2 * L.kside + L.amax);
+  p.n_chunks = (std::max(p.Sq_pad, s.Sk) + CHUNK_TOK - 1) / CHUNK_TOK;  // s.Sk: the longest key sequence
   p.dout = static_cast<const __nv_bfloat16*>(dout);
   p.out = static_cast<const __nv_bfloat16*>(out);
   p.q = static_cast<const __nv_bfloat16*>(q);
@@ -1110,13 +1357,20 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
     return FA_ERR_CUDA;
 
   {
+    // the replicas start at zero; the pre-pass raises them, then the rescale
+    // pass folds them and redoes the copies of groups that need a range factor
+    if (cudaMemsetAsync(p.amax_rep, 0, L.reps, stream) != cudaSuccess) return FA_ERR_CUDA;
     const long long cpr = D / 8;
     const long long n_q = (rows_q * s.H * cpr + 31) & ~31LL;
     const long long n_k = (rows_k * s.Hk * cpr + 31) & ~31LL;
     const long long total = n_q + n_k + (long long)s.B * s.H * p.Sq_pad;
     const long long cap = (long long)device_sm_count() * 8;  // 8 blocks of 256 threads per SM
-    const int grid = int(std::max(1LL, std::min(cap, (total + 255) / 256)));
-    fa_bwd_pre_kernel<D><<<grid, 256, 0, stream>>>(p);
+    fa_bwd_pre_kernel<D><<<int(std::max(1LL, std::min(cap, (total + 255) / 256))), 256, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    // about two blocks per SM over all groups, at least one per group
+    const long long groups = (long long)s.B * s.Hk;
+    const int rx = int(std::max(1LL, std::min((long long)p.n_chunks, (2LL * device_sm_count() + groups - 1) / groups)));
+    fa_bwd_rescale_kernel<D><<<dim3(rx, s.Hk, s.B), 256, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   }
   auto kv = drop ? fa_bwd_dkdv_kernel<D, true> : fa_bwd_dkdv_kernel<D, false>;

@@ -46,10 +46,13 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return bf16_bits_to_f32(bits).astype(np.float64)
 
 
-def normal_bf16_bits(shape, seed: int) -> np.ndarray:
-    """N(0,1) float32 draws from PCG64(seed), rounded once to bf16; returns uint16 bits."""
+def normal_bf16_bits(shape, seed: int, std: float = 1.0) -> np.ndarray:
+    """N(0, std^2) draws: N(0,1) float32 from PCG64(seed), times std in float32,
+    rounded once to bf16; returns uint16 bits."""
     rng = np.random.Generator(np.random.PCG64(seed))
     x = rng.standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        x = x * np.float32(std)
     return f32_to_bf16_bits(x)
 
 

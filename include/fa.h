@@ -136,9 +136,11 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* out, float*
 
 /*
  * Bytes of device workspace fa_bwd needs: the per-row D_i = rowsum(dO * O)
- * and L*log2(e) vectors, (B, H, Sq rounded up to 128) fp32 each, and fp16
- * copies of q, dout (B, Sq, H, D) and k, v (B, Sk, Hk, D), each section
- * rounded up to 256 bytes. Returns 0 for arguments fa_bwd would reject.
+ * and L*log2(e) vectors, (B, H, Sq rounded up to 128) fp32 each, fp16
+ * copies of q, dout (B, Sq, H, D) and k, v (B, Sk, Hk, D), and the largest
+ * magnitudes of q, k, v, dout per (batch, key/value head) group, (B, Hk, 4)
+ * uint32 plus 32 replicas of them (B, Hk, 32, 4), each section rounded up to
+ * 256 bytes. Returns 0 for arguments fa_bwd would reject.
  */
 size_t fa_bwd_workspace_size(int B, int Sq, int Sk, int H, int Hk, int D, int deterministic);
 
@@ -153,9 +155,13 @@ size_t fa_bwd_workspace_size(int B, int Sq, int Sk, int H, int Hk, int D, int de
  * run is bitwise reproducible in either mode, because no output element is
  * accumulated across thread blocks: one kernel per 128-key tile produces dK
  * and dV, another per 128-row query tile produces dQ.
- * Precision: the products run on fp16 copies of the inputs with fp16 P and
- * dS and fp32 accumulation, so dout, q, k and v must lie in the fp16 range
- * (|x| < 65504; larger values become infinite and the gradients non-finite).
+ * Precision: the products run on fp16 operands (copies of the inputs, P and
+ * dS) with fp32 accumulation. Each (sequence, key/value head) group of q, k,
+ * v and dout is copied times a power of two that puts its largest magnitude
+ * in [4, 8) (or left as is when it lies in [1, 8)), and the factors are taken
+ * back out exactly, so inputs of any finite bf16 magnitude keep fp16's
+ * precision: gradients of 1e-8 are as accurate, relative to their size, as
+ * gradients of 1. Non-finite inputs give non-finite gradients.
  * workspace: caller-owned device buffer of at least fa_bwd_workspace_size()
  * bytes, 256-byte aligned; its contents on entry are ignored.
  * Supported: D in {64, 128}.

@@ -60,3 +60,16 @@ def assert_bf16_close_beyond_rounding(got, ref, what=""):
     rr = rel_rms(got, ref) if got.size else 0.0
     assert excess <= ATOL_BF16, f"{what}: max (|err| - 2^-8 |ref|) {excess:.3e} > {ATOL_BF16}"
     assert rr <= RELRMS_BF16, f"{what}: rel RMS {rr:.3e} > {RELRMS_BF16}"
+
+
+# A problem whose exact result is f times one of natural size (inputs scaled by
+# known factors): the error divided by f must meet the bf16 bound, and the
+# relative RMS (scale-free, no floor) the 1e-2 bound.
+def assert_bf16_close_scaled(got, ref, f, what=""):
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    err = float(np.max(np.abs(got / f - ref / f)))
+    nref = np.linalg.norm(ref)
+    assert nref > 0, f"{what}: reference is all zero"
+    rr = float(np.linalg.norm(got - ref) / nref)
+    assert err <= ATOL_BF16, f"{what}: max |err| / {f:g} = {err:.3e} > {ATOL_BF16}"
+    assert rr <= RELRMS_BF16, f"{what}: rel RMS {rr:.3e} > {RELRMS_BF16}"
