@@ -5,10 +5,16 @@ One step = one pass of the whole hot path on synthetic inputs:
     seqlen S in {512, 1k, 2k, 4k, 8k, 16k}, batch 16384/S, causal off and on,
     each point a forward (fa_fwd) and a backward (fa_bwd);
   * split-KV decode (fa_decode_splitkv): B=16, H=32, D=128, one query row,
-    KV caches of 4k, 32k and 128k keys.
+    KV caches of 4k, 32k and 128k keys;
+  * the other workload shapes: the mask variants (B=2, H=16, D=128: causal
+    with Sq=2048, Sk=8192; window (4096, 0) at 16k; causal + ALiBi at 4k),
+    each a forward and a backward, and the long head dim (B=1, H=8, D=256,
+    16k, forward only, causal off and on).
 The headline value is the sweep's forward+backward TFLOP/s (4*B*H*S*S*D for
 the forward, halved for causal, and 2.5x that for the backward); the forward
-alone and decode HBM GB/s are reported beside it.
+alone, decode HBM GB/s and each other workload (with both the convention
+flops and the exact count over the live (query, key) pairs) are reported
+beside it.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun every rank runs the same per-GPU workload on its own GPU
@@ -31,6 +37,20 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 SWEEP_S = (512, 1024, 2048, 4096, 8192, 16384)
+# The other workload shapes, timed in every step beside the sweep: the mask
+# variants (fwd + bwd, B2 H16 D128) and the long head dim (forward only).
+WORKLOADS = (
+    dict(name="causal 2048x8192 (bottom-right)", B=2, Sq=2048, Sk=8192, H=16, D=128, causal=True, window=(-1, -1),
+         alibi=False, bwd=True),
+    dict(name="window (4096, 0) at 16k", B=2, Sq=16384, Sk=16384, H=16, D=128, causal=False, window=(4096, 0),
+         alibi=False, bwd=True),
+    dict(name="causal + ALiBi at 4k", B=2, Sq=4096, Sk=4096, H=16, D=128, causal=True, window=(-1, -1), alibi=True,
+         bwd=True),
+    dict(name="long head dim D256 16k", B=1, Sq=16384, Sk=16384, H=8, D=256, causal=False, window=(-1, -1),
+         alibi=False, bwd=False),
+    dict(name="long head dim D256 16k causal", B=1, Sq=16384, Sk=16384, H=8, D=256, causal=True, window=(-1, -1),
+         alibi=False, bwd=False),
+)
 SWEEP_DH = ((64, 32), (128, 16))
 DECODE_SK = (4096, 32768, 131072)
 DECODE_B, DECODE_H, DECODE_D = 16, 32, 128
@@ -61,6 +81,29 @@ def sweep_points():
 def fwd_flops(pt):
     f = 4.0 * pt["B"] * pt["H"] * pt["S"] * pt["S"] * pt["D"]
     return f / 2 if pt["causal"] else f
+
+
+def live_pairs(Sq, Sk, causal, window):
+    """Exact (query row, key) pairs the mask keeps, per (batch, head): row i keeps
+    keys [c - left, c + right] of its bottom-right diagonal c = i + Sk - Sq,
+    clipped to [0, Sk - 1] (causal: right = 0; -1: unbounded)."""
+    import numpy as np
+
+    wl, wr = window
+    if causal:
+        wr = 0
+    c = np.arange(Sq, dtype=np.int64) + Sk - Sq
+    lo = np.maximum(c - wl, 0) if wl >= 0 else np.zeros(Sq, np.int64)
+    hi = np.minimum(c + wr, Sk - 1) if wr >= 0 else np.full(Sq, Sk - 1, np.int64)
+    return int(np.maximum(hi - lo + 1, 0).sum())
+
+
+def workload_flops(w):
+    """Forward flops of a workload: the convention (4 B H Sq Sk D, halved when
+    causal) and the exact count over the live pairs (4 D per pair)."""
+    conv = 4.0 * w["B"] * w["H"] * w["Sq"] * w["Sk"] * w["D"] / (2 if w["causal"] else 1)
+    exact = 4.0 * w["B"] * w["H"] * w["D"] * live_pairs(w["Sq"], w["Sk"], w["causal"], w["window"])
+    return conv, exact
 
 
 def decode_bytes(Sk):
@@ -229,7 +272,10 @@ def oracle_sample(budget_s=12.0, points=None):
 def bench_config(ws):
     """The workload both arms report on."""
     return {"workload": "training-shaped sweep: hidden 2048 as D64/H32 and D128/H16, S 512..16k, "
-                        "B=16384/S, causal off+on, fwd+bwd; plus split-KV decode B16 H32 D128 Sk 4k/32k/128k",
+                        "B=16384/S, causal off+on, fwd+bwd; plus split-KV decode B16 H32 D128 Sk 4k/32k/128k; "
+                        "plus the mask variants (B2 H16 D128: causal 2048x8192, window (4096,0) at 16k, causal+ALiBi "
+                        "at 4k; fwd+bwd) and the long head dim (B1 H8 D256 16k, forward, causal off+on), reported "
+                        "beside the headline",
             "global_batch_tokens": TOKENS * ws, "parallelism": f"replicas x{ws}",
             "l2": "inputs larger than L2 (each sweep pass reads >= 320 MiB; decode caches >= 1 GiB)"}
 
@@ -310,7 +356,38 @@ def run_ours(args):
         d["n"] = fa.fa_decode_num_splits(B, 1, Sk, H, D)
         d["ws"] = torch.empty(fa.fa_decode_workspace_size(B, 1, Sk, H, D, d["n"]), dtype=torch.uint8, device=dev)
         dec.append(d)
+    wls = []
+    for n, w in enumerate(WORKLOADS):
+        B, Sq, Sk, H, D = w["B"], w["Sq"], w["Sk"], w["H"], w["D"]
+        seed = 7000 + 11 * n + 1000003 * rank
+        t = {"q": device_normal_bf16((B, Sq, H, D), seed, dev), "k": device_normal_bf16((B, Sk, H, D), seed + 1, dev),
+             "v": device_normal_bf16((B, Sk, H, D), seed + 2, dev)}
+        t["out"] = torch.empty_like(t["q"])
+        t["lse"] = torch.empty((B, H, Sq), dtype=torch.float32, device=dev)
+        t["alibi"] = (torch.exp2(-8.0 * torch.arange(1, H + 1, dtype=torch.float32) / H).to(dev)
+                      if w["alibi"] else None)
+        if w["bwd"]:
+            t["do"] = device_normal_bf16((B, Sq, H, D), seed + 3, dev)
+            t["dq"] = torch.empty_like(t["q"])
+            t["dk"] = torch.empty_like(t["k"])
+            t["dv"] = torch.empty_like(t["v"])
+            t["ws"] = torch.empty(fa.fa_bwd_workspace_size(B, Sq, Sk, H, D, False), dtype=torch.uint8, device=dev)
+        wls.append(t)
     torch.cuda.synchronize()
+    n_ev = len(pts) + len(dec) + len(WORKLOADS)
+
+    def run_workload(w, t, e=None):
+        kw = dict(causal=w["causal"], window_size=w["window"], alibi_slopes=t["alibi"], stream=stream)
+        if e is not None:
+            e[0].record(stream)
+        fa.fa_fwd(t["q"], t["k"], t["v"], out=t["out"], lse=t["lse"], **kw)
+        if e is not None:
+            e[1].record(stream)
+        if w["bwd"]:
+            fa.fa_bwd(t["do"], t["q"], t["k"], t["v"], t["out"], t["lse"], dq=t["dq"], dk=t["dk"], dv=t["dv"],
+                      workspace=t["ws"], **kw)
+        if e is not None:
+            e[2].record(stream)
 
     def step(ev=None):
         for i, (pt, t) in enumerate(zip(pts, bufs)):
@@ -330,6 +407,8 @@ def run_ours(args):
                                  out=d["out"], lse=d["lse"], stream=stream)
             if ev is not None:
                 ev[len(pts) + m][1].record(stream)
+        for m, (w, t) in enumerate(zip(WORKLOADS, wls)):
+            run_workload(w, t, None if ev is None else ev[len(pts) + len(dec) + m])
 
     for _ in range(args.warmup):
         step()
@@ -339,7 +418,7 @@ def run_ours(args):
         raise RuntimeError(f"device status {word:#x} after warm-up")
 
     mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    evs = [[[mk(), mk(), mk()] for _ in range(len(pts) + len(dec))] for _ in range(args.steps)]
+    evs = [[[mk(), mk(), mk()] for _ in range(n_ev)] for _ in range(args.steps)]
     e_all0, e_all1 = mk(), mk()
     _barrier(ws)
     torch.cuda.synchronize()
@@ -364,6 +443,13 @@ def run_ours(args):
             t_bwd[i] += evs[s][i][1].elapsed_time(evs[s][i][2])
         for m in range(len(dec)):
             t_dec[m] += evs[s][len(pts) + m][0].elapsed_time(evs[s][len(pts) + m][1])
+    t_wf = [0.0] * len(WORKLOADS)
+    t_wb = [0.0] * len(WORKLOADS)
+    for s in range(args.steps):
+        for m in range(len(WORKLOADS)):
+            e = evs[s][len(pts) + len(dec) + m]
+            t_wf[m] += e[0].elapsed_time(e[1])
+            t_wb[m] += e[1].elapsed_time(e[2])
     K = args.steps
     f_fwd = sum(fwd_flops(p) for p in pts)
     f_all = 3.5 * f_fwd
@@ -407,6 +493,25 @@ def run_ours(args):
               "per_sk": [{"Sk": Sk, "splits": d["n"], "gbs": round(decode_bytes(Sk) * K / (t * 1e-3) / 1e9, 1)}
                          for Sk, d, t in zip(DECODE_SK, dec, t_dec)]}
 
+    peak_sus = float(peaks.get("bf16_tflops_sustained", PEAK_FALLBACK["bf16_tflops_sustained"]))
+    workloads = []
+    for w, tf, tb in zip(WORKLOADS, t_wf, t_wb):
+        conv, exact = workload_flops(w)
+        tf_ms, tb_ms = _max_over_ranks(tf, ws, dev) / K, _max_over_ranks(tb, ws, dev) / K
+        r = {"name": w["name"], "B": w["B"], "H": w["H"], "Sq": w["Sq"], "Sk": w["Sk"], "D": w["D"],
+             "causal": w["causal"], "window": list(w["window"]), "alibi": w["alibi"],
+             "fwd_flops_convention": conv, "fwd_flops_exact": exact, "fwd_ms": round(tf_ms, 4),
+             "fwd_tflops_exact": round(ws * exact / (tf_ms * 1e-3) / 1e12, 1),
+             "fwd_tflops_convention": round(ws * conv / (tf_ms * 1e-3) / 1e12, 1)}
+        r["fwd_frac_exact"] = round(r["fwd_tflops_exact"] / ws / peak_sus, 3)
+        if w["bwd"]:
+            r["bwd_ms"] = round(tb_ms, 4)
+            r["bwd_tflops_exact"] = round(ws * 2.5 * exact / (tb_ms * 1e-3) / 1e12, 1)
+            r["fwdbwd_tflops_exact"] = round(ws * 3.5 * exact / ((tf_ms + tb_ms) * 1e-3) / 1e12, 1)
+            r["fwdbwd_tflops_convention"] = round(ws * 3.5 * conv / ((tf_ms + tb_ms) * 1e-3) / 1e12, 1)
+            r["fwdbwd_frac_exact"] = round(r["fwdbwd_tflops_exact"] / ws / peak_sus, 3)
+        workloads.append(r)
+
     # ---------------------------------------------------------------- end to end (pinned host <-> device)
     e2e = None
     if not args.skip_e2e:
@@ -429,10 +534,13 @@ def run_ours(args):
             "fwdbwd_frac": value / ws / float(peaks.get("bf16_tflops_sustained", 1700.0)),
             "decode": decode,
             "sweep": sweep,
+            "workloads": workloads,
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": K * (4 * len(pts) + 2 * len(dec)),
+            # per sweep point: forward, then pre-pass, rescale, dK/dV and dQ; per
+            # decode: split and combine; per other workload: forward (+ the four)
+            "gpu_launches": K * (5 * len(pts) + 2 * len(dec) + sum(5 if w["bwd"] else 1 for w in WORKLOADS)),
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
@@ -522,6 +630,9 @@ PROFILE_CASES = {
     "fwd256": dict(op="fwd", B=1, S=8192, H=8, D=256, causal=False),
     "bwd128": dict(op="bwd", B=4, S=4096, H=16, D=128, causal=False),
     "bwd64": dict(op="bwd", B=4, S=4096, H=32, D=64, causal=False),
+    # short and long training-sweep points of the backward
+    "bwd64_512c": dict(op="bwd", B=32, S=512, H=32, D=64, causal=True),
+    "bwd64_16kc": dict(op="bwd", B=1, S=16384, H=32, D=64, causal=True),
     "decode": dict(op="decode", B=16, S=32768, H=32, D=128, causal=True),
     # decode with a 1.07 GB cache: small enough for multi-pass captures
     "decode4k": dict(op="decode", B=16, S=4096, H=32, D=128, causal=True),

@@ -112,3 +112,28 @@ def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
     with bench.ClockSampler(0) as clk:
         pass
     assert clk.summary()["samples"] == 0
+
+
+def test_live_pair_counts_match_a_brute_force_count():
+    # the exact flop counts of the mask-variant workloads rest on live_pairs()
+    sys.path.insert(0, ROOT)
+    import numpy as np
+
+    import bench
+
+    for Sq, Sk, causal, window in ((5, 2, True, (-1, -1)), (2, 5, True, (-1, -1)), (7, 7, False, (2, 1)),
+                                   (9, 4, False, (0, 0)), (6, 11, True, (3, -1)), (8, 8, False, (-1, -1))):
+        wl, wr = window
+        if causal:
+            wr = 0
+        n = 0
+        for i in range(Sq):
+            for j in range(Sk):
+                c = i + Sk - Sq
+                n += (wl < 0 or j >= c - wl) and (wr < 0 or j <= c + wr)
+        assert bench.live_pairs(Sq, Sk, causal, window) == n, (Sq, Sk, causal, window)
+    # the three mask variants' per-head counts
+    assert bench.live_pairs(2048, 8192, True, (-1, -1)) == 14681088
+    assert bench.live_pairs(16384, 16384, False, (4096, 0)) == 58734592
+    assert bench.live_pairs(4096, 4096, True, (-1, -1)) == 8390656
+    assert np.isclose(bench.workload_flops(bench.WORKLOADS[0])[1], 4 * 2 * 16 * 128 * 14681088)
