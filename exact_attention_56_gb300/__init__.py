@@ -36,6 +36,10 @@ from ._native import (  # noqa: F401
     fa_decode_num_splits,
     fa_device_status,
     fa_selftest_wait_timeout,
+    fa_debug_set_fault,
+    FA_FAULT_NONE,
+    FA_FAULT_FWD_SKIP_KEY_TILE,
+    FA_FAULT_BWD_SKIP_KEY_TILE,
     FA_SELFTEST_SITE,
 )
 
@@ -60,4 +64,8 @@ __all__ = [
     "fa_decode_num_splits",
     "fa_device_status",
     "fa_selftest_wait_timeout",
+    "fa_debug_set_fault",
+    "FA_FAULT_NONE",
+    "FA_FAULT_FWD_SKIP_KEY_TILE",
+    "FA_FAULT_BWD_SKIP_KEY_TILE",
 ]

@@ -60,6 +60,7 @@ _SIGS = {
     "fa_decode_kvcache": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _SZ,
                                _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _I, _I, _P]),
     "fa_selftest_wait_timeout": (_I, [_P]),
+    "fa_debug_set_fault": (_I, [_I, ctypes.c_uint64]),
 }
 
 
@@ -499,6 +500,17 @@ def fa_selftest_wait_timeout(stream=None):
     """Launch the diagnostic warp whose bounded wait runs out (about one second)."""
     dev = torch.device("cuda", torch.cuda.current_device())
     _check("fa_selftest_wait_timeout", library().fa_selftest_wait_timeout(_stream_ptr(stream, dev)))
+
+
+FA_FAULT_NONE = 0
+FA_FAULT_FWD_SKIP_KEY_TILE = 1
+FA_FAULT_BWD_SKIP_KEY_TILE = 2
+
+
+def fa_debug_set_fault(fault=FA_FAULT_NONE, wait_limit_ns=0):
+    """Diagnostic: set the kernels' bounded-wait limit (0 = default, one second) and a
+    fault to inject in later launches (see include/fa.h)."""
+    _check("fa_debug_set_fault", library().fa_debug_set_fault(int(fault), int(wait_limit_ns)))
 
 
 def fa_device_status(stream=None):

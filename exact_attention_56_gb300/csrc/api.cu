@@ -11,9 +11,11 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/fa.h"
+#include "fa_device.cuh"
 #include "internal.h"
 
 namespace fa {
@@ -21,6 +23,11 @@ namespace fa {
 __device__ unsigned int g_status_word;
 
 static constexpr int kMaxDevices = 64;
+
+static std::atomic<uint64_t> g_wait_ns{FA_WAIT_TIMEOUT_NS};
+static std::atomic<unsigned int> g_inject{FA_INJECT_NONE};
+
+DebugSettings debug_settings() { return DebugSettings{g_wait_ns.load(), g_inject.load()}; }
 
 unsigned int* device_status_word() {
   static unsigned int* ptrs[kMaxDevices] = {};
@@ -387,6 +394,18 @@ int fa_decode_kvcache(const void* q, void* k_cache, void* v_cache, const int* ca
   st = fa::kv_append_launch(s, k_new, v_new, k_cache, v_cache, cg, cs);
   if (st != FA_OK) return st;
   return fa::decode_launch(s, q, k_cache, v_cache, out, lse, workspace, n, &cg, cs);
+}
+
+int fa_debug_set_fault(int fault, uint64_t wait_limit_ns) {
+  if (fault < FA_FAULT_NONE || fault > FA_FAULT_BWD_SKIP_KEY_TILE) return FA_ERR_INVALID;
+  if (wait_limit_ns != 0 && (wait_limit_ns < 1000000ull || wait_limit_ns > fa::FA_WAIT_TIMEOUT_NS))
+    return FA_ERR_INVALID;
+  static_assert(FA_FAULT_FWD_SKIP_KEY_TILE == int(fa::FA_INJECT_FWD_SKIP_K) &&
+                    FA_FAULT_BWD_SKIP_KEY_TILE == int(fa::FA_INJECT_BWD_SKIP_K),
+                "fault codes");
+  fa::g_wait_ns.store(wait_limit_ns ? wait_limit_ns : fa::FA_WAIT_TIMEOUT_NS);
+  fa::g_inject.store(unsigned(fault));
+  return FA_OK;
 }
 
 int fa_device_status(fa_stream_t stream, unsigned int* detail) {

@@ -98,6 +98,8 @@ struct BwdParams {
   float scale;
   float scale_log2;
   unsigned int* status;
+  uint64_t wait_ns;     // bounded-wait limit
+  unsigned int inject;  // FA_INJECT_* (diagnostics only)
 };
 
 enum : uint32_t {
@@ -143,11 +145,11 @@ __device__ __forceinline__ void bulk_load_w(void* dst, const void* src, uint32_t
 }
 
 // Timeout-only wait used while draining after an abort.
-__device__ __forceinline__ void drain_wait_b(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ void drain_wait_b(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(a, parity)) {
-    if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) return;
+    if (globaltimer_ns() - t0 > limit_ns) return;
   }
 }
 
@@ -591,7 +593,7 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const Watch watch{&bars->abort, p.status};
+  const Watch watch{&bars->abort, p.status, p.wait_ns};
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -631,11 +633,11 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
         do_issued = ii + 1;
       }
       // every copy must land before the CTA may exit
-      drain_wait_b(&bars->kv_full, 0);
+      drain_wait_b(&bars->kv_full, 0, p.wait_ns);
       for (int ii = (q_issued > C::NQ ? q_issued - C::NQ : 0); ii < q_issued; ++ii)
-        drain_wait_b(&bars->q_full[ii % C::NQ], uint32_t(ii / C::NQ) & 1u);
+        drain_wait_b(&bars->q_full[ii % C::NQ], uint32_t(ii / C::NQ) & 1u, p.wait_ns);
       for (int ii = (do_issued > C::NDO ? do_issued - C::NDO : 0); ii < do_issued; ++ii)
-        drain_wait_b(&bars->do_full[ii % C::NDO], uint32_t(ii / C::NDO) & 1u);
+        drain_wait_b(&bars->do_full[ii % C::NDO], uint32_t(ii / C::NDO) & 1u, p.wait_ns);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -726,7 +728,7 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
         mma_commit_w(&bars->acc_done);
       } else {
         mma_commit_w(&bars->drain);
-        drain_wait_b(&bars->drain, 0);
+        drain_wait_b(&bars->drain, 0, p.wait_ns);
       }
     }
   } else if (warp == 2) {
@@ -1017,7 +1019,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const Watch watch{&bars->abort, p.status};
+  const Watch watch{&bars->abort, p.status, p.wait_ns};
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -1039,10 +1041,12 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         const int row = sq_.k_off + (jb + jj) * 128;
         const int sk = jj % C::NK, sv = jj % C::NV;
         if (!fa_wait_warp(&bars->k_empty[sk], (uint32_t(jj / C::NK) & 1u) ^ 1u, watch, SITE_DQ_EMPTY)) break;
-        mbar_arrive_expect_tx_w(&bars->k_full[sk], C::TILE_BYTES);
-        for (int pn = 0; pn < C::PANELS; ++pn)
-          tma_load_4d_w(smem + C::K_OFF + sk * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_k, &bars->k_full[sk],
-                        pn * 64, hkv, row, sq_.tb);
+        if (!(p.inject == FA_INJECT_BWD_SKIP_K && jj == 1)) {  // diagnostics: key tile 1 never arrives
+          mbar_arrive_expect_tx_w(&bars->k_full[sk], C::TILE_BYTES);
+          for (int pn = 0; pn < C::PANELS; ++pn)
+            tma_load_4d_w(smem + C::K_OFF + sk * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_k, &bars->k_full[sk],
+                          pn * 64, hkv, row, sq_.tb);
+        }
         k_issued = jj + 1;
         if (!fa_wait_warp(&bars->v_empty[sv], (uint32_t(jj / C::NV) & 1u) ^ 1u, watch, SITE_DQ_EMPTY)) break;
         mbar_arrive_expect_tx_w(&bars->v_full[sv], C::TILE_BYTES);
@@ -1051,11 +1055,11 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
                         pn * 64, hkv, row, sq_.tb);
         v_issued = jj + 1;
       }
-      drain_wait_b(&bars->q_full, 0);
+      drain_wait_b(&bars->q_full, 0, p.wait_ns);
       for (int jj = (k_issued > C::NK ? k_issued - C::NK : 0); jj < k_issued; ++jj)
-        drain_wait_b(&bars->k_full[jj % C::NK], uint32_t(jj / C::NK) & 1u);
+        drain_wait_b(&bars->k_full[jj % C::NK], uint32_t(jj / C::NK) & 1u, p.wait_ns);
       for (int jj = (v_issued > C::NV ? v_issued - C::NV : 0); jj < v_issued; ++jj)
-        drain_wait_b(&bars->v_full[jj % C::NV], uint32_t(jj / C::NV) & 1u);
+        drain_wait_b(&bars->v_full[jj % C::NV], uint32_t(jj / C::NV) & 1u, p.wait_ns);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -1125,7 +1129,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         mma_commit_w(&bars->acc_done);
       } else {
         mma_commit_w(&bars->drain);
-        drain_wait_b(&bars->drain, 0);
+        drain_wait_b(&bars->drain, 0, p.wait_ns);
       }
     }
   } else if (warp == 2) {
@@ -1344,6 +1348,11 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
   p.scale = s.scale;
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.status = device_status_word();
+  {
+    const DebugSettings dbg = debug_settings();
+    p.wait_ns = dbg.wait_ns;
+    p.inject = dbg.inject;
+  }
   if (!p.status) return FA_ERR_CUDA;
   if (s.B > 65535 || s.H > 65535) return FA_ERR_UNSUPPORTED;
   // Packed sequences are one (1, total, H, D) tensor.

@@ -82,6 +82,7 @@ struct DecParams {
   int wl, wr;
   float scale_log2;
   unsigned int* status;
+  uint64_t wait_ns;  // bounded-wait limit
 };
 
 struct DecBars {
@@ -164,7 +165,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS)
     fence_barrier_init();
   }
   __syncthreads();
-  const Watch watch{&bars->abort, p.status};
+  const Watch watch{&bars->abort, p.status, p.wait_ns};
 
   if (threadIdx.x >= 128) {
     // ------------------------------------------------------------ producer
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS)
           const uint32_t a = smem_u32(&bars->full[t % C::NSTAGE]);
           const uint64_t t0 = globaltimer_ns();
           while (!mbar_try_wait(a, uint32_t(t / C::NSTAGE) & 1u))
-            if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) break;
+            if (globaltimer_ns() - t0 > p.wait_ns) break;
         }
       }
     }
@@ -400,11 +401,11 @@ enum : uint32_t {
 };
 
 // Timeout-only wait used while draining after an abort.
-__device__ __forceinline__ void dm_drain_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ void dm_drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(a, parity)) {
-    if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) return;
+    if (globaltimer_ns() - t0 > limit_ns) return;
   }
 }
 
@@ -473,7 +474,7 @@ __global__ void __launch_bounds__(DecMmaCfg<D, ROT>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const Watch watch{&bars->abort, p.status};
+  const Watch watch{&bars->abort, p.status, p.wait_ns};
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -516,9 +517,9 @@ __global__ void __launch_bounds__(DecMmaCfg<D, ROT>::THREADS, 1)
         }
       }
       if (!ok) {  // let the copies in flight land before the CTA leaves
-        dm_drain_wait(&bars->q_full, 0);
+        dm_drain_wait(&bars->q_full, 0, p.wait_ns);
         for (int it = (issued > C::NSLOT ? issued - C::NSLOT : 0); it < issued; ++it)
-          dm_drain_wait(&bars->kv_full[it % C::NSLOT], uint32_t(it / C::NSLOT) & 1u);
+          dm_drain_wait(&bars->kv_full[it % C::NSLOT], uint32_t(it / C::NSLOT) & 1u, p.wait_ns);
       }
     }
   } else if (warp == 1) {
@@ -597,7 +598,7 @@ __global__ void __launch_bounds__(DecMmaCfg<D, ROT>::THREADS, 1)
       }
       if (!ok) {  // let issued MMAs finish before TMEM is released
         mma_commit_w(&bars->drain);
-        dm_drain_wait(&bars->drain, 0);
+        dm_drain_wait(&bars->drain, 0, p.wait_ns);
       }
     }
   } else if (warp >= 4) {
@@ -1091,6 +1092,7 @@ static int launch_decode_t(const AttnShape& s, const void* q, const void* k, con
   p.wr = s.wr;
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.status = device_status_word();
+  p.wait_ns = debug_settings().wait_ns;
   if (!p.status) return FA_ERR_CUDA;
   if (mma) {
     using M = DecMmaCfg<D>;

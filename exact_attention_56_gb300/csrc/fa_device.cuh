@@ -12,6 +12,11 @@ constexpr unsigned int FA_DEV_SITE_MASK = 0x0000FFFFu;
 // A legitimate wait inside these kernels lasts microseconds; one second
 // means a lost arrival, after which the kernel leaves instead of hanging.
 constexpr uint64_t FA_WAIT_TIMEOUT_NS = 1000000000ull;
+// Diagnostic fault injection (fa_debug_set_fault), passed to the kernels with
+// the wait limit: the forward's producer, or the dQ kernel's, leaves out the
+// copy of key tile 1, so the wait for it expires and the kernel takes its
+// abort path. Off (0) in every normal call.
+constexpr unsigned int FA_INJECT_NONE = 0, FA_INJECT_FWD_SKIP_K = 1, FA_INJECT_BWD_SKIP_K = 2;
 // Longest single sleep of a waiting thread before it re-checks the abort flag
 // and the watchdog; the thread wakes earlier when the awaited phase completes.
 constexpr uint32_t FA_WAIT_SLEEP_NS = 2000u;

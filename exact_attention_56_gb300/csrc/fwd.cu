@@ -52,6 +52,8 @@ struct FwdParams {
   int wl, wr;
   float scale_log2;  // softmax scale * log2(e)
   unsigned int* status;
+  uint64_t wait_ns;      // bounded-wait limit
+  unsigned int inject;   // FA_INJECT_* (diagnostics only)
 };
 
 template <int D, int NT>
@@ -102,11 +104,11 @@ enum : uint32_t {
 };
 
 // Timeout-only wait used while draining after an abort.
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(a, parity)) {
-    if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) return;
+    if (globaltimer_ns() - t0 > limit_ns) return;
   }
 }
 
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const Watch watch{&bars->abort, p.status};
+  const Watch watch{&bars->abort, p.status, p.wait_ns};
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -217,6 +219,10 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
             ok = false;
             break;
           }
+          if (p.inject == FA_INJECT_FWD_SKIP_K && it == 2) {  // diagnostics: key tile 1 never arrives
+            issued = it + 1;
+            continue;
+          }
           mbar_arrive_expect_tx_w(&bars->kv_full[s], C::TILE_BYTES);
           const CUtensorMap* m = kv ? &tm_v : &tm_k;
           for (int pn = 0; pn < C::PANELS; ++pn)
@@ -225,11 +231,11 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
           issued = it + 1;
         }
       }
-      if (!ok) {  // let the copies in flight land before the CTA leaves
-        drain_wait(&bars->q_full, 0);
-        for (int it = (issued > C::NSLOT ? issued - C::NSLOT : 0); it < issued; ++it)
-          drain_wait(&bars->kv_full[it % C::NSLOT], uint32_t(it / C::NSLOT) & 1u);
-      }
+      // every copy must land before the CTA may leave (those of an aborted run
+      // included; on a normal run the consumers have waited for them already)
+      drain_wait(&bars->q_full, 0, p.wait_ns);
+      for (int it = (issued > C::NSLOT ? issued - C::NSLOT : 0); it < issued; ++it)
+        drain_wait(&bars->kv_full[it % C::NSLOT], uint32_t(it / C::NSLOT) & 1u, p.wait_ns);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -381,7 +387,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
       }
       if (!ok) {  // let issued MMAs finish before TMEM is released
         mma_commit_w(&bars->drain);
-        drain_wait(&bars->drain, 0);
+        drain_wait(&bars->drain, 0, p.wait_ns);
       }
     }
   } else if (warp >= 4) {
@@ -602,6 +608,11 @@ static int launch_fwd_t(const AttnShape& s, const CUtensorMap& mq, const CUtenso
   p.wr = s.wr;
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.status = device_status_word();
+  {
+    const DebugSettings dbg = debug_settings();
+    p.wait_ns = dbg.wait_ns;
+    p.inject = dbg.inject;
+  }
   if (!p.status) return FA_ERR_CUDA;
   dim3 grid((s.Sq + NT * 128 - 1) / (NT * 128), s.H, s.B);
   kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);

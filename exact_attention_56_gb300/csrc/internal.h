@@ -50,6 +50,15 @@ struct CacheArgs {
 int check_common(int B, int Sq, int Sk, int H, int Hk, int D, float scale, int causal, int wl, int wr,
                  const float* alibi, int alibi_bstride, AttnShape* s);
 
+// Diagnostic settings the launchers pass to the kernels: the bounded-wait
+// limit (FA_WAIT_TIMEOUT_NS) and a fault to inject (FA_INJECT_NONE), both
+// process-wide and changed only by fa_debug_set_fault().
+struct DebugSettings {
+  uint64_t wait_ns;
+  unsigned int inject;
+};
+DebugSettings debug_settings();
+
 // Status word of the current device (device pointer), or NULL on failure.
 unsigned int* device_status_word();
 

@@ -3,7 +3,7 @@
 //
 // Everything here is a thin wrapper over one documented PTX instruction
 // (PTX ISA: mbarrier, cp.async.bulk.tensor, tcgen05.*). No waits are
-// unbounded: fa_wait() gives up after FA_WAIT_TIMEOUT_NS, records where in
+// unbounded: fa_wait() gives up after its limit (FA_WAIT_TIMEOUT_NS), records where in
 // the device status word, and raises a CTA-wide abort flag so the other
 // roles of the CTA leave their loops too.
 #pragma once
@@ -82,15 +82,17 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar_addr, uint32_t 
   return ok != 0;
 }
 
-// Per-CTA watchdog state: a shared abort flag plus the global status word.
+// Per-CTA watchdog state: a shared abort flag, the global status word and the
+// wait limit (FA_WAIT_TIMEOUT_NS unless a diagnostic run shortened it).
 struct Watch {
   volatile int* abort;   // shared memory, 0 = running
   unsigned int* status;  // device status word (global), see fa_device.cuh
+  uint64_t limit_ns;     // a wait gives up after this long
 };
 
 // Waits until the phase with the given parity has completed. Returns false
 // (and raises the abort flag) if the CTA is aborting or the wait ran past
-// FA_WAIT_TIMEOUT_NS; `where` names the wait site in the status word.
+// w.limit_ns; `where` names the wait site in the status word.
 __device__ __forceinline__ bool fa_wait(uint64_t* bar, uint32_t parity, const Watch& w, uint32_t where) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
@@ -101,7 +103,7 @@ __device__ __forceinline__ bool fa_wait(uint64_t* bar, uint32_t parity, const Wa
     // warps sharing it (the MMA issuer shares one with compute warps).
     if (mbar_try_wait_sleep(a, parity, FA_WAIT_SLEEP_NS)) return true;
     if (*w.abort) return false;
-    if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) {
+    if (globaltimer_ns() - t0 > w.limit_ns) {
       *w.abort = 1;
       atomicOr(w.status, FA_DEV_TIMEOUT | (where & FA_DEV_SITE_MASK));
       return false;

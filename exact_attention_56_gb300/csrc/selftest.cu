@@ -22,7 +22,7 @@ __global__ void __launch_bounds__(32) fa_selftest_wait_kernel(unsigned int* stat
     fence_barrier_init();
   }
   __syncwarp();
-  const Watch w{&abort_flag, status};
+  const Watch w{&abort_flag, status, FA_WAIT_TIMEOUT_NS};
   (void)fa_wait_warp(&bar, 0, w, FA_SELFTEST_SITE);
 }
 

@@ -316,6 +316,29 @@ int fa_device_status(fa_stream_t stream, unsigned int* detail);
  */
 int fa_selftest_wait_timeout(fa_stream_t stream);
 
+/* Faults fa_debug_set_fault() can inject. */
+#define FA_FAULT_NONE 0
+#define FA_FAULT_FWD_SKIP_KEY_TILE 1 /* fa_fwd's producer never loads key tile 1 */
+#define FA_FAULT_BWD_SKIP_KEY_TILE 2 /* fa_bwd's dQ kernel never loads key tile 1 */
+
+/*
+ * Diagnostic, outside the method: exercises the attention kernels' own
+ * failure path on a real GPU without faulting it. Sets, for every later
+ * launch in this process (all devices), the limit of the kernels' bounded
+ * waits (wait_limit_ns; 0 restores the default of one second; otherwise
+ * 1 ms .. 1 s) and a fault to inject. With FA_FAULT_FWD_SKIP_KEY_TILE the
+ * forward's copy of key tile 1 is left out, so a CTA with at least two key
+ * tiles waits for it until the limit, raises its abort flag, lets its copies
+ * and tensor-core work in flight finish, frees its tensor memory and returns;
+ * fa_device_status() then reports FA_ERR_TIMEOUT with a forward wait site
+ * (0x10..0x1F in the low byte of the detail word). FA_FAULT_BWD_SKIP_KEY_TILE
+ * does the same in fa_bwd's dQ kernel (sites 0x40..0x4F). The outputs of such
+ * a call are undefined. FA_FAULT_NONE with 0 restores normal operation.
+ * Returns FA_OK, or FA_ERR_INVALID for an unknown fault or a limit outside
+ * that range. Not for use concurrently with normal calls.
+ */
+int fa_debug_set_fault(int fault, uint64_t wait_limit_ns);
+
 #ifdef __cplusplus
 }
 #endif

@@ -73,3 +73,47 @@ def assert_bf16_close_scaled(got, ref, f, what=""):
     rr = float(np.linalg.norm(got - ref) / nref)
     assert err <= ATOL_BF16, f"{what}: max |err| / {f:g} = {err:.3e} > {ATOL_BF16}"
     assert rr <= RELRMS_BF16, f"{what}: rel RMS {rr:.3e} > {RELRMS_BF16}"
+
+
+# Guard bands: an output (or workspace) is a view into a larger buffer whose
+# bytes before and after it hold a canary pattern (a NaN bit pattern, also
+# written into the view itself). After the call the bands must be bit-identical
+# (no write outside the tensor) and, for outputs, every element must have been
+# overwritten (no NaN pattern left). 4096 bytes of band keep every view's start
+# 256-byte aligned, as the library asks of workspaces.
+GUARD_BYTES = 4096
+_CANARY = {2: 0x7FA5, 4: 0x7FA5A5A5, 1: 0xA5}
+
+
+class Guarded:
+    def __init__(self, shape, dtype, device="cuda"):
+        import torch
+
+        self.shape = tuple(shape)
+        n = int(np.prod(self.shape)) if self.shape else 1
+        esz = torch.empty((), dtype=dtype).element_size()
+        self.pad = GUARD_BYTES // esz
+        self.n = n
+        self.buf = torch.empty(n + 2 * self.pad, dtype=dtype, device=device)
+        ity = {1: torch.uint8, 2: torch.int16, 4: torch.int32}[esz]
+        self.bits = self.buf.view(ity)
+        pat = _CANARY[esz]
+        if esz == 2 and pat > 0x7FFF:
+            pat -= 1 << 16
+        if esz == 4 and pat > 0x7FFFFFFF:
+            pat -= 1 << 32
+        self.pattern = pat
+        self.bits.fill_(pat)
+        self.view = self.buf[self.pad:self.pad + n].view(self.shape)
+
+    def check(self, what, written=True):
+        import torch
+
+        lo, hi = self.bits[:self.pad], self.bits[self.pad + self.n:]
+        assert bool((lo == self.pattern).all()), f"{what}: bytes before the tensor were overwritten"
+        assert bool((hi == self.pattern).all()), f"{what}: bytes after the tensor were overwritten"
+        if written:
+            mid = self.bits[self.pad:self.pad + self.n]
+            left = int((mid == self.pattern).sum())
+            assert left == 0, f"{what}: {left} elements were never written"
+        torch.cuda.synchronize()
