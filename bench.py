@@ -628,6 +628,9 @@ PROFILE_CASES = {
     "fwd64": dict(op="fwd", B=4, S=4096, H=32, D=64, causal=False),
     "fwd128c": dict(op="fwd", B=4, S=4096, H=16, D=128, causal=True),
     "fwd256": dict(op="fwd", B=1, S=8192, H=8, D=256, causal=False),
+    # the causal + ALiBi mask variant's shape (geometric slopes)
+    "fwd128a": dict(op="fwd", B=2, S=4096, H=16, D=128, causal=True, alibi=True),
+    "bwd128c": dict(op="bwd", B=4, S=4096, H=16, D=128, causal=True),
     "bwd128": dict(op="bwd", B=4, S=4096, H=16, D=128, causal=False),
     "bwd64": dict(op="bwd", B=4, S=4096, H=32, D=64, causal=False),
     # short and long training-sweep points of the backward
@@ -664,12 +667,15 @@ def run_profile(name):
         run = lambda: fa.fa_decode_splitkv(q, k, v, causal=True, num_splits=n, workspace=ws)  # noqa: E731
     else:
         q, k, v, do = (device_normal_bf16((B, S, H, D), i, dev) for i in range(4))
-        out, lse = fa.fa_fwd(q, k, v, causal=c["causal"])
+        al = (torch.exp2(-8.0 * torch.arange(1, H + 1, dtype=torch.float32) / H).to(dev)
+              if c.get("alibi") else None)
+        out, lse = fa.fa_fwd(q, k, v, causal=c["causal"], alibi_slopes=al)
         if c["op"] == "fwd":
-            run = lambda: fa.fa_fwd(q, k, v, causal=c["causal"], out=out, lse=lse)  # noqa: E731
+            run = lambda: fa.fa_fwd(q, k, v, causal=c["causal"], alibi_slopes=al, out=out, lse=lse)  # noqa: E731
         else:
             ws = torch.empty(fa.fa_bwd_workspace_size(B, S, S, H, D), dtype=torch.uint8, device=dev)
-            run = lambda: fa.fa_bwd(do, q, k, v, out, lse, causal=c["causal"], workspace=ws)  # noqa: E731
+            run = lambda: fa.fa_bwd(do, q, k, v, out, lse, causal=c["causal"], alibi_slopes=al,  # noqa: E731
+                                    workspace=ws)
     for _ in range(3):
         run()
     torch.cuda.synchronize()
