@@ -61,11 +61,17 @@ struct FwdCfg {
   static constexpr int PANELS = D / 64;
   static constexpr int PANEL_BYTES = 128 * 128;  // 128 rows x 128 B
   static constexpr int TILE_BYTES = PANELS * PANEL_BYTES;
-  static constexpr int NSLOT = D == 64 ? 8 : (D == 128 ? 4 : 2);
+  // K/V ring. At D = 256 the query tile takes 64 KB, so the ring holds half
+  // tiles (two 64-column panels, 32 KB): five of them. A whole-tile ring
+  // (two 64 KB slots) made each K and V load wait for the previous tile's
+  // MMAs and left its latency on the critical path.
+  static constexpr bool HALVES = D == 256;
+  static constexpr int SLOT_BYTES = HALVES ? 2 * PANEL_BYTES : TILE_BYTES;
+  static constexpr int NSLOT = D == 64 ? 8 : (D == 128 ? 4 : 5);
   static constexpr int THREADS = 128 * (1 + NT);
   static constexpr int Q_OFF = 0;
   static constexpr int KV_OFF = NT * TILE_BYTES;
-  static constexpr int BAR_OFF = KV_OFF + NSLOT * TILE_BYTES;
+  static constexpr int BAR_OFF = KV_OFF + NSLOT * SLOT_BYTES;
   static constexpr int SMEM_BYTES = BAR_OFF + 512 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   // S buffers (128 columns each): two, or three where the TMEM budget allows
@@ -102,6 +108,11 @@ enum : uint32_t {
   SITE_SM_PV = 0x17,
   SITE_SM_EPI = 0x18,
 };
+
+// Stream positions of the half tiles at D = 256 (the producer's order:
+// K0lo K0hi | K1lo K1hi V0lo V0hi | ... | V(n-1)lo V(n-1)hi); hi follows lo.
+__device__ __forceinline__ int fwd_pos_k(int j) { return j == 0 ? 0 : 4 * j - 2; }
+__device__ __forceinline__ int fwd_pos_v(int j, int n_blocks) { return 4 * j + (j + 1 < n_blocks ? 4 : 2); }
 
 // Timeout-only wait used while draining after an abort.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
@@ -210,25 +221,52 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
                       h, q_off + row0 + t * 128, tb);
       int issued = 0;
       bool ok = true;
-      for (int jj = 0; jj < n_blocks && ok; ++jj) {
-        for (int kv = 0; kv < 2; ++kv) {
-          const int it = 2 * jj + kv;
-          const int s = it % C::NSLOT;
-          const uint32_t ph = uint32_t(it / C::NSLOT) & 1u;
-          if (!fa_wait_warp(&bars->kv_empty[s], ph ^ 1u, watch, SITE_PROD_EMPTY)) {
-            ok = false;
-            break;
+      if constexpr (C::HALVES) {
+        // Half tiles in the order the MMAs consume them, K one key tile ahead of
+        // V: K0lo K0hi | K1lo K1hi V0lo V0hi | ... | V(n-1)lo V(n-1)hi (stream
+        // positions fwd_pos_k / fwd_pos_v); lo holds head dims 0-127, hi 128-255.
+        for (int bb = 0; bb <= n_blocks && ok; ++bb) {
+          for (int e = 0; e < 4; ++e) {
+            const bool isk = e < 2;
+            if (isk ? bb >= n_blocks : bb == 0) continue;
+            const int j = isk ? bb : bb - 1;
+            const int half = e & 1;
+            const int s = issued % C::NSLOT;
+            const uint32_t ph = uint32_t(issued / C::NSLOT) & 1u;
+            if (!fa_wait_warp(&bars->kv_empty[s], ph ^ 1u, watch, SITE_PROD_EMPTY)) {
+              ok = false;
+              break;
+            }
+            if (!(p.inject == FA_INJECT_FWD_SKIP_K && isk && j == 1)) {  // diagnostics: key tile 1 never arrives
+              mbar_arrive_expect_tx_w(&bars->kv_full[s], C::SLOT_BYTES);
+              for (int pl = 0; pl < 2; ++pl)
+                tma_load_4d_w(smem + C::KV_OFF + s * C::SLOT_BYTES + pl * C::PANEL_BYTES, isk ? &tm_k : &tm_v,
+                              &bars->kv_full[s], (2 * half + pl) * 64, hkv, k_off + key_tile(j) * 128, tb);
+            }
+            ++issued;
           }
-          if (p.inject == FA_INJECT_FWD_SKIP_K && it == 2) {  // diagnostics: key tile 1 never arrives
+        }
+      } else {
+        for (int jj = 0; jj < n_blocks && ok; ++jj) {
+          for (int kv = 0; kv < 2; ++kv) {
+            const int it = 2 * jj + kv;
+            const int s = it % C::NSLOT;
+            const uint32_t ph = uint32_t(it / C::NSLOT) & 1u;
+            if (!fa_wait_warp(&bars->kv_empty[s], ph ^ 1u, watch, SITE_PROD_EMPTY)) {
+              ok = false;
+              break;
+            }
+            if (p.inject == FA_INJECT_FWD_SKIP_K && it == 2) {  // diagnostics: key tile 1 never arrives
+              issued = it + 1;
+              continue;
+            }
+            mbar_arrive_expect_tx_w(&bars->kv_full[s], C::TILE_BYTES);
+            const CUtensorMap* m = kv ? &tm_v : &tm_k;
+            for (int pn = 0; pn < C::PANELS; ++pn)
+              tma_load_4d_w(smem + C::KV_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, m, &bars->kv_full[s],
+                            pn * 64, hkv, k_off + key_tile(jj) * 128, tb);
             issued = it + 1;
-            continue;
           }
-          mbar_arrive_expect_tx_w(&bars->kv_full[s], C::TILE_BYTES);
-          const CUtensorMap* m = kv ? &tm_v : &tm_k;
-          for (int pn = 0; pn < C::PANELS; ++pn)
-            tma_load_4d_w(smem + C::KV_OFF + s * C::TILE_BYTES + pn * C::PANEL_BYTES, m, &bars->kv_full[s],
-                        pn * 64, hkv, k_off + key_tile(jj) * 128, tb);
-          issued = it + 1;
         }
       }
       // every copy must land before the CTA may leave (those of an aborted run
@@ -357,6 +395,60 @@ __global__ void __launch_bounds__(FwdCfg<D, NT>::THREADS, 1)
             last_pv(jj, 1);
             mma_commit_w(&bars->kv_empty[slot_of(2 * jj + 1)]);
           }
+        }
+      } else if constexpr (C::HALVES) {
+        // One query tile, half-tile K/V ring (D = 256). Same order as below:
+        // S(jj+1) into the other S buffer, then PV(jj). S takes K in two halves
+        // of eight k-steps; PV writes O in two N = 128 halves, each reading its
+        // V half. Each half's ring slot is released as soon as its MMAs finish.
+        constexpr uint32_t IDESC_O_HALF = idesc_bf16_f32(128, 128, 0, 1);
+        auto wait_half = [&](int pos, uint32_t site) {
+          return fa_wait_warp(&bars->kv_full[pos % C::NSLOT], uint32_t(pos / C::NSLOT) & 1u, watch, site);
+        };
+        auto s_halves = [&](int jj, int sbuf) {  // S(jj) = Q K^T into buffer sbuf
+          const uint32_t ts = tmem + uint32_t(sbuf) * 128;
+          const int pos = fwd_pos_k(jj);
+          for (int hh = 0; hh < 2; ++hh) {
+            if (!wait_half(pos + hh, SITE_MMA_K)) return false;
+            tc_fence_after();
+            const uint64_t kd = sdesc_adv(kv_kdesc, uint32_t((pos + hh) % C::NSLOT) * C::SLOT_BYTES);
+#pragma unroll
+            for (int k8 = 0; k8 < 8; ++k8) {
+              const int kk = 8 * hh + k8;
+              const uint32_t qoff = (kk / 4) * C::PANEL_BYTES + (kk % 4) * 32;
+              const uint32_t koff = (k8 / 4) * C::PANEL_BYTES + (k8 % 4) * 32;
+              mma_ss_w(ts, sdesc_adv(q_desc, qoff), sdesc_adv(kd, koff), IDESC_S, kk > 0 ? 1u : 0u);
+            }
+            mma_commit_w(&bars->kv_empty[(pos + hh) % C::NSLOT]);
+          }
+          mma_commit_w(&bars->s_full[sbuf]);
+          return true;
+        };
+        auto pv_halves = [&](int jj, int sbuf) {  // O += P V, P in buffer sbuf
+          const uint32_t tp = tmem + uint32_t(sbuf) * 128;
+          const int pos = fwd_pos_v(jj, n_blocks);
+          for (int hh = 0; hh < 2; ++hh) {
+            if (!wait_half(pos + hh, SITE_MMA_V)) return false;
+            tc_fence_after();
+            const uint64_t vd = sdesc_adv(kv_mdesc, uint32_t((pos + hh) % C::NSLOT) * C::SLOT_BYTES);
+            const uint32_t to = tmem + C::O_COL0 + uint32_t(hh) * 128;
+            const uint32_t acc0 = jj > 0 ? 1u : 0u;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts_w(to, tp + kk * 8, sdesc_adv(vd, kk * 2048), IDESC_O_HALF, kk > 0 ? 1u : acc0);
+            mma_commit_w(&bars->kv_empty[(pos + hh) % C::NSLOT]);
+          }
+          mma_commit_w(&bars->pv_done[0]);
+          last_pv(jj, 0);
+          return true;
+        };
+        ok = ok && s_halves(0, 0);
+        for (int jj = 0; jj < n_blocks && ok; ++jj) {
+          if (jj + 1 < n_blocks && !(ok = s_halves(jj + 1, (jj + 1) & 1))) break;
+          // P barriers per S buffer, as below
+          if (!(ok = fa_wait_warp(&bars->p_full[jj & 1], uint32_t(jj >> 1) & 1u, watch, SITE_MMA_P))) break;
+          tc_fence_after();
+          if (!(ok = pv_halves(jj, jj & 1))) break;
         }
       } else {
         if (ok && (ok = wait_full(0, SITE_MMA_K))) {
