@@ -315,7 +315,8 @@ __device__ __forceinline__ uint32_t row_absmax(uint32_t m) {
 //   padding:    D = 0 and L2 = +inf on the vector rows of each (b, h) past its
 //               sequence, up to the whole 128-row tiles of Sq_pad;
 //   range:      each row's largest |q|, |dO| (|k|, |v|) into one replica of its
-//               group's maxima (amax_rep, zeroed before), one atomic per row.
+//               group's maxima (amax_rep, zeroed before), through a running
+//               maximum per thread that is sent when the thread changes group.
 // The three item ranges start on multiples of 32, so each warp works inside one
 // of them and the D/8 lanes of a row are consecutive lanes of one warp. The
 // grid strides over the items, so the blocks sweep memory together. The copies
@@ -334,6 +335,32 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
   const long long total = p0 + n_pad;
   const int lane = int(threadIdx.x & 31);
   const long long stride = (long long)gridDim.x * blockDim.x;
+  // A row-leader thread's running maxima (m0, m1) of group cur (index * 2 +
+  // side: 0 query rows (q, dO), 1 key rows (k, v)), kept in shared memory; they
+  // go to the group's replica only when the thread moves to another group. With
+  // long sequences the grid's stride keeps a thread on one group for many rows.
+  __shared__ long long run_gid[256];
+  __shared__ uint32_t run_max[256][2];
+  run_gid[threadIdx.x] = -1;
+  auto flush = [&]() {
+    const long long cur = run_gid[threadIdx.x];
+    if (cur < 0) return;
+    uint32_t* g = p.amax_rep + ((size_t)(cur >> 1) * AMAX_REPS + blockIdx.x % AMAX_REPS) * 4;
+    const bool key = cur & 1;
+    if (run_max[threadIdx.x][0]) atomicMax(g + (key ? 1 : 0), run_max[threadIdx.x][0]);
+    if (run_max[threadIdx.x][1]) atomicMax(g + (key ? 2 : 3), run_max[threadIdx.x][1]);
+  };
+  auto track = [&](long long gid, uint32_t m0, uint32_t m1) {
+    if (run_gid[threadIdx.x] != gid) {
+      flush();
+      run_gid[threadIdx.x] = gid;
+      run_max[threadIdx.x][0] = m0;
+      run_max[threadIdx.x][1] = m1;
+    } else {
+      run_max[threadIdx.x][0] = max(run_max[threadIdx.x][0], m0);
+      run_max[threadIdx.x][1] = max(run_max[threadIdx.x][1], m1);
+    }
+  };
   for (long long wb = ((long long)blockIdx.x * blockDim.x + threadIdx.x) - lane; wb < total; wb += stride) {
     const long long i = wb + lane;
     if (wb < k0) {
@@ -374,9 +401,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
         p.dvec[vi] = acc;
         const float L = p.lse[li];
         p.l2[vi] = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
-        uint32_t* g = p.amax_rep + (((size_t)b * p.Hk + h / p.group) * AMAX_REPS + blockIdx.x % AMAX_REPS) * 4;
-        if (mq) atomicMax(g + 0, mq);
-        if (mdo) atomicMax(g + 3, mdo);
+        track(((long long)b * p.Hk + h / p.group) * 2, mq, mdo);
       }
     } else if (wb < p0) {
       const long long t = i - k0;
@@ -397,9 +422,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
         const long long row = t / CPR;  // token * Hk + hk
         const long long tok = row / p.Hk;
         const int b = p.cu_q ? seq_of(p.cu_k, p.B, tok, 0) : int(tok / p.Sk);
-        uint32_t* g = p.amax_rep + (((size_t)b * p.Hk + int(row - tok * p.Hk)) * AMAX_REPS + blockIdx.x % AMAX_REPS) * 4;
-        if (mk) atomicMax(g + 1, mk);
-        if (mv) atomicMax(g + 2, mv);
+        track(((long long)b * p.Hk + (row - tok * p.Hk)) * 2 + 1, mk, mv);
       }
     } else {
       const long long t = i - p0;
@@ -414,6 +437,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
       }
     }
   }
+  flush();
 }
 
 // Folds each group's replicas into its maxima (amax, block x = 0 writes them)
@@ -1373,7 +1397,17 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
     const long long n_q = (rows_q * s.H * cpr + 31) & ~31LL;
     const long long n_k = (rows_k * s.Hk * cpr + 31) & ~31LL;
     const long long total = n_q + n_k + (long long)s.B * s.H * p.Sq_pad;
-    const long long cap = (long long)device_sm_count() * 8;  // 8 blocks of 256 threads per SM
+    // as many blocks as fit on the GPU at once: the grid strides over the items
+    static int per_sm[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FA_ERR_CUDA;
+    if (per_sm[dev] == 0) {
+      int n = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fa_bwd_pre_kernel<D>, 256, 0) != cudaSuccess || n < 1)
+        n = 1;
+      per_sm[dev] = n;
+    }
+    const long long cap = (long long)device_sm_count() * per_sm[dev];
     fa_bwd_pre_kernel<D><<<int(std::max(1LL, std::min(cap, (total + 255) / 256))), 256, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     // about two blocks per SM over all groups, at least one per group
