@@ -269,6 +269,38 @@ def oracle_sample(budget_s=12.0, points=None):
     return flops / t_used / 1e12, desc, t_used
 
 
+def oracle_tiny_single_core(repeats=5):
+    """The fp64 oracle's fwd+bwd on the tiny workload (B1 H2 S128 D64, causal off
+    and on) in a child process whose BLAS runs one thread: the median seconds of
+    a pass and the TFLOP/s by the same flop convention."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-tiny", str(repeats)], env=env,
+                       capture_output=True, text=True, timeout=120)
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return d["seconds"], d["tflops"]
+
+
+def _oracle_tiny_pass(repeats):
+    import numpy as np
+
+    import oracle
+    from fa_inputs import attention_inputs, bf16_bits_to_f64
+
+    inp = attention_inputs(1, 128, 128, 2, 64, seed=1, with_dout=True)
+    q, k, v, do = (bf16_bits_to_f64(inp[x]) for x in ("q", "k", "v", "dout"))
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        for causal in (False, True):
+            oracle.attention_fwd(q, k, v, None, causal)
+            oracle.attention_bwd(do, q, k, v, None, causal)
+        times.append(time.perf_counter() - t0)
+    sec = float(np.median(times))
+    flops = 3.5 * 4.0 * 1 * 2 * 128 * 128 * 64 * 1.5  # non-causal + causal (half)
+    print(json.dumps({"seconds": sec, "tflops": flops / sec / 1e12}), flush=True)
+    return 0
+
+
 def bench_config(ws):
     """The workload both arms report on."""
     return {"workload": "training-shaped sweep: hidden 2048 as D64/H32 and D128/H16, S 512..16k, "
@@ -521,6 +553,12 @@ def run_ours(args):
     if rank == 0 and not args.skip_cpu:
         v, desc, _ = oracle_sample(budget_s=args.cpu_budget)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": _cpu_cores_used(), "kind": "oracle", "sample": desc}
+        try:
+            sec, tfs = oracle_tiny_single_core()
+            cpu["tiny_single_core"] = {"seconds": sec, "tflops": tfs, "cores": 1,
+                                       "workload": "B1 H2 S128 D64 fwd+bwd, causal off and on"}
+        except Exception as e:
+            cpu["tiny_single_core"] = {"unavailable": str(e)[:120]}
 
     if rank == 0:
         line = {
@@ -700,7 +738,10 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--profile", choices=sorted(PROFILE_CASES), default=None,
                     help="run one small case of one op (for ncu captures) instead of the bench")
+    ap.add_argument("--oracle-tiny", type=int, default=0, help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
+    if args.oracle_tiny:
+        return _oracle_tiny_pass(args.oracle_tiny)
     if args.profile:
         return run_profile(args.profile)
     if args.warmup < 3:
