@@ -679,6 +679,8 @@ PROFILE_CASES = {
     "decode4k": dict(op="decode", B=16, S=4096, H=32, D=128, causal=True),
     # grouped decode (8 key/value heads, 4 query heads each): the tensor-core split kernel
     "decode_gqa4k": dict(op="decode", B=16, S=4096, H=32, Hk=8, D=128, causal=True),
+    # multi-query decode (one key/value head): 268 MB of cache
+    "decode_mqa32k": dict(op="decode", B=16, S=32768, H=32, Hk=1, D=128, causal=True),
 }
 
 

@@ -24,8 +24,8 @@
 //   log) in the workspace; a split with no live key writes O_s = 0, L_s = -inf.
 // Tensor-core split kernel (fa_decode_mma_kernel, described where it is
 // defined): the pairs of one key/value head as the rows of a 128-row MMA tile.
-// Merge kernel (one warp per (batch, query row, head)):
-//   L = log sum_s exp(L_s), O = sum_s exp(L_s - L) O_s, vectorised 16-byte loads.
+// Merge kernel (one block of four warps per (batch, query row, head)):
+//   L = log sum_s exp(L_s), O = sum_s exp(L_s - L) O_s.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -839,53 +839,78 @@ __global__ void __launch_bounds__(256) fa_kv_append_kernel(const __nv_bfloat16* 
   }
 }
 
-// One warp per (b, query row, head).
+// Merge of the splits' partials (section "2.2" of the page cited at the top of
+// this file): out = sum_s e^(L_s - L) O_s with L = log sum_s e^(L_s). One block of four warps per (b, query row, head); the
+// 128 threads read the L_s (n <= 256, two per thread), warp w folds the splits
+// s = w, w + 4, ... with independent loads in flight, and the four sums meet in
+// shared memory. A split with no live key wrote O_s = 0 and L_s = -inf.
+constexpr int COMBINE_THREADS = 128;
 template <int D>
-__global__ void __launch_bounds__(256) fa_decode_combine_kernel(const float* __restrict__ part_o,
-                                                                 const float* __restrict__ part_l,
-                                                                 __nv_bfloat16* __restrict__ out,
-                                                                 float* __restrict__ lse, int B, int Sq, int H,
-                                                                 int n) {
+__global__ void __launch_bounds__(COMBINE_THREADS) fa_decode_combine_kernel(const float* __restrict__ part_o,
+                                                                             const float* __restrict__ part_l,
+                                                                             __nv_bfloat16* __restrict__ out,
+                                                                             float* __restrict__ lse, int Sq, int H,
+                                                                             int n) {
   constexpr int PER = D / 32;  // columns per lane: 2, 4 or 8
-  const int warp_global = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (warp_global >= B * Sq * H) return;
-  const int h = warp_global % H;
-  const int i = (warp_global / H) % Sq;
-  const int b = warp_global / (H * Sq);
-  const size_t base = size_t(warp_global) * n;
-  float M = -INFINITY;
-  for (int s = lane; s < n; s += 32) M = fmaxf(M, part_l[base + s]);
+  constexpr int NWARP = COMBINE_THREADS / 32;
+  __shared__ float red[NWARP];
+  __shared__ float acc_s[NWARP - 1][D];
+  const int row = blockIdx.x;  // (b * Sq + i) * H + h
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const size_t base = size_t(row) * n;
+  const float l0 = tid < n ? part_l[base + tid] : -INFINITY;
+  const float l1 = tid + COMBINE_THREADS < n ? part_l[base + tid + COMBINE_THREADS] : -INFINITY;
+  float M = fmaxf(l0, l1);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  if (lane == 0) red[warp] = M;
+  __syncthreads();
+  M = red[0];
+#pragma unroll
+  for (int w = 1; w < NWARP; ++w) M = fmaxf(M, red[w]);
   const float Ms = (M == -INFINITY) ? 0.0f : M;
-  float Z = 0.0f;
-  for (int s = lane; s < n; s += 32) {
-    const float ls = part_l[base + s];
-    Z += (ls == -INFINITY) ? 0.0f : __expf(ls - Ms);
-  }
+  float Z = ((l0 == -INFINITY) ? 0.0f : __expf(l0 - Ms)) + ((l1 == -INFINITY) ? 0.0f : __expf(l1 - Ms));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, off);
-  const float invZ = Z > 0.0f ? 1.0f / Z : 0.0f;
+  __syncthreads();  // every thread has read red[] as maxima
+  if (lane == 0) red[warp] = Z;
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.0f;
-  for (int s = 0; s < n; ++s) {
+#pragma unroll 4
+  for (int s = warp; s < n; s += NWARP) {
     const float ls = part_l[base + s];
-    if (ls == -INFINITY) continue;
-    const float w = __expf(ls - Ms) * invZ;
     const float* src = part_o + (base + s) * D + lane * PER;
+    float v[PER];
 #pragma unroll
     for (int e = 0; e < PER; e += 2) {
       const float2 v2 = *reinterpret_cast<const float2*>(src + e);
-      acc[e] = fmaf(w, v2.x, acc[e]);
-      acc[e + 1] = fmaf(w, v2.y, acc[e + 1]);
+      v[e] = v2.x;
+      v[e + 1] = v2.y;
     }
+    const float w = (ls == -INFINITY) ? 0.0f : __expf(ls - Ms);
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, v[e], acc[e]);
+  }
+  if (warp > 0) {
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc_s[warp - 1][lane * PER + e] = acc[e];
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  Z = red[0];
+#pragma unroll
+  for (int w = 1; w < NWARP; ++w) Z += red[w];
+  const float invZ = Z > 0.0f ? 1.0f / Z : 0.0f;
+#pragma unroll
+  for (int w = 0; w < NWARP - 1; ++w) {
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] += acc_s[w][lane * PER + e];
   }
   uint32_t pk[PER / 2];
 #pragma unroll
-  for (int e = 0; e < PER / 2; ++e) pk[e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
-  __nv_bfloat16* dst = out + ((size_t(b) * Sq + i) * H + h) * D + lane * PER;
+  for (int e = 0; e < PER / 2; ++e) pk[e] = pack_bf16x2(acc[2 * e] * invZ, acc[2 * e + 1] * invZ);
+  __nv_bfloat16* dst = out + size_t(row) * D + lane * PER;  // out is (B, Sq, H, D)
   if constexpr (PER == 2) {
     *reinterpret_cast<uint32_t*>(dst) = pk[0];
   } else if constexpr (PER == 4) {
@@ -893,7 +918,10 @@ __global__ void __launch_bounds__(256) fa_decode_combine_kernel(const float* __r
   } else {
     *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   }
-  if (lane == 0) lse[(size_t(b) * H + h) * Sq + i] = (Z > 0.0f) ? Ms + __logf(Z) : -INFINITY;
+  if (lane == 0) {
+    const int h = row % H, i = (row / H) % Sq, b = row / (H * Sq);
+    lse[(size_t(b) * H + h) * Sq + i] = (Z > 0.0f) ? Ms + __logf(Z) : -INFINITY;
+  }
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -1017,17 +1045,26 @@ int decode_check(const AttnShape& s, const CacheArgs* cg) {
 int decode_auto_splits(int B, int Sq, int Sk, int H, int Hk, int D) {
   const bool mma = decode_mma_ok(Sq, H, Hk);
   const int tk = mma ? 128 : ((D == 64) ? 128 : (D == 128 ? 64 : 32));
-  const long long slots = (mma ? 1LL : 2LL) * device_sm_count();  // CTAs that fit per SM
+  const long long sms = device_sm_count();
+  const long long slots = (mma ? 1LL : 2LL) * sms;  // CTAs that fit per SM
   const int rpc = decode_rows_per_cta(Sq, H, Hk);
   const int rows_i = decode_mma_rows(Sq, H, Hk);
   const long long units = mma ? (long long)B * Hk * ((Sq + rows_i - 1) / rows_i)  // CTAs per split
                               : (long long)B * Hk * ((Sq * (H / Hk) + rpc - 1) / rpc);
-  // at least four tiles per split (eight for the tensor-core kernel, whose
-  // per-CTA start, one Q tile and the first K/V tiles, costs more)
-  const int min_tiles = mma ? 8 : 4;
-  int max_n = (Sk + min_tiles * tk - 1) / (min_tiles * tk);
+  // at least four tiles per split
+  int max_n = (Sk + 4 * tk - 1) / (4 * tk);
   if (max_n < 1) max_n = 1;
   if (max_n > 256) max_n = 256;
+  if (mma) {
+    // Tensor-core kernel (one CTA per SM): about 0.85 x the SM count of its CTAs
+    // already draw the whole HBM bandwidth on a long cache (measured on 152
+    // SMs: 128 CTAs beat 144 and 152, and every split count making more CTAs
+    // than that in one wave, or a second wave, only adds a tail). With fewer
+    // units than that, the largest split count staying within it.
+    const long long fill = std::max(1LL, sms * 85 / 100);
+    if (units <= fill) return int(std::max(1LL, std::min<long long>(max_n, fill / units)));
+  }
+  // Otherwise the fewest splits that fill whole waves to 95%, else the best fill.
   int best = 1;
   double best_eff = 0.0;
   for (int n = 1; n <= max_n; ++n) {
@@ -1137,9 +1174,9 @@ static int launch_decode_t(const AttnShape& s, const void* q, const void* k, con
     kern<<<dim3(n, s.Hk * p.n_rb, s.B), C::THREADS, C::SMEM_BYTES, stream>>>(mk, mv, p);
   }
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  const long long warps = (long long)s.B * s.Sq * s.H;
-  fa_decode_combine_kernel<D><<<unsigned((warps + 7) / 8), 256, 0, stream>>>(
-      p.part_o, p.part_l, static_cast<__nv_bfloat16*>(out), lse, s.B, s.Sq, s.H, n);
+  const long long rows = (long long)s.B * s.Sq * s.H;
+  fa_decode_combine_kernel<D><<<unsigned(rows), COMBINE_THREADS, 0, stream>>>(
+      p.part_o, p.part_l, static_cast<__nv_bfloat16*>(out), lse, s.Sq, s.H, n);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
