@@ -188,8 +188,11 @@ int fa_bwd_varlen(const void* dout, const void* q, const void* k, const void* v,
                   const float* alibi_slopes, int alibi_batch_stride, int deterministic, fa_stream_t stream);
 
 /*
- * Split count fa_decode_splitkv uses when num_splits == 0: chosen from the
- * SM count of the current device so the split kernel fills whole waves.
+ * Split count fa_decode_splitkv uses when num_splits == 0, from the SM count of
+ * the current device. For the tensor-core split kernel (four or more query
+ * pairs per key/value head), while its CTAs per split stay below 0.85 x the SM
+ * count: the largest count within that (that many CTAs already draw the whole
+ * HBM bandwidth). Otherwise: the fewest splits that fill whole waves.
  */
 int fa_decode_num_splits(int B, int Sq, int Sk, int H, int Hk, int D);
 
