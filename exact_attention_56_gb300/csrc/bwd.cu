@@ -65,7 +65,7 @@ struct BwdParams {
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
   const float* lse;
-  float* l2;      // (B, H, Sq_pad): L * log2(e); +inf on rows without keys and on padding
+  float* nl2;     // (B, H, Sq_pad): -L * log2(e), the exponent's bias; -inf on rows without keys and on padding
   float* dvec;    // (B, H, Sq_pad): rowsum(dO * O)
   uint16_t* q16;  // fp16 copies, (B, S, H, D) like the inputs
   uint16_t* do16;
@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
         const size_t vi = (size_t(b) * p.H + h) * p.Sq_pad + s;
         p.dvec[vi] = acc;
         const float L = p.lse[li];
-        p.l2[vi] = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
+        p.nl2[vi] = (L == -INFINITY) ? -INFINITY : -(L * 1.4426950408889634f);
         track(((long long)b * p.Hk + h / p.group) * 2, mq, mdo);
       }
     } else if (wb < p0) {
@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const BwdParams p) {
         const int sq = p.cu_q ? p.cu_q[b + 1] - p.cu_q[b] : p.Sq;
         if (s >= sq) {
           p.dvec[t] = 0.0f;
-          p.l2[t] = INFINITY;
+          p.nl2[t] = -INFINITY;
         }
       }
     }
@@ -576,7 +576,8 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
 
   // Live query tiles of this key tile: a contiguous range, the same for every
   // query head. Iteration ii covers query head hk*group + ii / n_qtl and query
-  // tile qt_first + ii % n_qtl, so the group's dK, dV sums stay in this CTA.
+  // tile qt_first + ii % n_qtl (the loops step both), so the group's dK, dV sums
+  // stay in this CTA.
   int qt_first = n_qt, qt_last = -1;
   for (int qt = 0; qt < n_qt; ++qt) {
     if (qtile_meets(qt, kt, p, Sq, Sk)) {
@@ -635,10 +636,11 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
                     sq_.tb);
       }
       int q_issued = 0, do_issued = 0;
-      for (int ii = 0; ii < n_iter; ++ii) {
+      // query head and tile of iteration ii, stepped instead of divided out
+      int hq = hk * p.group, qt = qt_first;
+      for (int ii = 0; ii < n_iter; ++ii, qt = (qt == qt_last) ? (++hq, qt_first) : qt + 1) {
         const int s = ii % C::NQ;
-        const int hq = hk * p.group + ii / n_qtl;
-        const int i0 = (qt_first + ii % n_qtl) * 128;
+        const int i0 = qt * 128;
         const size_t vec_base = (size_t(b) * p.H + hq) * p.Sq_pad;
         if (!fa_wait_warp(&bars->q_empty[s], (uint32_t(ii / C::NQ) & 1u) ^ 1u, watch, SITE_KV_EMPTY)) break;
         mbar_arrive_expect_tx_w(&bars->q_full[s], C::TILE_BYTES);
@@ -652,7 +654,7 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
         for (int pn = 0; pn < C::PANELS; ++pn)
           tma_load_4d_w(smem + C::DO_OFF + d * C::TILE_BYTES + pn * C::PANEL_BYTES, &tm_do, &bars->do_full[d],
                       pn * 64, hq, sq_.q_off + i0, sq_.tb);
-        bulk_load_w(smem + C::VEC_OFF + d * 1024, p.l2 + vec_base + i0, 512, &bars->do_full[d]);
+        bulk_load_w(smem + C::VEC_OFF + d * 1024, p.nl2 + vec_base + i0, 512, &bars->do_full[d]);
         bulk_load_w(smem + C::VEC_OFF + d * 1024 + 512, p.dvec + vec_base + i0, 512, &bars->do_full[d]);
         do_issued = ii + 1;
       }
@@ -793,14 +795,15 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
     // the group's range factors (warp 2): S^T arrives as 2^(eq+ek) S^T
     bool ok = fa_wait_warp(&bars->fac_ready, 0, watch, SITE_KV_FAC);
     const float sl = bars->fac[0];
-    for (int ii = 0; ii < n_iter && ok; ++ii) {
+    // query head and tile of iteration ii, stepped instead of divided out
+    int hq = hk * p.group, qt = qt_first;
+    for (int ii = 0; ii < n_iter && ok; ++ii, qt = (qt == qt_last) ? (++hq, qt_first) : qt + 1) {
       const int d = ii % C::NDO;
-      const int hq = hk * p.group + ii / n_qtl;
-      const int i0 = (qt_first + ii % n_qtl) * 128;
+      const int i0 = qt * 128;
       const float slope_log2 = has_alibi ? p.alibi[b * p.alibi_bstride + hq] * 1.4426950408889634f : 0.0f;
       const int ib = i0 + w * C::COLS;  // first query of this group
-      const float4* l2v = reinterpret_cast<const float4*>(smem + C::VEC_OFF + d * 1024) + w * (C::COLS / 4);
-      const float4* dvv = l2v + 32;
+      const float4* nl2v = reinterpret_cast<const float4*>(smem + C::VEC_OFF + d * 1024) + w * (C::COLS / 4);
+      const float4* dvv = nl2v + 32;
       // the L2 / D vectors of this tile land with dO
       if (!(ok = fa_wait_warp(&bars->do_full[d], uint32_t(ii / C::NDO) & 1u, watch, SITE_KV_DOFULL))) break;
       if (!(ok = fa_wait_warp(&bars->s_full, uint32_t(ii) & 1u, watch, SITE_KV_S))) break;
@@ -822,9 +825,9 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
         uint64_t distB = f2_pack(float(dd0) + 2.0f, float(dd0) + 3.0f);
 #pragma unroll
         for (int c4 = 0; c4 < C::COLS / 4; ++c4) {
-          const float4 l4 = l2v[c4];
-          const uint64_t bA = f2_sub(f2_pack(-l4.x, -l4.y), f2_mul(distA, ms2));
-          const uint64_t bB = f2_sub(f2_pack(-l4.z, -l4.w), f2_mul(distB, ms2));
+          const float4 l4 = nl2v[c4];
+          const uint64_t bA = f2_sub(f2_pack(l4.x, l4.y), f2_mul(distA, ms2));
+          const uint64_t bB = f2_sub(f2_pack(l4.z, l4.w), f2_mul(distB, ms2));
           distA = f2_add(distA, st2);
           distB = f2_add(distB, st2);
           float a0, a1, a2, a3;
@@ -835,21 +838,31 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
           pv[4 * c4 + 2] = ex2_approx(a2);
           pv[4 * c4 + 3] = ex2_approx(a3);
         }
-      } else {
+      } else if (has_alibi) {
 #pragma unroll
         for (int c4 = 0; c4 < C::COLS / 4; ++c4) {
-          const float4 l4 = l2v[c4];
-          float b0 = -l4.x, b1 = -l4.y, b2 = -l4.z, b3 = -l4.w;
-          if (has_alibi) {
-            const float dd = float(dd0 + 4 * c4);
-            b0 -= slope_log2 * fabsf(dd);
-            b1 -= slope_log2 * fabsf(dd + 1.0f);
-            b2 -= slope_log2 * fabsf(dd + 2.0f);
-            b3 -= slope_log2 * fabsf(dd + 3.0f);
-          }
+          const float4 l4 = nl2v[c4];
+          const float dd = float(dd0 + 4 * c4);
+          const float b0 = l4.x - slope_log2 * fabsf(dd);
+          const float b1 = l4.y - slope_log2 * fabsf(dd + 1.0f);
+          const float b2 = l4.z - slope_log2 * fabsf(dd + 2.0f);
+          const float b3 = l4.w - slope_log2 * fabsf(dd + 3.0f);
           float a0, a1, a2, a3;
           f2_unpack(f2_fma(f2_pack(pv[4 * c4], pv[4 * c4 + 1]), sl2, f2_pack(b0, b1)), a0, a1);
           f2_unpack(f2_fma(f2_pack(pv[4 * c4 + 2], pv[4 * c4 + 3]), sl2, f2_pack(b2, b3)), a2, a3);
+          pv[4 * c4] = ex2_approx(a0);
+          pv[4 * c4 + 1] = ex2_approx(a1);
+          pv[4 * c4 + 2] = ex2_approx(a2);
+          pv[4 * c4 + 3] = ex2_approx(a3);
+        }
+      } else {
+        // the stored bias pairs feed the paired FMA as they are
+#pragma unroll
+        for (int c4 = 0; c4 < C::COLS / 4; ++c4) {
+          const float4 l4 = nl2v[c4];
+          float a0, a1, a2, a3;
+          f2_unpack(f2_fma(f2_pack(pv[4 * c4], pv[4 * c4 + 1]), sl2, f2_pack(l4.x, l4.y)), a0, a1);
+          f2_unpack(f2_fma(f2_pack(pv[4 * c4 + 2], pv[4 * c4 + 3]), sl2, f2_pack(l4.z, l4.w)), a2, a3);
           pv[4 * c4] = ex2_approx(a0);
           pv[4 * c4 + 1] = ex2_approx(a1);
           pv[4 * c4 + 2] = ex2_approx(a2);
@@ -878,15 +891,18 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
           const float4 d4 = dvv[c / 4];
           const float dv0 = (c % 4 == 0) ? d4.x : d4.z;
           const float dv1 = (c % 4 == 0) ? d4.y : d4.w;
-          float z0 = 1.0f, z1 = 1.0f;
-          if (DROP) {  // this key's flags for query rows ib + c and ib + c + 1
-            const int bh = b * p.H + hq;
-            z0 = (dropout_keep4(p.drop, bh, ib + c, j >> 2) >> (j & 3)) & 1u ? p.drop.keep_scale : 0.0f;
-            z1 = (dropout_keep4(p.drop, bh, ib + c + 1, j >> 2) >> (j & 3)) & 1u ? p.drop.keep_scale : 0.0f;
-          }
           float s0, s1;
-          ds_pair(pv[c], pv[c + 1], dp[2 * e] * z0, dp[2 * e + 1] * z1, dv0, dv1, s0, s1);
-          pp[e] = pack_f16x2(pv[c] * z0, pv[c + 1] * z1);
+          if constexpr (DROP) {  // this key's flags for query rows ib + c and ib + c + 1
+            const int bh = b * p.H + hq;
+            const float z0 = (dropout_keep4(p.drop, bh, ib + c, j >> 2) >> (j & 3)) & 1u ? p.drop.keep_scale : 0.0f;
+            const float z1 =
+                (dropout_keep4(p.drop, bh, ib + c + 1, j >> 2) >> (j & 3)) & 1u ? p.drop.keep_scale : 0.0f;
+            ds_pair(pv[c], pv[c + 1], dp[2 * e] * z0, dp[2 * e + 1] * z1, dv0, dv1, s0, s1);
+            pp[e] = pack_f16x2(pv[c] * z0, pv[c + 1] * z1);
+          } else {
+            ds_pair(pv[c], pv[c + 1], dp[2 * e], dp[2 * e + 1], dv0, dv1, s0, s1);
+            pp[e] = pack_f16x2(pv[c], pv[c + 1]);
+          }
           ps[e] = pack_f16x2(s0, s1);
         }
         tmem_st_x8(col, pp);
@@ -1175,7 +1191,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     const int tile_lo_max = live_range(last_row, Sq, Sk, p.wl, p.wr).lo;
     const int tile_hi_min = live_range(row0, Sq, Sk, p.wl, p.wr).hi;
     const size_t vi = (size_t(b) * p.H + h) * p.Sq_pad + i;  // i < Sq_pad always
-    const float l2 = p.l2[vi];
+    const float nl2 = p.nl2[vi];
     const float dval = p.dvec[vi];
     const bool has_alibi = p.alibi != nullptr;
     const float slope_log2 = has_alibi ? p.alibi[b * p.alibi_bstride + h] * 1.4426950408889634f : 0.0f;
@@ -1198,7 +1214,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         // signed slope (same rounding as the scalar form below)
         const float d0 = float(c_i - kb);
         const float ns = (kb >= c_i) ? slope_log2 : -slope_log2;
-        const uint64_t ns2 = f2_pack(ns, ns), sl2 = f2_pack(sl, sl), nl2 = f2_pack(-l2, -l2);
+        const uint64_t ns2 = f2_pack(ns, ns), sl2 = f2_pack(sl, sl), nl2p = f2_pack(nl2, nl2);
         const uint64_t st2 = f2_pack(4.0f, 4.0f);
         uint64_t dist[2] = {f2_pack(d0, d0 - 1.0f), f2_pack(d0 - 2.0f, d0 - 3.0f)};
 #pragma unroll
@@ -1207,7 +1223,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
           for (int k = 0; k < 2; ++k) {
             const int cc = c + 2 * k;
             float a0, a1;
-            f2_unpack(f2_fma(f2_pack(pv[cc], pv[cc + 1]), sl2, f2_add(f2_mul(dist[k], ns2), nl2)), a0, a1);
+            f2_unpack(f2_fma(f2_pack(pv[cc], pv[cc + 1]), sl2, f2_add(f2_mul(dist[k], ns2), nl2p)), a0, a1);
             pv[cc] = ex2_approx(a0);
             pv[cc + 1] = ex2_approx(a1);
             dist[k] = f2_sub(dist[k], st2);
@@ -1217,13 +1233,13 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         const float d0 = float(c_i - kb);
 #pragma unroll
         for (int c = 0; c < C::COLS; ++c)
-          pv[c] = ex2_approx(fmaf(pv[c], sl, -slope_log2 * fabsf(d0 - float(c)) - l2));
+          pv[c] = ex2_approx(fmaf(pv[c], sl, -slope_log2 * fabsf(d0 - float(c)) + nl2));
       } else {
-        const uint64_t sl2 = f2_pack(sl, sl), nl2 = f2_pack(-l2, -l2);
+        const uint64_t sl2 = f2_pack(sl, sl), nl2p = f2_pack(nl2, nl2);
 #pragma unroll
         for (int c = 0; c < C::COLS; c += 2) {
           float a0, a1;
-          f2_unpack(f2_fma(f2_pack(pv[c], pv[c + 1]), sl2, nl2), a0, a1);
+          f2_unpack(f2_fma(f2_pack(pv[c], pv[c + 1]), sl2, nl2p), a0, a1);
           pv[c] = ex2_approx(a0);
           pv[c + 1] = ex2_approx(a1);
         }
@@ -1247,16 +1263,17 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         uint32_t keep = 0;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          float z0 = 1.0f, z1 = 1.0f;
-          if (DROP) {  // keys kb + c .. : one generator call per four keys
+          float s0, s1;
+          if constexpr (DROP) {  // keys kb + c .. : one generator call per four keys
             const int c = 16 * ch + 2 * e;
             if ((e & 1) == 0) keep = dropout_keep4(p.drop, b * p.H + h, i, (kb + c) >> 2);
-            z0 = (keep >> (c & 3)) & 1u ? p.drop.keep_scale : 0.0f;
-            z1 = (keep >> ((c & 3) + 1)) & 1u ? p.drop.keep_scale : 0.0f;
+            const float z0 = (keep >> (c & 3)) & 1u ? p.drop.keep_scale : 0.0f;
+            const float z1 = (keep >> ((c & 3) + 1)) & 1u ? p.drop.keep_scale : 0.0f;
+            ds_pair(pv[16 * ch + 2 * e], pv[16 * ch + 2 * e + 1], dp[2 * e] * z0, dp[2 * e + 1] * z1, dval, dval, s0,
+                    s1);
+          } else {
+            ds_pair(pv[16 * ch + 2 * e], pv[16 * ch + 2 * e + 1], dp[2 * e], dp[2 * e + 1], dval, dval, s0, s1);
           }
-          float s0, s1;
-          ds_pair(pv[16 * ch + 2 * e], pv[16 * ch + 2 * e + 1], dp[2 * e] * z0, dp[2 * e + 1] * z1, dval, dval, s0,
-                  s1);
           pk[e] = pack_f16x2(s0, s1);
         }
         tmem_st_x8(col, pk);
@@ -1347,7 +1364,7 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
   const long long rows_k = vl ? vl->total_k : (long long)s.B * s.Sk;
   const BwdWs L = bwd_ws(s.B, s.Sq, rows_q, rows_k, s.H, s.Hk, D);
   uint8_t* w = static_cast<uint8_t*>(ws);
-  p.l2 = reinterpret_cast<float*>(w);
+  p.nl2 = reinterpret_cast<float*>(w);
   p.dvec = reinterpret_cast<float*>(w + L.vec);
   p.q16 = reinterpret_cast<uint16_t*>(w + 2 * L.vec);
   p.do16 = reinterpret_cast<uint16_t*>(w + 2 * L.vec + L.qside);
