@@ -521,7 +521,10 @@ struct KvCfg {
   static constexpr int VEC_OFF = DO_OFF + NDO * TILE_BYTES;  // per dO stage: L2[128], D[128]
   static constexpr int BAR_OFF = VEC_OFF + NDO * 1024;
   static constexpr int SMEM_BYTES = BAR_OFF + 256;
-  static constexpr int NCW = 4;  // compute warpgroups; each owns COLS query columns
+  // Compute warpgroups; each owns COLS query columns. Two halve the per-tile
+  // bookkeeping (waits, fences, arrives, addresses) per element against four:
+  // 20% fewer instructions, 1% (D = 64) to 4% (D = 128) faster at S = 4096.
+  static constexpr int NCW = 2;
   static constexpr int COLS = 128 / NCW;
   static constexpr int NCT = 128 * NCW;  // compute threads
   static constexpr int THREADS = 128 + NCT;
@@ -971,7 +974,10 @@ struct DqCfg {
   static constexpr int V_OFF = K_OFF + NK * TILE_BYTES;
   static constexpr int BAR_OFF = V_OFF + NV * TILE_BYTES;
   static constexpr int SMEM_BYTES = BAR_OFF + 256;
-  static constexpr int NCW = 4;  // compute warpgroups; each owns COLS key columns
+  // Compute warpgroups; each owns COLS key columns. Two at D = 128 (3.5% faster
+  // than four at S = 4096); four at D = 64, where shorter per-warp chains hide
+  // more of the per-tile latency (two were 1.3% slower).
+  static constexpr int NCW = D == 64 ? 4 : 2;
   static constexpr int COLS = 128 / NCW;
   static constexpr int NCT = 128 * NCW;
   static constexpr int THREADS = 128 + NCT;
