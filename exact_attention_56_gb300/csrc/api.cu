@@ -87,6 +87,19 @@ bool make_bshd_map_box(CUtensorMap* map, const void* base, int B, int S, int H, 
   return r == CUDA_SUCCESS;
 }
 
+bool make_bshd_map_f32(CUtensorMap* map, const void* base, int B, int S, int H, int D, int box_cols, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {cuuint64_t(D), cuuint64_t(H), cuuint64_t(S), cuuint64_t(B)};
+  cuuint64_t strides[3] = {cuuint64_t(D) * 4, cuuint64_t(H) * D * 4, cuuint64_t(S) * H * D * 4};
+  cuuint32_t box[4] = {cuuint32_t(box_cols), 1, cuuint32_t(box_rows), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int check_common(int B, int Sq, int Sk, int H, int Hk, int D, float scale, int causal, int wl, int wr,
                         const float* alibi, int alibi_bstride, AttnShape* s) {
   if (B < 1 || Sq < 1 || Sk < 1 || H < 1 || D < 1) return FA_ERR_INVALID;

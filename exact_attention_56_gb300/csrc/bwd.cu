@@ -115,6 +115,8 @@ enum : uint32_t {
   SITE_KV_DOEMPTY = 0x3A,
   SITE_KV_ALIGN = 0x3B,
   SITE_KV_FAC = 0x3C,
+  SITE_KV_DS = 0x3D,
+  SITE_KV_DQ = 0x3E,
   SITE_DQ_EMPTY = 0x41,
   SITE_DQ_Q = 0x42,
   SITE_DQ_K = 0x43,
@@ -502,8 +504,14 @@ __global__ void __launch_bounds__(256) fa_bwd_rescale_kernel(const BwdParams p) 
 }
 
 // ============================================================================ dK / dV
-template <int D>
+// FDQ: the dK/dV kernel also forms each query tile's share of dQ (dS K over
+// this CTA's 128 keys, M = queries) and adds it into an fp32 accumulator with a
+// TMA reduction (page "FlashAttention：快速且内存高效的准确注意力机制", section
+// "并行性 / 反向传播": dQ is summed across the key blocks). D = 64 only: TMEM then
+// has room for the dQ tile beside S^T, one dP^T buffer, dV and dK.
+template <int D, bool FDQ = false>
 struct KvCfg {
+  static_assert(!FDQ || D == 64, "the fused dQ fits TMEM at D = 64 only");
   static constexpr int PANELS = D / 64;
   static constexpr int PANEL_BYTES = 128 * 128;
   static constexpr int TILE_BYTES = PANELS * PANEL_BYTES;
@@ -511,16 +519,23 @@ struct KvCfg {
   // is still being processed), so Q gets a third stage; dO is read last. At
   // D = 64, dP^T of tile ii+1 also runs early (two dP^T buffers), and the
   // smaller tiles leave room for four stages of each.
-  static constexpr int NQ = D == 64 ? 4 : 3;   // Q stages
-  static constexpr int NDO = D == 64 ? 4 : 2;  // dO (+ L2, D) stages
-  static constexpr int NDP = D == 64 ? 2 : 1;  // dP^T buffers in TMEM
+  static constexpr int NQ = D == 64 ? 4 : 3;                    // Q stages
+  static constexpr int NDO = D == 64 ? (FDQ ? 3 : 4) : 2;       // dO (+ L2, D) stages
+  static constexpr int NDP = (D == 64 && !FDQ) ? 2 : 1;         // dP^T buffers in TMEM
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = TILE_BYTES;
   static constexpr int Q_OFF = 2 * TILE_BYTES;
   static constexpr int DO_OFF = Q_OFF + NQ * TILE_BYTES;
   static constexpr int VEC_OFF = DO_OFF + NDO * TILE_BYTES;  // per dO stage: L2[128], D[128]
-  static constexpr int BAR_OFF = VEC_OFF + NDO * 1024;
-  static constexpr int SMEM_BYTES = BAR_OFF + 256;
+  // FDQ: dS of the tile as the dQ MMA's A operand (M = 128 queries in two
+  // 64-query panels of 128 key rows, MN-major, 128-byte swizzled), and per
+  // compute warp a 32-row x 32-column fp32 staging box for its reduction.
+  static constexpr int DS_OFF = VEC_OFF + NDO * 1024;
+  static constexpr int DS_BYTES = FDQ ? 2 * PANEL_BYTES : 0;
+  static constexpr int STG_OFF = DS_OFF + DS_BYTES;
+  static constexpr int STG_BYTES = FDQ ? 2 * 128 * 128 : 0;
+  static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
+  static constexpr int SMEM_BYTES = BAR_OFF + 320;
   // Compute warpgroups; each owns COLS query columns. Two halve the per-tile
   // bookkeeping (waits, fences, arrives, addresses) per element against four:
   // 20% fewer instructions, 1% (D = 64) to 4% (D = 128) faster at S = 4096.
@@ -536,9 +551,11 @@ struct KvCfg {
   // has read itself; dV and dK accumulators after the buffers. With two
   // buffers, S^T and dP^T of tile ii+1 run on the tensor pipe while the
   // compute groups form P^T and dS^T of tile ii.
-  static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 128 + 128 * NDP, T_DK = T_DV + D;
-  static_assert(T_DK + D <= 512, "TMEM budget");
+  // FDQ: the tile's dQ share (lanes = query rows) after dK.
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 128 + 128 * NDP, T_DK = T_DV + D, T_DQ = T_DK + D;
+  static_assert(T_DK + D + (FDQ ? D : 0) <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(!FDQ || NCW == 2, "one staging box of 32 dQ columns per compute group");
 };
 
 struct KvBars {
@@ -548,18 +565,21 @@ struct KvBars {
   uint64_t s_full, s_free, acc_done, drain;
   uint64_t dp_full[2], pd_ready[2];  // per dP^T buffer
   uint64_t fac_ready;                 // fac[] written (warp 2)
-  float fac[4];                       // scale_log2 for S^T, dV factor, dK factors m1, m2
+  uint64_t ds_ready, dq_full;         // FDQ: dS in shared memory; the tile's dQ share done
+  float fac[6];                       // scale_log2 for S^T, dV factor, dK factors m1, m2, dQ factors m1, m2
   uint32_t tmem_base;
   int abort;
 };
-static_assert(sizeof(KvBars) <= 256, "barrier block");
+static_assert(sizeof(KvBars) <= 320, "barrier block");
 
-template <int D, bool DROP>
-__global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
+// FDQ: tm_dqa maps the fp32 dQ accumulator (B, Sq, H, D) in boxes of 32 columns x
+// 32 rows; otherwise unused.
+template <int D, bool DROP, bool FDQ>
+__global__ void __launch_bounds__(KvCfg<D, FDQ>::THREADS, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                       const BwdParams p) {
-  using C = KvCfg<D>;
+                       const __grid_constant__ CUtensorMap tm_dqa, const BwdParams p) {
+  using C = KvCfg<D, FDQ>;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {  // the swizzled layouts need 1024-byte alignment
     if (threadIdx.x == 0) atomicOr(p.status, FA_DEV_TIMEOUT | SITE_KV_ALIGN);
@@ -610,6 +630,8 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->drain, 1);
     mbar_init(&bars->fac_ready, 1);
+    mbar_init(&bars->ds_ready, C::NCT / 32);  // one arrive per compute warp
+    mbar_init(&bars->dq_full, 1);
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -682,7 +704,12 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
       const uint64_t do_kdesc = sdesc_sw128(smem_u32(smem + C::DO_OFF), 16, 1024);   // dO as K-major (dP^T)
       const uint64_t q_mdesc = sdesc_sw128(smem_u32(smem + C::Q_OFF), C::PANEL_BYTES, 1024);    // MN-major (dK)
       const uint64_t do_mdesc = sdesc_sw128(smem_u32(smem + C::DO_OFF), C::PANEL_BYTES, 1024);  // MN-major (dV)
+      // FDQ: dQ share = dS K, A = dS (queries x keys) and B = K (keys x D), both MN-major
+      constexpr uint32_t ID_DQ = idesc_f16_f32(128, D, 1, 1);
+      const uint64_t ds_desc = sdesc_sw128(smem_u32(smem + C::DS_OFF), C::PANEL_BYTES, 1024);
+      const uint64_t k_mdesc = sdesc_sw128(smem_u32(smem + C::K_OFF), C::PANEL_BYTES, 1024);
       const uint32_t t_s = tmem + C::T_S, t_dp = tmem + C::T_DP, t_dv = tmem + C::T_DV, t_dk = tmem + C::T_DK;
+      const uint32_t t_dq = tmem + C::T_DQ;
       // dP^T(ii) = V dO^T into buffer ii % NDP
       auto issue_dp = [&](int ii) {
         if (!fa_wait_warp(&bars->do_full[ii % C::NDO], uint32_t(ii / C::NDO) & 1u, watch, SITE_KV_DOFULL))
@@ -752,6 +779,18 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
         // with one buffer, dP^T of the next tile overwrites P^T and dS^T of this
         // one, read above (in order)
         if (C::NDP == 1 && more && !(ok = issue_dp(ii + 1))) break;
+        if constexpr (FDQ) {
+          // this tile's dQ share over the CTA's 128 keys, from scratch, once dS is in
+          // shared memory; behind dP^T of the next tile, so that one reaches the
+          // compute warps first. They read the share (dq_full) during the next
+          // tile, before they arrive on its ds_ready, which the next share waits for.
+          if (!(ok = fa_wait_warp(&bars->ds_ready, uint32_t(ii) & 1u, watch, SITE_KV_DS))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss_w(t_dq, sdesc_adv(ds_desc, kk * 2048), sdesc_adv(k_mdesc, kk * 2048), ID_DQ, kk > 0 ? 1u : 0u);
+          mma_commit_w(&bars->dq_full);
+        }
       }
       if (ok) {
         mma_commit_w(&bars->acc_done);
@@ -767,6 +806,7 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
       bars->fac[0] = p.scale_log2 * pow2f(-ge.q) * pow2f(-ge.k);
       bars->fac[1] = pow2f(-ge.dO);
       unscale_factors(p.scale, ge.dO + ge.v + ge.q, bars->fac[2], bars->fac[3]);
+      unscale_factors(p.scale, ge.dO + ge.v + ge.k, bars->fac[4], bars->fac[5]);  // dQ' = 2^(edo+ev+ek) dQ / scale
       mbar_arrive(&bars->fac_ready);
     }
   } else if (warp >= 4) {
@@ -798,6 +838,32 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
     // the group's range factors (warp 2): S^T arrives as 2^(eq+ek) S^T
     bool ok = fa_wait_warp(&bars->fac_ready, 0, watch, SITE_KV_FAC);
     const float sl = bars->fac[0];
+    // FDQ: a tile's dQ share (TMEM lanes = query rows; group w takes columns
+    // 32w .. 32w+31), times the unscaling factors, into the warp's staging box
+    // (its 32 rows at 128 bytes each, 16-byte chunk c of row l at c ^ (l & 7): the
+    // 128-byte swizzle of the accumulator's tensor map), then one TMA reduction of
+    // the box into the fp32 accumulator, issued by lane 0. Before the box is
+    // written again, lane 0 waits until its last reduction has read it.
+    uint8_t* stg = smem + C::STG_OFF + w * (128 * 128) + wq * (32 * 128);
+    auto reduce_dq = [&](int hq_t, int i0_t) {
+      float a[32];
+      tmem_ld_cols(tmem + lane_addr + C::T_DQ + uint32_t(w) * 32, a);
+      if (lane == 0) bulk_wait_group_read0();
+      __syncwarp();
+      const float m1 = bars->fac[4], m2 = bars->fac[5];
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4*>(stg + lane * 128 + ((c ^ (lane & 7)) * 16)) =
+            make_float4(a[4 * c] * m1 * m2, a[4 * c + 1] * m1 * m2, a[4 * c + 2] * m1 * m2, a[4 * c + 3] * m1 * m2);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_reduce_add_4d(&tm_dqa, stg, w * 32, hq_t, i0_t + wq * 32, b);
+        bulk_commit_group();
+      }
+      __syncwarp();
+    };
+    int hq_prev = 0, i0_prev = 0;  // FDQ: the previous tile's query head and first row
     // query head and tile of iteration ii, stepped instead of divided out
     int hq = hk * p.group, qt = qt_first;
     for (int ii = 0; ii < n_iter && ok; ++ii, qt = (qt == qt_last) ? (++hq, qt_first) : qt + 1) {
@@ -882,6 +948,7 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
       tc_fence_after();
       // per 16-query chunk: load dP^T, form dS^T, then P^T and dS^T as fp16 pairs over
       // the chunk's consumed dP^T columns (see the TMEM map)
+      uint32_t ds_all[FDQ ? C::COLS / 2 : 1];  // FDQ: the tile's dS, kept for shared memory
 #pragma unroll
       for (int ch = 0; ch < C::COLS / 16; ++ch) {
         float dp[16];
@@ -910,10 +977,36 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
         }
         tmem_st_x8(col, pp);
         tmem_st_x8(col + 8, ps);
+        if constexpr (FDQ) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ds_all[8 * ch + e] = ps[e];
+        }
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive_warp(&bars->pd_ready[pb]);
+      if constexpr (FDQ) {
+        // The last tile's dQ share is complete (and has read the dS buffer): add it
+        // into the accumulator, then this tile's dS as the dQ MMA's A operand, key
+        // row r of the group's 64-query panel.
+        if (ii > 0) {
+          if (!(ok = fa_wait_warp(&bars->dq_full, uint32_t(ii - 1) & 1u, watch, SITE_KV_DQ))) break;
+          tc_fence_after();
+          reduce_dq(hq_prev, i0_prev);
+        }
+        uint8_t* ds_row = smem + C::DS_OFF + w * C::PANEL_BYTES + r * 128;
+#pragma unroll
+        for (int ch = 0; ch < C::COLS / 16; ++ch) {
+          const uint32_t* v = ds_all + 8 * ch;
+          *reinterpret_cast<uint4*>(ds_row + (((2 * ch) ^ (r & 7)) * 16)) = make_uint4(v[0], v[1], v[2], v[3]);
+          *reinterpret_cast<uint4*>(ds_row + (((2 * ch + 1) ^ (r & 7)) * 16)) = make_uint4(v[4], v[5], v[6], v[7]);
+        }
+        fence_proxy_async_smem();  // dS is read by the tensor core next
+        tc_fence_before();         // and the share's TMEM columns are rewritten by the next share
+        mbar_arrive_warp(&bars->ds_ready);
+      }
+      hq_prev = hq;
+      i0_prev = i0;
     }
     // ------------------------------------------------------------ dK / dV epilogue
     // groups 0..NCW/2-1 write dV, the rest dK (times scale); each a D/(NCW/2)-column slice
@@ -933,6 +1026,7 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
         for (int e = 0; e < SLICE / 8; ++e) reinterpret_cast<uint4*>(dst)[e] = make_uint4(0, 0, 0, 0);
     } else if (ok && fa_wait_warp(&bars->acc_done, 0, watch, SITE_KV_ACC)) {
       tc_fence_after();
+      if constexpr (FDQ) reduce_dq(hq_prev, i0_prev);  // the last tile's dQ share (acc_done follows it)
 #pragma unroll 1
       for (int cc = 0; cc < SLICE / 32; ++cc) {
         float a[32];
@@ -947,6 +1041,8 @@ __global__ void __launch_bounds__(KvCfg<D>::THREADS, 1)
         }
       }
     }
+    // every reduction this warp issued has landed before the CTA ends
+    if (FDQ && lane == 0) bulk_wait_group0();
   }
 
   tc_fence_before();
@@ -1326,31 +1422,48 @@ static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 // Workspace: L2 and D vectors (B, H, Sq_pad) fp32 (Sq_pad: the longest query
 // sequence rounded up to 128 rows), then fp16 copies of Q, dO (rows_q tokens,
 // H heads) and K, V (rows_k tokens, Hk heads), then the group maxima (B, Hk, 4)
-// and their replicas (B, Hk, AMAX_REPS, 4) uint32, each region 256-byte aligned.
+// and their replicas (B, Hk, AMAX_REPS, 4) uint32, then (fused dQ only) the
+// fp32 dQ accumulator (rows_q, H, D), each region 256-byte aligned.
 struct BwdWs {
-  size_t vec, qside, kside, amax, reps;
-  size_t total() const { return 2 * vec + 2 * qside + 2 * kside + amax + reps; }
+  size_t vec, qside, kside, amax, reps, dqa;
+  size_t total() const { return 2 * vec + 2 * qside + 2 * kside + amax + reps + dqa; }
 };
-static BwdWs bwd_ws(int B, int max_sq, long long rows_q, long long rows_k, int H, int Hk, int D) {
+static BwdWs bwd_ws(int B, int max_sq, long long rows_q, long long rows_k, int H, int Hk, int D, bool fdq) {
   const size_t sq_pad = size_t((max_sq + 127) / 128) * 128;
   return BwdWs{al256(size_t(B) * H * sq_pad * 4), al256(size_t(rows_q) * H * D * 2),
                al256(size_t(rows_k) * Hk * D * 2), al256(size_t(B) * Hk * 16),
-               al256(size_t(B) * Hk * AMAX_REPS * 16)};
+               al256(size_t(B) * Hk * AMAX_REPS * 16), fdq ? al256(size_t(rows_q) * H * D * 4) : 0};
 }
 
+// The fused dQ (dK/dV kernel plus TMA reductions of dQ) runs for D = 64 when
+// the caller does not ask for bitwise reproducibility: the reductions' order
+// varies from run to run.
+static bool bwd_fused_dq(int D, int deterministic) { return D == 64 && !deterministic; }
+
 size_t bwd_workspace_bytes(int B, int Sq, int Sk, int H, int Hk, int D, int deterministic) {
-  (void)deterministic;  // every run is deterministic: no cross-CTA reductions
-  return bwd_ws(B, Sq, (long long)B * Sq, (long long)B * Sk, H, Hk, D).total();
+  return bwd_ws(B, Sq, (long long)B * Sq, (long long)B * Sk, H, Hk, D, bwd_fused_dq(D, deterministic)).total();
 }
 
 size_t bwd_varlen_workspace_bytes(int B, int total_q, int total_k, int max_sq, int H, int Hk, int D) {
-  return bwd_ws(B, max_sq, total_q, total_k, H, Hk, D).total();
+  return bwd_ws(B, max_sq, total_q, total_k, H, Hk, D, false).total();
+}
+
+// dQ from the fused dK/dV kernel's fp32 accumulator (already unscaled) to bf16,
+// eight values per thread; n8 = elements / 8.
+__global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float* __restrict__ acc,
+                                                                 __nv_bfloat16* __restrict__ dq, long long n8) {
+  for (long long t = blockIdx.x * 256LL + threadIdx.x; t < n8; t += (long long)gridDim.x * 256) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * t];
+    const float4 c = reinterpret_cast<const float4*>(acc)[2 * t + 1];
+    reinterpret_cast<uint4*>(dq)[t] =
+        make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(c.x, c.y), pack_bf16x2(c.z, c.w));
+  }
 }
 
 template <int D>
 static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, const void* k, const void* v,
                         const void* out, const float* lse, void* dq, void* dk, void* dv, void* ws,
-                        const VarlenArgs* vl, const Dropout* dr, cudaStream_t stream) {
+                        int deterministic, const VarlenArgs* vl, const Dropout* dr, cudaStream_t stream) {
   BwdParams p;
   p.B = s.B;
   p.Sq = s.Sq;
@@ -1368,7 +1481,9 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
   const bool drop = p.drop.thr != 0;
   const long long rows_q = vl ? vl->total_q : (long long)s.B * s.Sq;
   const long long rows_k = vl ? vl->total_k : (long long)s.B * s.Sk;
-  const BwdWs L = bwd_ws(s.B, s.Sq, rows_q, rows_k, s.H, s.Hk, D);
+  // the fused dQ for dense, dropout-free calls (the workspace of those has the accumulator)
+  const bool fdq = bwd_fused_dq(D, deterministic) && !vl && !drop;
+  const BwdWs L = bwd_ws(s.B, s.Sq, rows_q, rows_k, s.H, s.Hk, D, bwd_fused_dq(D, deterministic) && !vl);
   uint8_t* w = static_cast<uint8_t*>(ws);
   p.nl2 = reinterpret_cast<float*>(w);
   p.dvec = reinterpret_cast<float*>(w + L.vec);
@@ -1439,10 +1554,30 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
     fa_bwd_rescale_kernel<D><<<dim3(rx, s.Hk, s.B), 256, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   }
-  auto kv = drop ? fa_bwd_dkdv_kernel<D, true> : fa_bwd_dkdv_kernel<D, false>;
+  const dim3 kv_grid((s.Sk + 127) / 128, s.Hk, s.B);
+  if constexpr (D == 64) {
+    if (fdq) {
+      // dK/dV kernel with the dQ shares added into the zeroed accumulator, then bf16
+      float* dqa = reinterpret_cast<float*>(w + 2 * L.vec + 2 * L.qside + 2 * L.kside + L.amax + L.reps);
+      CUtensorMap mdqa;
+      if (!make_bshd_map_f32(&mdqa, dqa, s.B, s.Sq, s.H, D, 32, 32)) return FA_ERR_CUDA;  // one warp's rows
+      if (cudaMemsetAsync(dqa, 0, size_t(rows_q) * s.H * D * 4, stream) != cudaSuccess) return FA_ERR_CUDA;
+      using CF = KvCfg<D, true>;
+      auto kf = fa_bwd_dkdv_kernel<D, false, true>;
+      if (cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_BYTES) != cudaSuccess)
+        return FA_ERR_CUDA;
+      kf<<<kv_grid, CF::THREADS, CF::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, mdqa, p);
+      if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+      const long long n8 = rows_q * s.H * D / 8;
+      const long long cgrid = std::max(1LL, std::min((long long)device_sm_count() * 8, (n8 + 255) / 256));
+      fa_bwd_dq_convert_kernel<<<unsigned(cgrid), 256, 0, stream>>>(dqa, p.dq, n8);
+      return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    }
+  }
+  auto kv = drop ? fa_bwd_dkdv_kernel<D, true, false> : fa_bwd_dkdv_kernel<D, false, false>;
   if (cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, KvCfg<D>::SMEM_BYTES) != cudaSuccess)
     return FA_ERR_CUDA;
-  kv<<<dim3((s.Sk + 127) / 128, s.Hk, s.B), KvCfg<D>::THREADS, KvCfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
+  kv<<<kv_grid, KvCfg<D>::THREADS, KvCfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, mdo, mq, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   auto dqk = drop ? fa_bwd_dq_kernel<D, true> : fa_bwd_dq_kernel<D, false>;
   if (cudaFuncSetAttribute(dqk, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::SMEM_BYTES) != cudaSuccess)
@@ -1454,12 +1589,13 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
 int bwd_launch(const AttnShape& s, const void* dout, const void* q, const void* k, const void* v, const void* out,
                const float* lse, void* dq, void* dk, void* dv, void* workspace, int deterministic,
                const VarlenArgs* varlen, const Dropout* dropout, cudaStream_t stream) {
-  (void)deterministic;
   switch (s.D) {
     case 64:
-      return launch_bwd_t<64>(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, varlen, dropout, stream);
+      return launch_bwd_t<64>(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, deterministic, varlen, dropout,
+                              stream);
     case 128:
-      return launch_bwd_t<128>(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, varlen, dropout, stream);
+      return launch_bwd_t<128>(s, dout, q, k, v, out, lse, dq, dk, dv, workspace, deterministic, varlen, dropout,
+                               stream);
     default:
       return FA_ERR_UNSUPPORTED;
   }

@@ -73,6 +73,9 @@ bool make_bshd_map(CUtensorMap* map, const void* base, int B, int S, int H, int 
 // (smem rows ordered row-major over (row, head)).
 bool make_bshd_map_box(CUtensorMap* map, const void* base, int B, int S, int H, int D, int box_heads, int box_rows,
                        bool f16 = false);
+// fp32 (B, S, H, D) tensor in boxes of box_cols columns (box_cols * 4 = 128
+// bytes for the 128-byte swizzle) x box_rows rows of one head; for TMA reductions.
+bool make_bshd_map_f32(CUtensorMap* map, const void* base, int B, int S, int H, int D, int box_cols, int box_rows);
 
 // Kernel launchers (return an fa_status value).
 int fwd_launch(const AttnShape& s, const void* q, const void* k, const void* v, void* out, float* lse,

@@ -103,7 +103,9 @@ def test_backward_wait_expires_in_the_dq_kernel(D):
     q, k, v, do = (to_dev(inp[n]) for n in ("q", "k", "v", "dout"))
     out, lse = fa.fa_fwd(q, k, v, causal=True)
     torch.cuda.synchronize()
-    _injected(fa.FA_FAULT_BWD_SKIP_KEY_TILE, lambda: fa.fa_bwd(do, q, k, v, out, lse, causal=True), 0x40)
+    # the two-kernel path (deterministic), whose dQ kernel's producer leaves out the key tile
+    _injected(fa.FA_FAULT_BWD_SKIP_KEY_TILE,
+              lambda: fa.fa_bwd(do, q, k, v, out, lse, causal=True, deterministic=True), 0x40)
     dq, dk, dv = fa.fa_bwd(do, q, k, v, out, lse, causal=True)
     torch.cuda.synchronize()
     st, word = fa.fa_device_status()
