@@ -139,8 +139,9 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* out, float*
  * and L*log2(e) vectors, (B, H, Sq rounded up to 128) fp32 each, fp16
  * copies of q, dout (B, Sq, H, D) and k, v (B, Sk, Hk, D), and the largest
  * magnitudes of q, k, v, dout per (batch, key/value head) group, (B, Hk, 4)
- * uint32 plus 32 replicas of them (B, Hk, 32, 4), each section rounded up to
- * 256 bytes. Returns 0 for arguments fa_bwd would reject.
+ * uint32 plus 32 replicas of them (B, Hk, 32, 4), and with D = 64 and
+ * deterministic == 0 an fp32 dQ accumulator (B, Sq, H, D), each section
+ * rounded up to 256 bytes. Returns 0 for arguments fa_bwd would reject.
  */
 size_t fa_bwd_workspace_size(int B, int Sq, int Sk, int H, int Hk, int D, int deterministic);
 
@@ -151,10 +152,14 @@ size_t fa_bwd_workspace_size(int B, int Sq, int Sk, int H, int Hk, int D, int de
  * (B,Sk,Hk,D) bf16; they are overwritten, not accumulated. With Hk < H the
  * dk and dv of a key/value head are the sums over the query heads sharing
  * it, formed inside one thread block.
- * deterministic: accepted for the page's interface (section "2.4"). Every
- * run is bitwise reproducible in either mode, because no output element is
- * accumulated across thread blocks: one kernel per 128-key tile produces dK
- * and dV, another per 128-row query tile produces dQ.
+ * deterministic (section "2.4": slower, bitwise reproducible): with 1 every
+ * run is bitwise reproducible, because no output element is accumulated
+ * across thread blocks: one kernel per 128-key tile produces dK and dV,
+ * another per 128-row query tile produces dQ. With 0 and D = 64, the dK/dV
+ * kernel also forms dQ and adds each 128-key tile's share into an fp32
+ * accumulator in the workspace: dK and dV are the same bits as with 1, dQ
+ * agrees to within its rounding but the order of its sums varies from run to
+ * run. With 0 at D = 128 the two modes run the same kernels.
  * Precision: the products run on fp16 operands (copies of the inputs, P and
  * dS) with fp32 accumulation. Each (sequence, key/value head) group of q, k,
  * v and dout is copied times a power of two that puts its largest magnitude
