@@ -671,6 +671,8 @@ PROFILE_CASES = {
     "bwd128c": dict(op="bwd", B=4, S=4096, H=16, D=128, causal=True),
     "bwd128": dict(op="bwd", B=4, S=4096, H=16, D=128, causal=False),
     "bwd64": dict(op="bwd", B=4, S=4096, H=32, D=64, causal=False),
+    # the same with deterministic=True: the two-kernel path (dK/dV, then dQ) at D = 64
+    "bwd64d": dict(op="bwd", B=4, S=4096, H=32, D=64, causal=False, deterministic=True),
     # short and long training-sweep points of the backward
     "bwd64_512c": dict(op="bwd", B=32, S=512, H=32, D=64, causal=True),
     "bwd64_16kc": dict(op="bwd", B=1, S=16384, H=32, D=64, causal=True),
@@ -713,9 +715,10 @@ def run_profile(name):
         if c["op"] == "fwd":
             run = lambda: fa.fa_fwd(q, k, v, causal=c["causal"], alibi_slopes=al, out=out, lse=lse)  # noqa: E731
         else:
-            ws = torch.empty(fa.fa_bwd_workspace_size(B, S, S, H, D), dtype=torch.uint8, device=dev)
+            det = c.get("deterministic", False)
+            ws = torch.empty(fa.fa_bwd_workspace_size(B, S, S, H, D, det), dtype=torch.uint8, device=dev)
             run = lambda: fa.fa_bwd(do, q, k, v, out, lse, causal=c["causal"], alibi_slopes=al,  # noqa: E731
-                                    workspace=ws)
+                                    deterministic=det, workspace=ws)
     for _ in range(3):
         run()
     torch.cuda.synchronize()
