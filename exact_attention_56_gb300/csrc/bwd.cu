@@ -858,9 +858,15 @@ __global__ void __launch_bounds__(KvCfg<D, FDQ>::THREADS, 1)
       __syncwarp();
       const float m1 = bars->fac[4], m2 = bars->fac[5];
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<float4*>(stg + lane * 128 + ((c ^ (lane & 7)) * 16)) =
-            make_float4(a[4 * c] * m1 * m2, a[4 * c + 1] * m1 * m2, a[4 * c + 2] * m1 * m2, a[4 * c + 3] * m1 * m2);
+      for (int c = 0; c < 8; ++c) {
+        float4 v;
+        if (m2 == 1.0f) {  // the usual case (|E| <= 100): x * m1 * m2 is x * m1
+          v = make_float4(a[4 * c] * m1, a[4 * c + 1] * m1, a[4 * c + 2] * m1, a[4 * c + 3] * m1);
+        } else {
+          v = make_float4(a[4 * c] * m1 * m2, a[4 * c + 1] * m1 * m2, a[4 * c + 2] * m1 * m2, a[4 * c + 3] * m1 * m2);
+        }
+        *reinterpret_cast<float4*>(stg + lane * 128 + ((c ^ (lane & 7)) * 16)) = v;
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
