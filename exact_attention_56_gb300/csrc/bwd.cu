@@ -533,21 +533,25 @@ struct KvCfg {
   static constexpr int Q_OFF = 2 * TILE_BYTES;
   static constexpr int DO_OFF = Q_OFF + NQ * TILE_BYTES;
   static constexpr int VEC_OFF = DO_OFF + NDO * TILE_BYTES;  // per dO stage: L2[128], D[128]
+  // Compute warpgroups; each owns COLS query columns. Without FDQ, two halve
+  // the per-tile bookkeeping (waits, fences, arrives, addresses) per element
+  // against four: 20% fewer instructions, 1% (D = 64) to 4% (D = 128) faster at
+  // S = 4096. FDQ lengthens each tile's compute chain (dS to shared memory, the
+  // dQ reduction), and four groups hide more of its latency.
+  static constexpr int NCW = FDQ ? 4 : 2;
+  static constexpr int COLS = 128 / NCW;
+  static constexpr int NCT = 128 * NCW;  // compute threads
   // FDQ: dS of the tile as the dQ MMA's A operand (M = 128 queries in two
   // 64-query panels of 128 key rows, MN-major, 128-byte swizzled), and per
-  // compute warp a 32-row x 32-column fp32 staging box for its reduction.
+  // compute warp a 32-row x DQC-column fp32 staging box for its reduction
+  // (group w reduces dQ columns w*DQC .. w*DQC + DQC - 1).
+  static constexpr int DQC = D / NCW;
   static constexpr int DS_OFF = VEC_OFF + NDO * 1024;
   static constexpr int DS_BYTES = FDQ ? 2 * PANEL_BYTES : 0;
   static constexpr int STG_OFF = DS_OFF + DS_BYTES;
-  static constexpr int STG_BYTES = FDQ ? 2 * 128 * 128 : 0;
+  static constexpr int STG_BYTES = FDQ ? NCT * DQC * 4 : 0;
   static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
   static constexpr int SMEM_BYTES = BAR_OFF + 320;
-  // Compute warpgroups; each owns COLS query columns. Two halve the per-tile
-  // bookkeeping (waits, fences, arrives, addresses) per element against four:
-  // 20% fewer instructions, 1% (D = 64) to 4% (D = 128) faster at S = 4096.
-  static constexpr int NCW = 2;
-  static constexpr int COLS = 128 / NCW;
-  static constexpr int NCT = 128 * NCW;  // compute threads
   static constexpr int THREADS = 128 + NCT;
   static constexpr int DO_TX = TILE_BYTES + 1024;
   // TMEM: S^T [0,128) fp32; dP^T of tile ii in buffer ii % NDP at
@@ -561,7 +565,7 @@ struct KvCfg {
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 128 + 128 * NDP, T_DK = T_DV + D, T_DQ = T_DK + D;
   static_assert(T_DK + D + (FDQ ? D : 0) <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert(!FDQ || NCW == 2, "one staging box of 32 dQ columns per compute group");
+  static_assert(!FDQ || DQC == 16 || DQC == 32, "staging rows of 64 or 128 bytes (the map's swizzle span)");
 };
 
 struct KvBars {
@@ -844,33 +848,36 @@ __global__ void __launch_bounds__(KvCfg<D, FDQ>::THREADS, 1)
     // the group's range factors (warp 2): S^T arrives as 2^(eq+ek) S^T
     bool ok = fa_wait_warp(&bars->fac_ready, 0, watch, SITE_KV_FAC);
     const float sl = bars->fac[0];
-    // FDQ: a tile's dQ share (TMEM lanes = query rows; group w takes columns
-    // 32w .. 32w+31), times the unscaling factors, into the warp's staging box
-    // (its 32 rows at 128 bytes each, 16-byte chunk c of row l at c ^ (l & 7): the
-    // 128-byte swizzle of the accumulator's tensor map), then one TMA reduction of
-    // the box into the fp32 accumulator, issued by lane 0. Before the box is
-    // written again, lane 0 waits until its last reduction has read it.
-    uint8_t* stg = smem + C::STG_OFF + w * (128 * 128) + wq * (32 * 128);
+    // FDQ: a tile's dQ share (TMEM lanes = query rows; group w takes DQC
+    // columns from w * DQC), times the unscaling factors, into the warp's staging
+    // box (its 32 rows at DQC * 4 bytes each, swizzled as the accumulator's
+    // tensor map is: 16-byte chunk c of row l at c ^ (l & 7) for 128-byte rows,
+    // c ^ ((l >> 1) & 3) for 64-byte rows), then one TMA reduction of the box into
+    // the fp32 accumulator, issued by lane 0. Before the box is written again,
+    // lane 0 waits until its last reduction has read it.
+    constexpr int RB = C::DQC * 4;  // staging row bytes
+    uint8_t* stg = smem + C::STG_OFF + (w * 4 + wq) * (32 * RB);
+    const int sw = RB == 128 ? (lane & 7) : ((lane >> 1) & 3);
     auto reduce_dq = [&](int hq_t, int i0_t) {
-      float a[32];
-      tmem_ld_cols(tmem + lane_addr + C::T_DQ + uint32_t(w) * 32, a);
+      float a[C::DQC];
+      tmem_ld_cols(tmem + lane_addr + C::T_DQ + uint32_t(w * C::DQC), a);
       if (lane == 0) bulk_wait_group_read0();
       __syncwarp();
       const float m1 = bars->fac[4], m2 = bars->fac[5];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < C::DQC / 4; ++c) {
         float4 v;
         if (m2 == 1.0f) {  // the usual case (|E| <= 100): x * m1 * m2 is x * m1
           v = make_float4(a[4 * c] * m1, a[4 * c + 1] * m1, a[4 * c + 2] * m1, a[4 * c + 3] * m1);
         } else {
           v = make_float4(a[4 * c] * m1 * m2, a[4 * c + 1] * m1 * m2, a[4 * c + 2] * m1 * m2, a[4 * c + 3] * m1 * m2);
         }
-        *reinterpret_cast<float4*>(stg + lane * 128 + ((c ^ (lane & 7)) * 16)) = v;
+        *reinterpret_cast<float4*>(stg + lane * RB + ((c ^ sw) * 16)) = v;
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_reduce_add_4d(&tm_dqa, stg, w * 32, hq_t, i0_t + wq * 32, b);
+        tma_reduce_add_4d(&tm_dqa, stg, w * C::DQC, hq_t, i0_t + wq * 32, b);
         bulk_commit_group();
       }
       __syncwarp();
@@ -999,19 +1006,22 @@ __global__ void __launch_bounds__(KvCfg<D, FDQ>::THREADS, 1)
       mbar_arrive_warp(&bars->pd_ready[pb]);
       if constexpr (FDQ) {
         // The last tile's dQ share is complete (and has read the dS buffer): add it
-        // into the accumulator, then this tile's dS as the dQ MMA's A operand, key
-        // row r of the group's 64-query panel.
+        // into the accumulator, then this tile's dS as the dQ MMA's A operand: key
+        // row r of the 64-query panel holding the group's queries, from 16-byte
+        // chunk (w * COLS % 64) / 8.
         if (ii > 0) {
           if (!(ok = fa_wait_warp(&bars->dq_full, uint32_t(ii - 1) & 1u, watch, SITE_KV_DQ))) break;
           tc_fence_after();
           reduce_dq(hq_prev, i0_prev);
         }
-        uint8_t* ds_row = smem + C::DS_OFF + w * C::PANEL_BYTES + r * 128;
+        uint8_t* ds_row = smem + C::DS_OFF + (w * C::COLS / 64) * C::PANEL_BYTES + r * 128;
+        const int ck0 = (w * C::COLS % 64) / 8;
 #pragma unroll
         for (int ch = 0; ch < C::COLS / 16; ++ch) {
           const uint32_t* v = ds_all + 8 * ch;
-          *reinterpret_cast<uint4*>(ds_row + (((2 * ch) ^ (r & 7)) * 16)) = make_uint4(v[0], v[1], v[2], v[3]);
-          *reinterpret_cast<uint4*>(ds_row + (((2 * ch + 1) ^ (r & 7)) * 16)) = make_uint4(v[4], v[5], v[6], v[7]);
+          *reinterpret_cast<uint4*>(ds_row + (((ck0 + 2 * ch) ^ (r & 7)) * 16)) = make_uint4(v[0], v[1], v[2], v[3]);
+          *reinterpret_cast<uint4*>(ds_row + (((ck0 + 2 * ch + 1) ^ (r & 7)) * 16)) =
+              make_uint4(v[4], v[5], v[6], v[7]);
         }
         fence_proxy_async_smem();  // dS is read by the tensor core next
         tc_fence_before();         // and the share's TMEM columns are rewritten by the next share
@@ -1571,10 +1581,10 @@ static int launch_bwd_t(const AttnShape& s, const void* dout, const void* q, con
     if (fdq) {
       // dK/dV kernel with the dQ shares added into the zeroed accumulator, then bf16
       float* dqa = reinterpret_cast<float*>(w + 2 * L.vec + 2 * L.qside + 2 * L.kside + L.amax + L.reps);
-      CUtensorMap mdqa;
-      if (!make_bshd_map_f32(&mdqa, dqa, s.B, s.Sq, s.H, D, 32, 32)) return FA_ERR_CUDA;  // one warp's rows
-      if (cudaMemsetAsync(dqa, 0, size_t(rows_q) * s.H * D * 4, stream) != cudaSuccess) return FA_ERR_CUDA;
       using CF = KvCfg<D, true>;
+      CUtensorMap mdqa;
+      if (!make_bshd_map_f32(&mdqa, dqa, s.B, s.Sq, s.H, D, CF::DQC, 32)) return FA_ERR_CUDA;  // one warp's box
+      if (cudaMemsetAsync(dqa, 0, size_t(rows_q) * s.H * D * 4, stream) != cudaSuccess) return FA_ERR_CUDA;
       auto kf = fa_bwd_dkdv_kernel<D, false, true>;
       if (cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_BYTES) != cudaSuccess)
         return FA_ERR_CUDA;

@@ -73,8 +73,9 @@ bool make_bshd_map(CUtensorMap* map, const void* base, int B, int S, int H, int 
 // (smem rows ordered row-major over (row, head)).
 bool make_bshd_map_box(CUtensorMap* map, const void* base, int B, int S, int H, int D, int box_heads, int box_rows,
                        bool f16 = false);
-// fp32 (B, S, H, D) tensor in boxes of box_cols columns (box_cols * 4 = 128
-// bytes for the 128-byte swizzle) x box_rows rows of one head; for TMA reductions.
+// fp32 (B, S, H, D) tensor in boxes of box_cols columns x box_rows rows of one
+// head, for TMA reductions; rows of box_cols * 4 = 64 bytes take the 64-byte
+// swizzle, rows of 128 bytes the 128-byte swizzle.
 bool make_bshd_map_f32(CUtensorMap* map, const void* base, int B, int S, int H, int D, int box_cols, int box_rows);
 
 // Kernel launchers (return an fa_status value).
