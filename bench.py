@@ -664,6 +664,7 @@ PROFILE_CASES = {
     # small cases (inputs > L2, < 1 GB on the device) for ncu captures of one kernel group
     "fwd128": dict(op="fwd", B=4, S=4096, H=16, D=128, causal=False),
     "fwd64": dict(op="fwd", B=4, S=4096, H=32, D=64, causal=False),
+    "fwd64c": dict(op="fwd", B=4, S=4096, H=32, D=64, causal=True),
     "fwd128c": dict(op="fwd", B=4, S=4096, H=16, D=128, causal=True),
     "fwd256": dict(op="fwd", B=1, S=8192, H=8, D=256, causal=False),
     # the causal + ALiBi mask variant's shape (geometric slopes)
