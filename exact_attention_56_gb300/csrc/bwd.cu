@@ -582,8 +582,8 @@ struct KvBars {
 };
 static_assert(sizeof(KvBars) <= 320, "barrier block");
 
-// FDQ: tm_dqa maps the fp32 dQ accumulator (B, Sq, H, D) in boxes of 32 columns x
-// 32 rows; otherwise unused.
+// FDQ: tm_dqa maps the fp32 dQ accumulator (B, Sq, H, D) in boxes of DQC columns
+// (one compute group's share of D) x 32 rows, 64-byte swizzled; otherwise unused.
 template <int D, bool DROP, bool FDQ>
 __global__ void __launch_bounds__(KvCfg<D, FDQ>::THREADS, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
